@@ -1,0 +1,378 @@
+"""Plain CPU oracle for paged KV-cache decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` import this package.  It shares no code
+with the CUDA path (``paged_kv_cache_103_gb300``) and never imports it.
+
+Sources, cited by page title and section:
+
+* [P1] "LLM推理优化：vLLM PagedAttention深度解析与工程实践" (lpnh.cn/news/754185):
+  section 二 (attention formula and the per-token KV-size formula),
+  section 3.1 (block table), section 3.2 (BlockManager: free list, allocate,
+  free), section 4.1 (paged K layout).
+* [P2] "vLLM推理加速深度解析：从PagedAttention原理到生产部署实战"
+  (kwkr.cn/news/169259): section 2.2 (workflow: each new token's K/V goes into
+  the physical block the current logical block points to; a full block gets a
+  new free block).
+* [P3] "vLLM 深度拆解：当大模型推理学会「分页注意力」" (chenxutan.com/d/4834.html):
+  section 2.1 (block table diagram), section 3.3 (BlockSpaceManager:
+  append_slot, free, copy-on-write sharing).
+* [P4] "LLM推理优化技术地图：从KV Cache到量化与投机解码" (qwbw.cn/news/280730):
+  section 2.2 (KV size formula 2 x layers x kv_heads x head_dim x seq x batch x
+  bytes), section 2.3 (GQA grouping).
+* [P5] untitled Qwen2.5-7B deployment page (mhpq.cn/news/468822), section 1.2
+  (57344 bytes of KV per token for 28 layers x 4 KV heads x 128 x 2 bytes).
+
+Contents:
+
+* :func:`decode` -- the fp64 attention over a block table (C, ``pa_oracle.c``).
+* :func:`reshape_and_cache` -- the KV append: a plain per-token scatter.
+* :func:`copy_blocks` -- the copy-on-write block copy: plain slice copies.
+* :class:`BlockManagerModel` -- the allocator, restated from [P1] section 3.2
+  and [P3] section 3.3.
+* :func:`kv_bytes_per_token` / :func:`kv_cache_bytes` -- the closed forms.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from collections import deque
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libpa_oracle.so")
+
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.c`` with gcc into ``oracle/_build``.
+
+    ``-ffp-contract=off`` keeps every multiply and add separately rounded, so
+    x86 and Arm hosts produce the same fp64 values.
+    """
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c99",
+                               "-o", tmp, _SRC, "-lpthread", "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.pa_oracle_decode.restype = ctypes.c_int
+        lib.pa_oracle_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64,
+                                         i32, P, i32]
+        lib.pa_oracle_weights.restype = ctypes.c_int
+        lib.pa_oracle_weights.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64, i32,
+                                          i32, i32, P]
+        lib.pa_oracle_to_double.restype = ctypes.c_int
+        lib.pa_oracle_to_double.argtypes = [P, i64, i32, P]
+        _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("expected fp16/bf16 bit patterns as uint16, got %s" % a.dtype)
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def to_double(bits, dtype: int) -> np.ndarray:
+    """Exact fp64 values of fp16 (dtype 0) or bf16 (dtype 1) bit patterns."""
+    x = _u16(bits)
+    y = np.empty(x.shape, dtype=np.float64)
+    rc = _load().pa_oracle_to_double(_ptr(x), x.size, dtype, _ptr(y))
+    if rc:
+        raise ValueError("pa_oracle_to_double failed (%d)" % rc)
+    return y
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, dtype: int,
+           num_threads: int = 1) -> np.ndarray:
+    """fp64 paged decode attention; returns ``out[B, H, d]`` as float64.
+
+    ``q``: uint16 ``[B, H, d]``; caches: uint16 ``[N, bs, Hkv, d]``;
+    ``block_tables``: int32 ``[B, max_blocks]``; ``context_lens``: int32 ``[B]``.
+    Follows [P1] section 二 for the arithmetic, section 3.1 / 4.1 for the table
+    walk and [P4] section 2.3 for the head grouping (see ``pa_oracle.c``).
+    """
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    tbl = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, H, d = q.shape
+    N, bs, Hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or lens.shape != (B,) or tbl.shape[0] != B:
+        raise ValueError("shape mismatch")
+    out = np.empty((B, H, d), dtype=np.float64)
+    rc = _load().pa_oracle_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(tbl), tbl.shape[1],
+                                  _ptr(lens), B, H, Hkv, d, bs, N, float(scale), dtype, _ptr(out),
+                                  int(num_threads))
+    if rc:
+        raise ValueError("pa_oracle_decode failed (%d)" % rc)
+    return out
+
+
+def weights(q, k_cache, block_tables, context_lens, scale: float, dtype: int, i: int,
+            h: int) -> np.ndarray:
+    """The softmax weights of one (sequence, query head), fp64."""
+    q, k_cache = _u16(q), _u16(k_cache)
+    tbl = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    w = np.empty(max(int(lens[i]), 1), dtype=np.float64)
+    rc = _load().pa_oracle_weights(_ptr(q), _ptr(k_cache), _ptr(tbl), tbl.shape[1], _ptr(lens), B,
+                                   H, Hkv, d, bs, N, float(scale), dtype, i, h, _ptr(w))
+    if rc:
+        raise ValueError("pa_oracle_weights failed (%d)" % rc)
+    return w[: int(lens[i])]
+
+
+def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache) -> None:
+    """The KV append, in place: token t goes to ``cache[s // bs, s % bs]``.
+
+    [P2] section 2.2: each generated token's K/V is stored into the physical
+    block the current logical block points to.  The slot of a token is
+    ``physical_block * block_size + offset`` (a reading: the pages give no
+    formula).  A negative slot marks padding and is skipped.
+    """
+    bs = k_cache.shape[1]
+    for t in range(k_new.shape[0]):
+        s = int(slot_mapping[t])
+        if s < 0:
+            continue
+        k_cache[s // bs, s % bs] = k_new[t]
+        v_cache[s // bs, s % bs] = v_new[t]
+
+
+def copy_blocks(k_caches, v_caches, pairs) -> None:
+    """Copy-on-write block copies, in place, for every layer's cache.
+
+    [P3] section 3.3: a shared block is copied only when a sharer must write
+    into it.  ``pairs`` is a sequence of (src, dst) physical block ids.
+    """
+    for kc, vc in zip(k_caches, v_caches):
+        for src, dst in pairs:
+            kc[int(dst)] = kc[int(src)]
+            vc[int(dst)] = vc[int(src)]
+
+
+def kv_bytes_per_token(num_layers: int, kv_heads: int, head_dim: int, dtype_bytes: int) -> int:
+    """[P4] section 2.2 / [P5] section 1.2: 2 (K and V) x layers x KV heads x
+    head dim x element bytes.  For MHA, kv_heads x head_dim is d_model ([P1]
+    section 二)."""
+    return 2 * num_layers * kv_heads * head_dim * dtype_bytes
+
+
+def kv_cache_bytes(num_layers: int, kv_heads: int, head_dim: int, seq_len: int, batch: int,
+                   dtype_bytes: int) -> int:
+    """[P4] section 2.2: the per-token size times sequence length times batch."""
+    return kv_bytes_per_token(num_layers, kv_heads, head_dim, dtype_bytes) * seq_len * batch
+
+
+class OracleOOM(Exception):
+    """Raised when the free list cannot cover a request ([P1] section 3.2)."""
+
+
+class OracleInvalid(Exception):
+    """Raised for an operation on an unknown / duplicate sequence."""
+
+
+class BlockManagerModel:
+    """The block allocator, restated from the pages.
+
+    [P1] section 3.2: the free list starts as the block ids in order, a block is
+    taken from the FRONT of the free list and a freed block is put at the BACK,
+    in the order of the sequence's table; ``allocate(seq, num_tokens)`` gives a
+    sequence enough blocks to hold ``num_tokens`` tokens, checking the free
+    list before taking anything (all or nothing).  [P3] section 3.3:
+    ``append_slot`` writes into the current last block if it has room, else
+    takes a new block; sharing is by reference, and a shared block is copied
+    only when a sharer writes into it (copy-on-write).
+
+    Readings where the pages are silent: ``init_free_order`` replaces the
+    initial ``0..N-1`` order (random placement is a permutation); a shared
+    block carries a reference count and returns to the free list when it
+    drops to zero; ``fork`` copies the parent's table and raises the counts;
+    a sequence that writes into a shared, partially filled last block takes a
+    new block from the front of the free list, the pair (old, new) is reported
+    for a copy and the old block's count drops by one -- the last sharer left
+    writes in place.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, init_free_order=None):
+        if num_blocks < 0 or block_size <= 0:
+            raise OracleInvalid("bad pool")
+        order = list(range(num_blocks)) if init_free_order is None else [int(b) for b in init_free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise OracleInvalid("init_free_order must be a permutation of 0..N-1")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free_blocks = deque(order)
+        self.allocated: dict[int, list[int]] = {}
+        self.lens: dict[int, int] = {}
+        self.ref = [0] * num_blocks
+
+    # -- [P1] section 3.2 -------------------------------------------------
+    def allocate(self, seq_id: int, num_tokens: int) -> None:
+        if num_tokens < 0:
+            raise OracleInvalid("negative token count")
+        table = self.allocated.get(seq_id, [])
+        cur_len = self.lens.get(seq_id, 0)
+        already_used = len(table) * self.block_size
+        if (num_tokens > cur_len and cur_len % self.block_size != 0 and table
+                and self.ref[table[-1]] > 1):
+            raise OracleInvalid("growing into a shared partial block needs append_slot")
+        if already_used < num_tokens:
+            need = math.ceil((num_tokens - already_used) / self.block_size)
+            if len(self.free_blocks) < need:
+                raise OracleOOM("need %d blocks, %d free" % (need, len(self.free_blocks)))
+            for _ in range(need):
+                b = self.free_blocks.popleft()
+                self.ref[b] = 1
+                table.append(b)
+        self.allocated[seq_id] = table
+        self.lens[seq_id] = max(cur_len, num_tokens)
+
+    def free(self, seq_id: int) -> None:
+        if seq_id not in self.allocated:
+            raise OracleInvalid("unknown sequence")
+        for b in self.allocated[seq_id]:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free_blocks.append(b)
+        del self.allocated[seq_id]
+        del self.lens[seq_id]
+
+    # -- [P3] section 3.3 -------------------------------------------------
+    def _blocks_needed_for_append(self, seq_id: int, ref_view) -> int:
+        pos = self.lens[seq_id]
+        table = self.allocated[seq_id]
+        if pos == len(table) * self.block_size:
+            return 1
+        return 1 if ref_view(table[pos // self.block_size]) > 1 else 0
+
+    def append_slot(self, seq_id: int):
+        """Reserve the slot of the sequence's next token.
+
+        Returns ``(slot, cow)`` where ``cow`` is ``None`` or ``(src, dst)``.
+        """
+        if seq_id not in self.allocated:
+            raise OracleInvalid("unknown sequence")
+        if self._blocks_needed_for_append(seq_id, lambda b: self.ref[b]) > len(self.free_blocks):
+            raise OracleOOM("no free block")
+        return self._append_unchecked(seq_id)
+
+    def _append_unchecked(self, seq_id: int):
+        bs = self.block_size
+        table = self.allocated[seq_id]
+        pos = self.lens[seq_id]
+        cow = None
+        if pos == len(table) * bs:
+            b = self.free_blocks.popleft()
+            self.ref[b] = 1
+            table.append(b)
+        else:
+            last = table[pos // bs]
+            if self.ref[last] > 1:
+                new = self.free_blocks.popleft()
+                self.ref[last] -= 1
+                self.ref[new] = 1
+                table[pos // bs] = new
+                cow = (last, new)
+        self.lens[seq_id] = pos + 1
+        slot = table[pos // bs] * bs + pos % bs
+        return slot, cow
+
+    def append_batch(self, seq_ids):
+        """One new token for each sequence of a decode batch, all or nothing.
+
+        Sequences are served in the given order (so with k sharers of one
+        partial block in the batch, the first k-1 copy it and the last writes
+        in place).  Returns ``(slots, cow_pairs)``.
+        """
+        seq_ids = [int(s) for s in seq_ids]
+        if len(set(seq_ids)) != len(seq_ids):
+            raise OracleInvalid("duplicate sequence in batch")
+        for s in seq_ids:
+            if s not in self.allocated:
+                raise OracleInvalid("unknown sequence")
+        # count the blocks the whole batch takes, with the counts it changes
+        delta: dict[int, int] = {}
+        need = 0
+        for s in seq_ids:
+            n = self._blocks_needed_for_append(s, lambda b: self.ref[b] + delta.get(b, 0))
+            pos = self.lens[s]
+            table = self.allocated[s]
+            if n and pos != len(table) * self.block_size:
+                last = table[pos // self.block_size]
+                delta[last] = delta.get(last, 0) - 1
+            need += n
+        if need > len(self.free_blocks):
+            raise OracleOOM("batch needs %d blocks, %d free" % (need, len(self.free_blocks)))
+        slots, pairs = [], []
+        for s in seq_ids:
+            slot, cow = self._append_unchecked(s)
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(cow)
+        return slots, pairs
+
+    def fork(self, parent: int, child: int) -> None:
+        """[P4] section 3.3 / [P3] section 3.3: the child shares the parent's
+        blocks; only the table is copied."""
+        if parent not in self.allocated or child in self.allocated:
+            raise OracleInvalid("bad fork")
+        table = list(self.allocated[parent])
+        for b in table:
+            self.ref[b] += 1
+        self.allocated[child] = table
+        self.lens[child] = self.lens[parent]
+
+    # -- exports ------------------------------------------------------------
+    def slot_of(self, seq_id: int, pos: int) -> int:
+        table = self.allocated[seq_id]
+        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def export(self, seq_ids, max_blocks: int | None = None):
+        """``(block_tables [B, max_blocks] int32 padded with -1, context_lens [B] int32)``."""
+        seq_ids = [int(s) for s in seq_ids]
+        if max_blocks is None:
+            max_blocks = max([len(self.allocated[s]) for s in seq_ids] + [1])
+        tbl = np.full((len(seq_ids), max_blocks), -1, dtype=np.int32)
+        lens = np.zeros(len(seq_ids), dtype=np.int32)
+        for r, s in enumerate(seq_ids):
+            t = self.allocated[s]
+            if len(t) > max_blocks:
+                raise OracleInvalid("table wider than max_blocks")
+            tbl[r, : len(t)] = t
+            lens[r] = self.lens[s]
+        return tbl, lens
+
+    def stats(self) -> dict:
+        used = sum(1 for r in self.ref if r > 0)
+        shared = sum(1 for r in self.ref if r > 1)
+        return {"num_blocks": self.num_blocks, "free_blocks": len(self.free_blocks),
+                "used_blocks": used, "shared_blocks": shared, "num_seqs": len(self.allocated),
+                "num_tokens": sum(self.lens.values())}
