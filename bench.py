@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode layer-step on a GB300.
+
+Workload: the LLaMA-13B-shaped MHA decode batch -- 64 sequences, 40 query
+heads = 40 KV heads of 128, fp16, block size 16, context lengths uniform in
+[128, 2048], blocks scattered over a pool of 1.25x the need.  A step is the
+whole hot path over the batch: the KV append of each sequence's new token
+(pa_reshape_and_cache) and the decode attention over its context (pa_decode);
+the e2e leg adds the host allocator step (pa_append_batch + pa_export), the
+host->device copies of that step's inputs from pinned memory and the
+device->host copy of the output.
+
+The metric is KV-cache bytes attended per second (GB/s): the K and V bytes of
+every context token, divided by the step time.  One JSON line is printed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV GB/s (% of GB300 HBM peak); decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kv_bytes(lens, Hkv, d, e=2):
+    return 2 * int(sum(int(n) for n in lens)) * Hkv * d * e
+
+
+def algorithmic_bytes(lens, B, H, Hkv, d, bs, e=2):
+    """Bytes pa_decode must move: K and V of every context token, Q and the
+    output, the used table entries and the lengths."""
+    table = sum((int(n) + bs - 1) // bs for n in lens) * 4
+    return kv_bytes(lens, Hkv, d, e) + 2 * B * H * d * e + table + 4 * B
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(name):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
+    workload, or None if the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", name)
+    src = os.path.join(ROOT, "paged_kv_cache_103_gb300", "csrc", "pa_decode.cu")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith(" "):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if fields.get("pa_decode.cu sha256[:16]") != sha:
+            return None
+        return int(float(fields["dram bytes per launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "timed region"
+        if not inside:   # region shorter than the sampling period: nearest samples
+            inside = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+            note = "within 250 ms of the timed region"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+                for n, v in zip(names, s[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm), "window": note}
+
+
+def setup_workload(args):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+    from paged_kv_cache_103_gb300 import workloads as wl
+
+    w = wl.llama13b(B=args.batch)
+    host = wl.qkv(w)
+    alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
+    for i in range(w.B):
+        alloc.alloc(i, int(w.context_lens[i]) - 1)
+    slots, pairs = alloc.append_batch(list(range(w.B)))
+    assert len(pairs) == 0
+    max_blocks = int(math.ceil((int(w.context_lens.max()) + args.e2e_extra) / w.block_size)) + 1
+    tbl, lens = alloc.export(list(range(w.B)), max_blocks)
+    return w, host, alloc, slots, tbl, lens, max_blocks
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+    from paged_kv_cache_103_gb300 import build as pa_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pa_build.build()
+    binding.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    w, host, alloc, slots, tbl, lens, max_blocks = setup_workload(args)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        q = host["q"].to(dev)
+        kc = host["k_cache"].to(dev)
+        vc = host["v_cache"].to(dev)
+        kn = host["k_new"].to(dev)
+        vn = host["v_new"].to(dev)
+        slots_d = torch.from_numpy(slots).to(dev)
+        tbl_d = torch.from_numpy(tbl).to(dev)
+        lens_d = torch.from_numpy(lens).to(dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(binding.pa_decode_workspace_size(w.B, w.H, w.d), dtype=torch.uint8,
+                         device=dev)
+        binding.pa_decode_workspace_init(ws, stream)
+    stream.synchronize()
+    max_len = int(lens.max())
+
+    def step():
+        binding.pa_reshape_and_cache(kn, vn, slots_d, kc, vc, stream)
+        binding.pa_decode(q, kc, vc, tbl_d, lens_d, max_len, w.scale, out, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    if binding.pa_check_device_errors(stream):
+        raise RuntimeError("device error flags set during warm-up")
+
+    # ---- device-timed leg: inputs resident in HBM (1.43 GB of KV > L2)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 2)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev[0].record(stream)
+    for k in range(K):
+        binding.pa_reshape_and_cache(kn, vn, slots_d, kc, vc, stream)
+        ev[1 + 2 * k].record(stream)
+        binding.pa_decode(q, kc, vc, tbl_d, lens_d, max_len, w.scale, out, ws, stream)
+        ev[2 + 2 * k].record(stream)
+    ev[-1].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    decode_ms = [ev[1 + 2 * k].elapsed_time(ev[2 + 2 * k]) for k in range(K)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if sampler:
+        sampler.stop()
+    flags = binding.pa_check_device_errors(stream)
+    if flags:
+        raise RuntimeError("device error flags 0x%x in the timed region" % flags)
+
+    ms_per_step = total_ms / K
+    kvb = kv_bytes(lens, w.Hkv, w.d)
+    value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    alg = algorithmic_bytes(lens, w.B, w.H, w.Hkv, w.d, w.block_size)
+    dec_avg_ms = sum(decode_ms) / len(decode_ms)
+    achieved = alg / (dec_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = load_peak()
+
+    # ---- e2e leg through the C ABI: host allocator step, pinned H2D, kernels, D2H
+    e2e = run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, uniform context lengths, random block placement)",
+        "config": {"workload": "llama13b_mha_decode_layer_step", "batch": w.B,
+                   "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
+                   "block_size": w.block_size, "context_lens": "uniform[128,2048]",
+                   "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
+                   "l2": "inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9)},
+        "pct_of_hbm_peak": round(100 * value / peak, 1),
+        "tokens_per_s": round(w.B / (ms_per_step * 1e-3 * w.layers), 1),
+        "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "roofline": {"kernel": "pa_decode", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                     if peak_kind == "measured" else "fallback",
+                     "traffic": recorded_traffic("pa_decode_llama13b.txt"),
+                     "algorithmic_bytes_per_launch": alg,
+                     "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result))
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks):
+    """Real decode steps through the C ABI with host buffers: each step appends
+    one token per sequence in the host allocator, exports the tables into
+    pinned memory, copies them and the step's q / new K / new V to the device,
+    runs the append and the decode, and reads the output back."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+
+    steps = min(args.steps, args.e2e_extra)
+    B, H, Hkv, d = w.B, w.H, w.Hkv, w.d
+    pin = dict(pin_memory=True)
+    h_q = host["q"].clone().pin_memory()
+    h_kn = host["k_new"].clone().pin_memory()
+    h_vn = host["v_new"].clone().pin_memory()
+    h_tbl = torch.empty((B, max_blocks), dtype=torch.int32, **pin)
+    h_lens = torch.empty(B, dtype=torch.int32, **pin)
+    h_slots = torch.empty(B, dtype=torch.int64, **pin)
+    h_pairs = torch.empty((B, 2), dtype=torch.int32, **pin)
+    h_out = torch.empty_like(h_q, **pin)
+    d_q = torch.empty_like(q)
+    d_kn = torch.empty((B, Hkv, d), dtype=q.dtype, device=dev)
+    d_vn = torch.empty_like(d_kn)
+    d_tbl = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
+    d_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    d_slots = torch.empty(B, dtype=torch.int64, device=dev)
+    d_pairs = torch.empty((B, 2), dtype=torch.int32, device=dev)
+    d_out = torch.empty_like(q)
+    ids = list(range(B))
+    n_tbl, n_lens, n_slots, n_pairs = (h_tbl.numpy(), h_lens.numpy(), h_slots.numpy(),
+                                      h_pairs.numpy())
+    h2d = d2h = 0
+    kv_total = 0
+    launches = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _, pairs = alloc.append_batch(ids, n_slots, n_pairs)
+        alloc.export(ids, max_blocks, n_tbl, n_lens)
+        with torch.cuda.stream(stream):
+            for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tbl, h_tbl),
+                             (d_lens, h_lens), (d_slots, h_slots)):
+                dst.copy_(src, non_blocking=True)
+                h2d += src.numel() * src.element_size()
+            if len(pairs):
+                d_pairs[: len(pairs)].copy_(h_pairs[: len(pairs)], non_blocking=True)
+                h2d += len(pairs) * 8
+                binding.pa_copy_blocks([kc], [vc], d_pairs[: len(pairs)], stream)
+                launches += 1
+            binding.pa_reshape_and_cache(d_kn, d_vn, d_slots, kc, vc, stream)
+            binding.pa_decode(d_q, kc, vc, d_tbl, d_lens, int(n_lens.max()), w.scale, d_out, ws,
+                              stream)
+            launches += 2
+            h_out.copy_(d_out, non_blocking=True)
+            d2h += d_out.numel() * d_out.element_size()
+        stream.synchronize()
+        kv_total += kv_bytes(n_lens, Hkv, d)
+    t1 = time.perf_counter()
+    if binding.pa_check_device_errors(stream):
+        raise RuntimeError("device error flags set in the e2e leg")
+    return {"value": round(kv_total / (t1 - t0) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "steps": steps, "ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
+            "gpu_launches": launches,
+            "includes": "host append_batch + export, pinned H2D of q/k_new/v_new/tables/lens/"
+                        "slots, reshape_and_cache, decode, D2H of out, stream sync per step"}
+
+
+def oracle_sample_run(w, host, tbl, lens, seqs, threads):
+    """Runs the oracle on the sequences `seqs` (cache taken as it stands)."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_103_gb300 import workloads as wl
+
+    sel = np.asarray(seqs)
+    q = wl.bits(host["q"])[sel]
+    return oracle.decode(q, wl.bits(host["k_cache"]), wl.bits(host["v_cache"]), tbl[sel],
+                         lens[sel], w.scale, oracle.DTYPE_F16, num_threads=threads)
+
+
+def cpu_baseline(w, host, tbl, lens, seconds):
+    """The oracle on the host cores over a bounded sample of the same batch:
+    the first k sequences, k chosen from a one-sequence calibration so the
+    sample takes about `seconds`."""
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle_sample_run(w, host, tbl, lens, [0], 1)
+    one = max(time.perf_counter() - t0, 1e-3) / max(int(lens[0]), 1)   # s per token, 1 thread
+    per_seq = one * float(lens.mean()) / threads
+    k = int(max(threads, min(w.B, seconds / max(per_seq, 1e-6))))
+    k = min(k, w.B)
+    seqs = list(range(k))
+    t0 = time.perf_counter()
+    oracle_sample_run(w, host, tbl, lens, seqs, threads)
+    dt = time.perf_counter() - t0
+    kvb = kv_bytes(lens[:k], w.Hkv, w.d)
+    return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "first %d of %d sequences of the same batch (%d context tokens), all "
+                      "heads, fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()),
+                                                             threads)}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, on the host cores."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    oracle.build()
+    from paged_kv_cache_103_gb300 import workloads as wl
+    import numpy as np
+
+    w = wl.llama13b(B=args.batch)
+    host = wl.qkv(w)
+    m = oracle.BlockManagerModel(w.num_blocks, w.block_size, w.free_order)
+    for i in range(w.B):
+        m.allocate(i, int(w.context_lens[i]) - 1)
+    slots, _ = m.append_batch(range(w.B))
+    oracle.reshape_and_cache(host["k_new"], host["v_new"], slots, host["k_cache"],
+                             host["v_cache"])
+    tbl, lens = m.export(range(w.B))
+    threads = os.cpu_count() or 1
+    # each step: a bounded sample of sequences, sized to about `ref_step_seconds`
+    t0 = time.perf_counter()
+    oracle_sample_run(w, host, tbl, lens, [0], 1)
+    one = max(time.perf_counter() - t0, 1e-3)   # one sequence on one thread
+    k = int(max(1, min(w.B, threads * args.ref_step_seconds / one)))
+    seqs = list(range(k))
+    for _ in range(args.warmup):
+        oracle_sample_run(w, host, tbl, lens, seqs[:1], threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_run(w, host, tbl, lens, seqs, threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = kv_bytes(lens[:k], w.Hkv, w.d) / dt / 1e9
+    sample = ("first %d of %d sequences of the batch per step (%d context tokens), all heads, "
+              "fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()), threads))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Q/K/V, uniform context lengths, random block placement)",
+        "config": {"workload": "llama13b_mha_decode_layer_step", "batch": w.B, "q_heads": w.H,
+                   "kv_heads": w.Hkv, "head_dim": w.d, "block_size": w.block_size,
+                   "context_lens": "uniform[128,2048]"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--e2e-extra", type=int, default=64,
+                    help="e2e steps (each appends a token to every sequence)")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

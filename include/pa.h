@@ -1,0 +1,238 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode library.
+ *
+ * The operations follow five web pages on vLLM's PagedAttention, cited by
+ * title and section:
+ *   [P1] "LLM推理优化：vLLM PagedAttention深度解析与工程实践" (lpnh.cn/news/754185)
+ *   [P2] "vLLM推理加速深度解析：从PagedAttention原理到生产部署实战" (kwkr.cn/news/169259)
+ *   [P3] "vLLM 深度拆解：当大模型推理学会「分页注意力」——PagedAttention、连续批处理与
+ *        V1 引擎如何重写 GPU 推理服务的心智模型" (chenxutan.com/d/4834.html)
+ *   [P4] "LLM推理优化技术地图：从KV Cache到量化与投机解码" (qwbw.cn/news/280730)
+ *
+ * Conventions
+ *   - Every call returns a pa_status; nothing throws across the ABI.
+ *   - Host pointers are marked (host), device pointers (device).  The caller
+ *     owns every buffer; the library allocates no device memory.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronise.  Errors found by a kernel
+ *     (a block id outside the pool, a slot outside the cache, a context longer
+ *     than its table row) set bits in a per-device error word; the offending
+ *     access is skipped, never performed.  pa_check_device_errors() reads and
+ *     clears that word.
+ *   - KV cache layout ([P1] section 4.1): one K and one V tensor per layer,
+ *     each [num_blocks][block_size][num_kv_heads][head_dim], row-major,
+ *     16-byte aligned.  A token's slot is physical_block * block_size +
+ *     offset_in_block.
+ *   - Supported shapes: head_dim 64 or 128; block_size 8, 16 or 32;
+ *     num_heads % num_kv_heads == 0 with at most 16 query heads per KV head;
+ *     fp16 or bf16 elements.  Other shapes return PA_ERR_UNSUPPORTED.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* bad argument or an operation the state forbids */
+    PA_ERR_OOM = 2,          /* the free block list cannot cover the request */
+    PA_ERR_NOT_FOUND = 3,    /* unknown sequence id */
+    PA_ERR_BOUNDS = 4,       /* a kernel met an index outside its buffers */
+    PA_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+    PA_ERR_UNSUPPORTED = 6,  /* shape or dtype outside the supported set */
+    PA_ERR_TIMEOUT = 7       /* a kernel's bounded wait ran out */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device error word (pa_check_device_errors). */
+#define PA_DEVERR_BLOCK_ID 0x1u     /* table entry < 0 or >= num_blocks */
+#define PA_DEVERR_TABLE_WIDTH 0x2u  /* context_len needs more blocks than max_blocks */
+#define PA_DEVERR_SLOT 0x4u         /* slot >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT 0x8u      /* a bounded pipeline wait gave up */
+#define PA_DEVERR_PAIR 0x10u        /* copy pair outside the pool */
+#define PA_DEVERR_CONTEXT 0x20u     /* negative context length */
+
+PA_API const char* pa_status_str(pa_status s);
+PA_API int32_t pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator.  [P1] section 3.2 (BlockManager): the free list starts
+ * in block order (or in the caller's order), blocks are taken from its front
+ * and returned to its back in table order, and an allocation checks the free
+ * list before taking anything.  [P3] section 3.3 (BlockSpaceManager):
+ * append_slot writes into the last block while it has room and takes a new
+ * block when it is full; free returns all blocks; sequences with the same
+ * prefix share physical blocks, and a shared block is copied only when a
+ * sharer writes into it (copy-on-write).  [P2] section 2.2 gives the same
+ * workflow.  Shared blocks carry a reference count; a block returns to the
+ * free list when its count reaches zero.
+ *
+ * A pa_allocator is host-only and not thread-safe; the caller owns it
+ * (create/destroy).  Sequence ids are arbitrary int64 keys.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_allocator pa_allocator;
+
+typedef struct pa_alloc_stats {
+    int32_t num_blocks;     /* pool size */
+    int32_t block_size;     /* tokens per block */
+    int32_t free_blocks;    /* blocks on the free list */
+    int32_t used_blocks;    /* blocks with reference count >= 1 */
+    int32_t shared_blocks;  /* blocks with reference count >= 2 */
+    int32_t num_seqs;       /* live sequences */
+    int64_t num_tokens;     /* sum of the live sequences' lengths */
+} pa_alloc_stats;
+
+/* Creates a pool of num_blocks blocks of block_size tokens.  init_free_order
+ * (host, num_blocks int32, nullable) is the initial free list and must be a
+ * permutation of 0..num_blocks-1; NULL means 0..num_blocks-1. */
+PA_API pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size,
+                                 const int32_t* init_free_order, pa_allocator** out);
+PA_API void pa_alloc_destroy(pa_allocator* a);
+
+/* [P1] section 3.2 allocate(seq_id, num_tokens): grows the sequence (creating
+ * it if new) so that its blocks hold num_tokens tokens, taking
+ * ceil((num_tokens - held_slots) / block_size) blocks from the front of the
+ * free list; the sequence's length becomes max(length, num_tokens).  All or
+ * nothing: PA_ERR_OOM leaves every state unchanged.  Growing a sequence whose
+ * partially filled last block is shared returns PA_ERR_INVALID (use
+ * pa_append_slot, which copies on write). */
+PA_API pa_status pa_alloc(pa_allocator* a, int64_t seq_id, int32_t num_tokens);
+
+/* [P3] section 3.3 append_slot(): reserves the slot of the sequence's next
+ * token (position = current length) and returns it in *slot_out (host).  If
+ * that position opens a new block, a block is taken from the front of the free
+ * list.  If it falls in a partially filled block shared with other sequences,
+ * a new block is taken, the sequence's table points to it, the old block's
+ * count drops by one, and (*cow_src, *cow_dst) name the copy the caller must
+ * make (pa_copy_blocks) before writing the token; otherwise both are -1.
+ * cow_src / cow_dst may be NULL.  PA_ERR_OOM leaves state unchanged. */
+PA_API pa_status pa_append_slot(pa_allocator* a, int64_t seq_id, int64_t* slot_out,
+                                int32_t* cow_src, int32_t* cow_dst);
+
+/* One decode step's appends: pa_append_slot for seq_ids[0..B) in that order,
+ * all or nothing.  slot_mapping (host, B int64) receives each new token's
+ * slot, cow_pairs (host, capacity B pairs of int32 {src, dst}) the copies to
+ * make, *num_cow their count.  Duplicate ids return PA_ERR_INVALID. */
+PA_API pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t B,
+                                 int64_t* slot_mapping, int32_t* cow_pairs, int32_t* num_cow);
+
+/* Shares parent's blocks with a new sequence child: the table is copied and
+ * every block's count rises by one; no KV data moves ([P4] section 3.3, [P3]
+ * section 3.3). */
+PA_API pa_status pa_fork(pa_allocator* a, int64_t parent, int64_t child);
+
+/* [P1] section 3.2 free(seq_id): drops the sequence; each block's count
+ * falls by one and blocks reaching zero go to the back of the free list in
+ * table order. */
+PA_API pa_status pa_free(pa_allocator* a, int64_t seq_id);
+
+/* Fills block_tables (host, [B][max_blocks] int32, unused entries -1) and
+ * context_lens (host, [B] int32) for seq_ids[0..B).  A table longer than
+ * max_blocks returns PA_ERR_INVALID. */
+PA_API pa_status pa_export(const pa_allocator* a, const int64_t* seq_ids, int32_t B,
+                           int32_t max_blocks, int32_t* block_tables, int32_t* context_lens);
+
+/* Slots (host, count int64) of token positions [start, start+count) of a
+ * sequence, e.g. to write a prompt's K/V with pa_reshape_and_cache. */
+PA_API pa_status pa_seq_slots(const pa_allocator* a, int64_t seq_id, int32_t start,
+                              int32_t count, int64_t* slots);
+PA_API pa_status pa_seq_info(const pa_allocator* a, int64_t seq_id, int32_t* length,
+                             int32_t* num_table_blocks);
+PA_API pa_status pa_block_ref(const pa_allocator* a, int32_t block, int32_t* ref);
+/* Copies the free list, front first, into out (host, capacity cap). */
+PA_API pa_status pa_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
+PA_API pa_status pa_alloc_stats_get(const pa_allocator* a, pa_alloc_stats* out);
+
+/* ------------------------------------------------------------------------
+ * Device operations.
+ * ---------------------------------------------------------------------- */
+
+/* KV append ([P2] section 2.2: each generated token's K/V is stored in the
+ * physical block its current logical block points to; [P3] section 3.3).
+ * For t in [0, T): if slot_mapping[t] >= 0,
+ *   k_cache[slot / block_size][slot % block_size][h][:] = k_new[t][h][:]
+ * and the same for V, for every KV head h.  A negative slot is padding and is
+ * skipped.  A slot >= num_blocks * block_size is skipped and sets
+ * PA_DEVERR_SLOT.  Bit-exact copy.
+ *   k_new, v_new   (device) [T][Hkv][d] fp16/bf16
+ *   slot_mapping   (device) [T] int64
+ *   k_cache, v_cache (device) [num_blocks][block_size][Hkv][d], updated in place */
+PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                      void* v_cache, int32_t num_blocks, int32_t block_size,
+                                      int32_t Hkv, int32_t d, pa_dtype dtype, void* stream);
+
+/* Copy-on-write block copies ([P3] section 3.3): for every layer l and pair p,
+ * block pairs[p][1] of k_caches[l] and v_caches[l] becomes a bit copy of
+ * block pairs[p][0].  block_bytes = block_size * Hkv * d * element size and
+ * must be a multiple of 16.  A pair outside [0, num_blocks) is skipped and
+ * sets PA_DEVERR_PAIR.  Destinations must be distinct and must not be sources.
+ *   k_caches, v_caches (host) arrays of num_layers device pointers
+ *   pairs              (device) [num_pairs][2] int32 {src, dst} */
+PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
+                                int32_t num_layers, const int32_t* pairs, int32_t num_pairs,
+                                int64_t block_bytes, int32_t num_blocks, void* stream);
+
+/* Bytes of workspace pa_decode needs for batch B, H query heads and head dim
+ * d; 0 for unsupported sizes.  The workspace holds per-(sequence, KV head)
+ * arrival counters and per-CTA partial results of split contexts. */
+PA_API size_t pa_decode_workspace_size(int32_t B, int32_t H, int32_t d);
+
+/* Zeroes a workspace (async on stream).  Call once after allocating it; every
+ * pa_decode call leaves the counters at zero again.  A workspace serves one
+ * stream at a time: pa_decode calls that overlap on the GPU must not share one. */
+PA_API pa_status pa_decode_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Paged decode attention ([P1] section 二: attn = softmax(Q K^T / sqrt(d)) V;
+ * [P3] section 1.1: the new token's query attends to every cached K/V;
+ * [P1] sections 3.1 and 4.1, [P3] section 2.1: K/V reached through the block
+ * table; [P4] section 2.3: query heads grouped, G = H / Hkv heads per KV head,
+ * query head h reads KV head h / G).  For each sequence i with
+ * n = context_lens[i] and query head h:
+ *   s_j = scale * q[i][h] . K_j,  K_j = k_cache[block_tables[i][j / bs]][j % bs][h / G]
+ *   out[i][h] = sum_j softmax(s)_j V_j       over j in [0, n)
+ * with fp32 accumulation, rounded once to the output dtype; n == 0 gives a
+ * zero row.  The caller passes scale (1/sqrt(d) for the pages' formula).
+ *   q            (device) [B][H][d]
+ *   k_cache, v_cache (device) [num_blocks][block_size][Hkv][d]
+ *   block_tables (device) [B][max_blocks] int32
+ *   context_lens (device) [B] int32, each <= max_context_len
+ *   max_context_len (host) an upper bound of context_lens (sizes the split)
+ *   out          (device) [B][H][d], same dtype as q
+ *   workspace    (device) >= pa_decode_workspace_size(B, H, d) bytes, zeroed
+ *                once by pa_decode_workspace_init
+ * Blocks past a context's end are never read; a table entry outside the pool
+ * is read as zeros and sets PA_DEVERR_BLOCK_ID. */
+PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int32_t max_blocks,
+                           const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                           int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                           int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the current device's error word in *flags
+ * (host, nullable) and clears it.  Returns PA_ERR_BOUNDS or PA_ERR_TIMEOUT if
+ * any bit was set, PA_ERR_CUDA if the stream reports an error, else PA_OK. */
+PA_API pa_status pa_check_device_errors(void* stream, uint32_t* flags);
+
+/* Number of decode CTAs pa_decode launches on the current device (one per SM
+ * times the resident CTAs per SM), for launch accounting; 0 on error. */
+PA_API int32_t pa_decode_grid_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,1 +1,9 @@
-"""GB300-native paged KV-cache decode attention (sm_103a)."""
+"""GB300-native paged KV-cache decode attention (sm_103a).
+
+The compute path is ``libpa.so`` (C ABI, ``include/pa.h``); ``binding``
+exposes it under the same names.  Importing the package loads nothing; the
+library is loaded on first use and its absence is an error, never a fallback.
+"""
+from .binding import (Allocator, PaError, load, pa_check_device_errors, pa_copy_blocks,  # noqa: F401
+                      pa_decode, pa_decode_grid_size, pa_decode_workspace_init,
+                      pa_decode_workspace_size, pa_reshape_and_cache)

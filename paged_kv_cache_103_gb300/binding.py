@@ -1,0 +1,289 @@
+"""ctypes binding of ``libpa.so`` (``include/pa.h``), with the C names.
+
+Argument marshalling only: tensors become raw pointers and sizes, statuses
+become :class:`PaError`.  Every step runs inside the library.  The library
+must have been built (``paged_kv_cache_103_gb300.build.build()``); loading
+fails loudly if it is missing -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+PA_OK = 0
+PA_F16, PA_BF16 = 0, 1
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_OOM", 3: "PA_ERR_NOT_FOUND",
+                4: "PA_ERR_BOUNDS", 5: "PA_ERR_CUDA", 6: "PA_ERR_UNSUPPORTED",
+                7: "PA_ERR_TIMEOUT"}
+DEVERR = {"BLOCK_ID": 0x1, "TABLE_WIDTH": 0x2, "SLOT": 0x4, "TIMEOUT": 0x8, "PAIR": 0x10,
+          "CONTEXT": 0x20}
+
+# Every symbol pa.h declares, with (restype, argtypes).
+_P, _I32, _I64, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_ST = ctypes.c_int
+
+
+class AllocStats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32),
+                ("shared_blocks", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int64)]
+
+
+SIGNATURES = {
+    "pa_status_str": (ctypes.c_char_p, [_ST]),
+    "pa_version": (_I32, []),
+    "pa_alloc_create": (_ST, [_I32, _I32, _P, ctypes.POINTER(_P)]),
+    "pa_alloc_destroy": (None, [_P]),
+    "pa_alloc": (_ST, [_P, _I64, _I32]),
+    "pa_append_slot": (_ST, [_P, _I64, _P, _P, _P]),
+    "pa_append_batch": (_ST, [_P, _P, _I32, _P, _P, _P]),
+    "pa_fork": (_ST, [_P, _I64, _I64]),
+    "pa_free": (_ST, [_P, _I64]),
+    "pa_export": (_ST, [_P, _P, _I32, _I32, _P, _P]),
+    "pa_seq_slots": (_ST, [_P, _I64, _I32, _I32, _P]),
+    "pa_seq_info": (_ST, [_P, _I64, _P, _P]),
+    "pa_block_ref": (_ST, [_P, _I32, _P]),
+    "pa_free_list": (_ST, [_P, _P, _I32, _P]),
+    "pa_alloc_stats_get": (_ST, [_P, ctypes.POINTER(AllocStats)]),
+    "pa_reshape_and_cache": (_ST, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _ST, _P]),
+    "pa_copy_blocks": (_ST, [_P, _P, _I32, _P, _I32, _I64, _I32, _P]),
+    "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "pa_decode_workspace_init": (_ST, [_P, _SZ, _P]),
+    "pa_decode": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                        _F32, _ST, _P, _P, _SZ, _P]),
+    "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "pa_decode_grid_size": (_I32, []),
+}
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (what, STATUS_NAMES.get(status, status),
+                                          _lib_status_str(status)))
+
+
+_lib = None
+
+
+def _lib_status_str(status: int) -> str:
+    if _lib is None:
+        return "?"
+    s = _lib.pa_status_str(status)
+    return s.decode() if s else "?"
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Loads libpa.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError("libpa.so is not built (%s); run __graft_entry__.build() or "
+                               "python -m paged_kv_cache_103_gb300.build" % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError("fp16 or bf16 expected, got %s" % t.dtype)
+
+
+def _dev(t, dtype=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("contiguous CUDA tensor expected")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s expected, got %s" % (dtype, t.dtype))
+    return t.data_ptr()
+
+
+# --------------------------------------------------------------------------- device ops
+def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """``k_new/v_new [T, Hkv, d]``, ``slot_mapping [T] int64``, caches ``[N, bs, Hkv, d]``."""
+    import torch
+    T, Hkv, d = k_new.shape
+    N, bs = k_cache.shape[0], k_cache.shape[1]
+    _check(load().pa_reshape_and_cache(_dev(k_new), _dev(v_new), _dev(slot_mapping, torch.int64),
+                                       T, _dev(k_cache), _dev(v_cache), N, bs, Hkv, d,
+                                       _dtype_code(k_cache), _stream_ptr(stream)),
+           "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_caches, v_caches, pairs, stream=None) -> None:
+    """Copies block ``pairs[p][0]`` onto ``pairs[p][1]`` in every layer's caches."""
+    import torch
+    L = len(k_caches)
+    P = int(pairs.shape[0])
+    kc = (ctypes.c_void_p * max(L, 1))(*[_dev(t) for t in k_caches])
+    vc = (ctypes.c_void_p * max(L, 1))(*[_dev(t) for t in v_caches])
+    ref = k_caches[0]
+    block_bytes = ref[0].numel() * ref.element_size()
+    _check(load().pa_copy_blocks(kc, vc, L, _dev(pairs, torch.int32), P, block_bytes,
+                                 int(ref.shape[0]), _stream_ptr(stream)), "pa_copy_blocks")
+
+
+def pa_decode_workspace_size(B: int, H: int, d: int) -> int:
+    return int(load().pa_decode_workspace_size(B, H, d))
+
+
+def pa_decode_workspace_init(workspace, stream=None) -> None:
+    _check(load().pa_decode_workspace_init(_dev(workspace), workspace.numel() *
+                                           workspace.element_size(), _stream_ptr(stream)),
+           "pa_decode_workspace_init")
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+              scale: float, out, workspace, stream=None) -> None:
+    """``q/out [B, H, d]``, caches ``[N, bs, Hkv, d]``, ``block_tables [B, max_blocks]``
+    int32, ``context_lens [B]`` int32, ``workspace`` a zero-initialised byte tensor."""
+    import torch
+    B, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    _check(load().pa_decode(_dev(q), _dev(k_cache), _dev(v_cache),
+                            _dev(block_tables, torch.int32), int(block_tables.shape[1]),
+                            _dev(context_lens, torch.int32), int(max_context_len), B, H, Hkv, d,
+                            bs, N, float(scale), _dtype_code(q), _dev(out), _dev(workspace),
+                            workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "pa_decode")
+
+
+def pa_check_device_errors(stream=None) -> int:
+    """Synchronises the stream; returns the error word's bits (and clears them)."""
+    flags = ctypes.c_uint32(0)
+    st = load().pa_check_device_errors(_stream_ptr(stream), ctypes.byref(flags))
+    if st not in (PA_OK, 4, 7):
+        raise PaError(st, "pa_check_device_errors")
+    return int(flags.value)
+
+
+def pa_decode_grid_size() -> int:
+    return int(load().pa_decode_grid_size())
+
+
+# ------------------------------------------------------------------------- allocator
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Allocator:
+    """The host block allocator (``pa_alloc_*``); owns one ``pa_allocator``."""
+
+    def __init__(self, num_blocks: int, block_size: int, init_free_order=None):
+        self._lib = load()
+        self._h = ctypes.c_void_p()
+        order = None
+        if init_free_order is not None:
+            self._order = np.ascontiguousarray(init_free_order, dtype=np.int32)
+            order = _np_ptr(self._order)
+        _check(self._lib.pa_alloc_create(num_blocks, block_size, order, ctypes.byref(self._h)),
+               "pa_alloc_create")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_alloc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, seq_id: int, num_tokens: int) -> None:
+        _check(self._lib.pa_alloc(self._h, seq_id, num_tokens), "pa_alloc")
+
+    def append_slot(self, seq_id: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_append_slot(self._h, seq_id, ctypes.byref(slot), ctypes.byref(src),
+                                        ctypes.byref(dst)), "pa_append_slot")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def append_batch(self, seq_ids, slot_mapping=None, cow_pairs=None):
+        """Returns ``(slot_mapping int64 [B], cow_pairs int32 [P, 2])``; output arrays may
+        be passed in (e.g. pinned host memory as numpy views)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        B = ids.shape[0]
+        slots = np.empty(B, np.int64) if slot_mapping is None else slot_mapping
+        pairs = np.empty((max(B, 1), 2), np.int32) if cow_pairs is None else cow_pairs
+        n = ctypes.c_int32()
+        _check(self._lib.pa_append_batch(self._h, _np_ptr(ids), B, _np_ptr(slots),
+                                         _np_ptr(pairs), ctypes.byref(n)), "pa_append_batch")
+        return slots, pairs[: n.value]
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(self._lib.pa_fork(self._h, parent, child), "pa_fork")
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pa_free(self._h, seq_id), "pa_free")
+
+    def export(self, seq_ids, max_blocks: int, block_tables=None, context_lens=None):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        B = ids.shape[0]
+        tbl = np.empty((B, max_blocks), np.int32) if block_tables is None else block_tables
+        lens = np.empty(B, np.int32) if context_lens is None else context_lens
+        _check(self._lib.pa_export(self._h, _np_ptr(ids), B, max_blocks, _np_ptr(tbl),
+                                   _np_ptr(lens)), "pa_export")
+        return tbl, lens
+
+    def seq_slots(self, seq_id: int, start: int, count: int) -> np.ndarray:
+        out = np.empty(max(count, 1), np.int64)
+        _check(self._lib.pa_seq_slots(self._h, seq_id, start, count, _np_ptr(out)),
+               "pa_seq_slots")
+        return out[:count]
+
+    def seq_info(self, seq_id: int):
+        ln, nb = ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_seq_info(self._h, seq_id, ctypes.byref(ln), ctypes.byref(nb)),
+               "pa_seq_info")
+        return ln.value, nb.value
+
+    def block_ref(self, block: int) -> int:
+        r = ctypes.c_int32()
+        _check(self._lib.pa_block_ref(self._h, block, ctypes.byref(r)), "pa_block_ref")
+        return r.value
+
+    def free_list(self):
+        out = np.empty(max(self.num_blocks, 1), np.int32)
+        n = ctypes.c_int32()
+        _check(self._lib.pa_free_list(self._h, _np_ptr(out), self.num_blocks, ctypes.byref(n)),
+               "pa_free_list")
+        return out[: n.value].tolist()
+
+    def stats(self) -> dict:
+        s = AllocStats()
+        _check(self._lib.pa_alloc_stats_get(self._h, ctypes.byref(s)), "pa_alloc_stats_get")
+        return {f: getattr(s, f) for f, _ in AllocStats._fields_}

@@ -1,0 +1,291 @@
+// Host-side KV block allocator behind the pa_alloc* / pa_append* / pa_fork /
+// pa_free / pa_export entry points of pa.h.
+//
+// Rules, from the pages:
+//   "LLM推理优化：vLLM PagedAttention深度解析与工程实践", section 3.2 (BlockManager):
+//     the free list begins in block order, allocation takes from its front,
+//     freeing appends to its back in the sequence's table order, and
+//     allocate(seq, num_tokens) checks the free list before taking blocks.
+//   "vLLM 深度拆解：当大模型推理学会「分页注意力」", section 3.3 (BlockSpaceManager):
+//     append_slot fills the current block and takes a new one when it is full;
+//     free returns all blocks; identical prefixes share physical blocks and a
+//     shared block is copied only when a sharer writes into it.
+// Reference counts decide when a shared block is free again; a sharer writing
+// into a shared, partially filled last block takes a fresh block (front of the
+// free list) and reports the (old, new) copy; the last remaining sharer writes
+// in place.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "pa.h"
+
+namespace {
+
+struct Sequence {
+    std::vector<int32_t> table;  // logical block -> physical block
+    int32_t length = 0;          // tokens written or reserved
+};
+
+}  // namespace
+
+struct pa_allocator {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    std::deque<int32_t> free_list;
+    std::vector<int32_t> ref;
+    std::unordered_map<int64_t, Sequence> seqs;
+
+    int64_t capacity(const Sequence& s) const { return (int64_t)s.table.size() * block_size; }
+
+    int32_t take_front() {
+        int32_t b = free_list.front();
+        free_list.pop_front();
+        ref[b] = 1;
+        return b;
+    }
+
+    // Blocks one append of `s` takes, given `ref_of(block)` as the current count.
+    template <class RefOf>
+    int32_t append_need(const Sequence& s, RefOf ref_of) const {
+        if (s.length == capacity(s)) return 1;
+        return ref_of(s.table[s.length / block_size]) > 1 ? 1 : 0;
+    }
+
+    // Performs one append whose blocks were checked; returns the slot.
+    int64_t append_checked(Sequence& s, int32_t* cow_src, int32_t* cow_dst) {
+        *cow_src = -1;
+        *cow_dst = -1;
+        const int32_t pos = s.length;
+        if (pos == capacity(s)) {
+            s.table.push_back(take_front());
+        } else {
+            int32_t& last = s.table[pos / block_size];
+            if (ref[last] > 1) {
+                int32_t fresh = take_front();
+                ref[last] -= 1;
+                *cow_src = last;
+                *cow_dst = fresh;
+                last = fresh;
+            }
+        }
+        s.length = pos + 1;
+        return (int64_t)s.table[pos / block_size] * block_size + pos % block_size;
+    }
+};
+
+extern "C" {
+
+PA_API pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size,
+                                 const int32_t* init_free_order, pa_allocator** out) {
+    if (!out || num_blocks < 0 || block_size <= 0) return PA_ERR_INVALID;
+    *out = nullptr;
+    pa_allocator* a = new (std::nothrow) pa_allocator();
+    if (!a) return PA_ERR_OOM;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ref.assign((size_t)num_blocks, 0);
+    if (init_free_order) {
+        std::vector<char> seen((size_t)num_blocks, 0);
+        for (int32_t i = 0; i < num_blocks; ++i) {
+            int32_t b = init_free_order[i];
+            if (b < 0 || b >= num_blocks || seen[(size_t)b]) {
+                delete a;
+                return PA_ERR_INVALID;
+            }
+            seen[(size_t)b] = 1;
+            a->free_list.push_back(b);
+        }
+    } else {
+        for (int32_t b = 0; b < num_blocks; ++b) a->free_list.push_back(b);
+    }
+    *out = a;
+    return PA_OK;
+}
+
+PA_API void pa_alloc_destroy(pa_allocator* a) { delete a; }
+
+PA_API pa_status pa_alloc(pa_allocator* a, int64_t seq_id, int32_t num_tokens) {
+    if (!a || num_tokens < 0) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    const bool fresh = (it == a->seqs.end());
+    Sequence empty;
+    const Sequence& cur = fresh ? empty : it->second;
+    const int64_t held = a->capacity(cur);
+    if (!fresh && num_tokens > cur.length && cur.length % a->block_size != 0 &&
+        !cur.table.empty() && a->ref[cur.table.back()] > 1)
+        return PA_ERR_INVALID;  // would write into a shared partial block
+    int64_t need = 0;
+    if (held < num_tokens) need = (num_tokens - held + a->block_size - 1) / a->block_size;
+    if (need > (int64_t)a->free_list.size()) return PA_ERR_OOM;
+    Sequence& s = a->seqs[seq_id];
+    for (int64_t k = 0; k < need; ++k) s.table.push_back(a->take_front());
+    s.length = std::max(s.length, num_tokens);
+    return PA_OK;
+}
+
+PA_API pa_status pa_append_slot(pa_allocator* a, int64_t seq_id, int64_t* slot_out,
+                                int32_t* cow_src, int32_t* cow_dst) {
+    if (!a || !slot_out) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    if (it->second.length == INT32_MAX) return PA_ERR_INVALID;
+    if (a->append_need(it->second, [&](int32_t b) { return a->ref[b]; }) >
+        (int32_t)a->free_list.size())
+        return PA_ERR_OOM;
+    int32_t src, dst;
+    *slot_out = a->append_checked(it->second, &src, &dst);
+    if (cow_src) *cow_src = src;
+    if (cow_dst) *cow_dst = dst;
+    return PA_OK;
+}
+
+PA_API pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t B,
+                                 int64_t* slot_mapping, int32_t* cow_pairs, int32_t* num_cow) {
+    if (!a || B < 0 || (B > 0 && (!seq_ids || !slot_mapping || !cow_pairs)) || !num_cow)
+        return PA_ERR_INVALID;
+    *num_cow = 0;
+    std::vector<Sequence*> batch((size_t)B);
+    std::unordered_set<int64_t> seen;
+    seen.reserve((size_t)B * 2);
+    for (int32_t i = 0; i < B; ++i) {
+        if (!seen.insert(seq_ids[i]).second) return PA_ERR_INVALID;
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+        if (it->second.length == INT32_MAX) return PA_ERR_INVALID;
+        batch[(size_t)i] = &it->second;
+    }
+    // Count the blocks the batch takes, following the counts it lowers as
+    // earlier sharers in the batch copy away from a shared block.
+    std::unordered_map<int32_t, int32_t> lowered;
+    int64_t need = 0;
+    for (Sequence* s : batch) {
+        auto ref_of = [&](int32_t b) {
+            auto f = lowered.find(b);
+            return a->ref[b] - (f == lowered.end() ? 0 : f->second);
+        };
+        int32_t n = a->append_need(*s, ref_of);
+        if (n && s->length != a->capacity(*s)) lowered[s->table[s->length / a->block_size]] += 1;
+        need += n;
+    }
+    if (need > (int64_t)a->free_list.size()) return PA_ERR_OOM;
+    int32_t ncow = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        int32_t src, dst;
+        slot_mapping[i] = a->append_checked(*batch[(size_t)i], &src, &dst);
+        if (src >= 0) {
+            cow_pairs[2 * ncow] = src;
+            cow_pairs[2 * ncow + 1] = dst;
+            ++ncow;
+        }
+    }
+    *num_cow = ncow;
+    return PA_OK;
+}
+
+PA_API pa_status pa_fork(pa_allocator* a, int64_t parent, int64_t child) {
+    if (!a) return PA_ERR_INVALID;
+    auto p = a->seqs.find(parent);
+    if (p == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    if (a->seqs.count(child)) return PA_ERR_INVALID;
+    Sequence copy = p->second;
+    for (int32_t b : copy.table) a->ref[b] += 1;
+    a->seqs.emplace(child, std::move(copy));
+    return PA_OK;
+}
+
+PA_API pa_status pa_free(pa_allocator* a, int64_t seq_id) {
+    if (!a) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    for (int32_t b : it->second.table)
+        if (--a->ref[b] == 0) a->free_list.push_back(b);
+    a->seqs.erase(it);
+    return PA_OK;
+}
+
+PA_API pa_status pa_export(const pa_allocator* a, const int64_t* seq_ids, int32_t B,
+                           int32_t max_blocks, int32_t* block_tables, int32_t* context_lens) {
+    if (!a || B < 0 || max_blocks < 0 ||
+        (B > 0 && (!seq_ids || !context_lens || (max_blocks > 0 && !block_tables))))
+        return PA_ERR_INVALID;
+    for (int32_t i = 0; i < B; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+        if ((int64_t)it->second.table.size() > max_blocks) return PA_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < B; ++i) {
+        const Sequence& s = a->seqs.find(seq_ids[i])->second;
+        int32_t* row = block_tables + (int64_t)i * max_blocks;
+        const int32_t n = (int32_t)s.table.size();
+        if (n) std::memcpy(row, s.table.data(), sizeof(int32_t) * (size_t)n);
+        for (int32_t j = n; j < max_blocks; ++j) row[j] = -1;
+        context_lens[i] = s.length;
+    }
+    return PA_OK;
+}
+
+PA_API pa_status pa_seq_slots(const pa_allocator* a, int64_t seq_id, int32_t start,
+                              int32_t count, int64_t* slots) {
+    if (!a || start < 0 || count < 0 || (count > 0 && !slots)) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    const Sequence& s = it->second;
+    if ((int64_t)start + count > a->capacity(s)) return PA_ERR_INVALID;
+    for (int32_t t = 0; t < count; ++t) {
+        const int32_t pos = start + t;
+        slots[t] = (int64_t)s.table[pos / a->block_size] * a->block_size + pos % a->block_size;
+    }
+    return PA_OK;
+}
+
+PA_API pa_status pa_seq_info(const pa_allocator* a, int64_t seq_id, int32_t* length,
+                             int32_t* num_table_blocks) {
+    if (!a) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    if (length) *length = it->second.length;
+    if (num_table_blocks) *num_table_blocks = (int32_t)it->second.table.size();
+    return PA_OK;
+}
+
+PA_API pa_status pa_block_ref(const pa_allocator* a, int32_t block, int32_t* ref) {
+    if (!a || !ref || block < 0 || block >= a->num_blocks) return PA_ERR_INVALID;
+    *ref = a->ref[(size_t)block];
+    return PA_OK;
+}
+
+PA_API pa_status pa_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n) {
+    if (!a || !n || cap < 0) return PA_ERR_INVALID;
+    *n = (int32_t)a->free_list.size();
+    if (cap < *n) return PA_ERR_INVALID;
+    int32_t i = 0;
+    for (int32_t b : a->free_list) out[i++] = b;
+    return PA_OK;
+}
+
+PA_API pa_status pa_alloc_stats_get(const pa_allocator* a, pa_alloc_stats* out) {
+    if (!a || !out) return PA_ERR_INVALID;
+    out->num_blocks = a->num_blocks;
+    out->block_size = a->block_size;
+    out->free_blocks = (int32_t)a->free_list.size();
+    int32_t used = 0, shared = 0;
+    for (int32_t r : a->ref) {
+        used += r > 0;
+        shared += r > 1;
+    }
+    out->used_blocks = used;
+    out->shared_blocks = shared;
+    out->num_seqs = (int32_t)a->seqs.size();
+    int64_t tokens = 0;
+    for (const auto& kv : a->seqs) tokens += kv.second.length;
+    out->num_tokens = tokens;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// KV append (pa_reshape_and_cache) and copy-on-write block copies
+// (pa_copy_blocks).  Both are bit copies of 16-byte vectors; every index is
+// checked against its buffer before the access, and a bad one raises a bit in
+// the device error word instead of being used.
+//
+// Sources: "vLLM推理加速深度解析：从PagedAttention原理到生产部署实战", section 2.2
+// (each new token's K/V goes into the physical block its current logical block
+// points to); "vLLM 深度拆解：当大模型推理学会「分页注意力」", section 3.3
+// (append_slot; shared blocks copied only when a sharer writes).
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// One thread moves one 16-byte vector of K and the same vector of V.
+__global__ void __launch_bounds__(kThreads)
+reshape_and_cache_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                         const int64_t* __restrict__ slot_mapping, int32_t T,
+                         int32_t vecs_per_token, uint4* __restrict__ k_cache,
+                         uint4* __restrict__ v_cache, int64_t num_slots,
+                         unsigned int* __restrict__ err) {
+    const int64_t total = (int64_t)T * vecs_per_token;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = idx / vecs_per_token;
+        const int64_t v = idx - t * vecs_per_token;
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;  // padding token
+        if (slot >= num_slots) {
+            if (v == 0) pa::raise_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t dst = slot * vecs_per_token + v;
+        k_cache[dst] = __ldg(k_new + idx);
+        v_cache[dst] = __ldg(v_new + idx);
+    }
+}
+
+constexpr int kMaxLayersPerLaunch = 32;
+
+struct LayerPtrs {
+    uint4* k[kMaxLayersPerLaunch];
+    uint4* v[kMaxLayersPerLaunch];
+};
+
+// blockIdx.x = pair, blockIdx.y = layer within this launch's group.
+__global__ void __launch_bounds__(kThreads)
+copy_blocks_kernel(const __grid_constant__ LayerPtrs layers, const int32_t* __restrict__ pairs,
+                   int64_t vecs_per_block, int32_t num_blocks, unsigned int* __restrict__ err) {
+    const int32_t p = blockIdx.x;
+    const int32_t src = __ldg(pairs + 2 * p);
+    const int32_t dst = __ldg(pairs + 2 * p + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) pa::raise_error(err, PA_DEVERR_PAIR);
+        return;
+    }
+    const uint4* ks = layers.k[blockIdx.y] + (int64_t)src * vecs_per_block;
+    const uint4* vs = layers.v[blockIdx.y] + (int64_t)src * vecs_per_block;
+    uint4* kd = layers.k[blockIdx.y] + (int64_t)dst * vecs_per_block;
+    uint4* vd = layers.v[blockIdx.y] + (int64_t)dst * vecs_per_block;
+    for (int64_t i = threadIdx.x; i < vecs_per_block; i += kThreads) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                      void* v_cache, int32_t num_blocks, int32_t block_size,
+                                      int32_t Hkv, int32_t d, pa_dtype dtype, void* stream) {
+    if (T < 0 || num_blocks < 0 || block_size <= 0 || Hkv <= 0 || d <= 0) return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if ((Hkv * d * 2) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (T == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID;
+    unsigned int* err = pa::device_error_word();
+    const int sms = pa::device_sm_count();
+    if (!err || !sms) return PA_ERR_CUDA;
+    const int32_t vecs = Hkv * d * 2 / 16;
+    const int64_t total = (int64_t)T * vecs;
+    int64_t blocks = (total + kThreads - 1) / kThreads;
+    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+    reshape_and_cache_kernel<<<(unsigned)blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, T, vecs,
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+        (int64_t)num_blocks * block_size, err);
+    return pa::cuda_status(cudaGetLastError());
+}
+
+PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
+                                int32_t num_layers, const int32_t* pairs, int32_t num_pairs,
+                                int64_t block_bytes, int32_t num_blocks, void* stream) {
+    if (num_layers < 0 || num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 != 0 ||
+        num_blocks < 0)
+        return PA_ERR_INVALID;
+    if (num_layers == 0 || num_pairs == 0) return PA_OK;
+    if (!k_caches || !v_caches || !pairs) return PA_ERR_INVALID;
+    if (num_pairs > 65535 * 64) return PA_ERR_UNSUPPORTED;
+    unsigned int* err = pa::device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    for (int32_t l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+        const int32_t nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0
+                                                                 : kMaxLayersPerLaunch;
+        LayerPtrs lp{};
+        for (int32_t l = 0; l < nl; ++l) {
+            if (!k_caches[l0 + l] || !v_caches[l0 + l] || !aligned16(k_caches[l0 + l]) ||
+                !aligned16(v_caches[l0 + l]))
+                return PA_ERR_INVALID;
+            lp.k[l] = static_cast<uint4*>(k_caches[l0 + l]);
+            lp.v[l] = static_cast<uint4*>(v_caches[l0 + l]);
+        }
+        copy_blocks_kernel<<<dim3((unsigned)num_pairs, (unsigned)nl), kThreads, 0,
+                             static_cast<cudaStream_t>(stream)>>>(lp, pairs, block_bytes / 16,
+                                                                   num_blocks, err);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

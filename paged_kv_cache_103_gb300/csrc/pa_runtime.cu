@@ -1,0 +1,94 @@
+// Runtime pieces of the C ABI: status strings, the per-device error word that
+// kernels raise bits in (instead of trapping), SM-count caching and the decode
+// workspace initialisation.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pa.h"
+#include "pa_common.cuh"
+
+namespace {
+
+// One word per device (a file-scope __device__ variable exists once per device
+// that loads this library).  Kernels OR PA_DEVERR_* bits into it.
+__device__ unsigned int g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_error_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+}  // namespace
+
+namespace pa {
+
+unsigned int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_error_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_error_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_error_ptr[dev];
+}
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace pa
+
+extern "C" {
+
+PA_API const char* pa_status_str(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID: return "invalid argument or operation";
+        case PA_ERR_OOM: return "out of KV blocks";
+        case PA_ERR_NOT_FOUND: return "unknown sequence";
+        case PA_ERR_BOUNDS: return "kernel met an index outside its buffers";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+PA_API int32_t pa_version(void) { return 1; }
+
+PA_API pa_status pa_check_device_errors(void* stream, uint32_t* flags) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    unsigned int* word = pa::device_error_word();
+    if (!word) return PA_ERR_CUDA;
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaMemsetAsync(word, 0, sizeof host, st) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    if (flags) *flags = host;
+    if (host & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
+    if (host) return PA_ERR_BOUNDS;
+    return PA_OK;
+}
+
+PA_API pa_status pa_decode_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!workspace && bytes) return PA_ERR_INVALID;
+    if (!bytes) return PA_OK;
+    return pa::cuda_status(
+        cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol the
+header declares; host-side argument checks answer before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_103_gb300 import binding
+from paged_kv_cache_103_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return binding.load()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "pa.h"), encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"PA_API\s+[^;(]*?\b(pa_\w+)\s*\(", text, flags=re.S)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for must in ("pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_alloc", "pa_free",
+                 "pa_append_slot", "pa_fork", "pa_export"):
+        assert must in names
+    assert set(names) == set(binding.SIGNATURES), set(names) ^ set(binding.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_only_the_abi_is_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         stdout=subprocess.PIPE, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("pa_")}
+    assert ours == set(_declared_symbols())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pa_version() == 1
+    for s in range(8):
+        assert lib.pa_status_str(s)
+
+
+def test_decode_host_checks_answer_without_a_gpu(lib):
+    P = ctypes.c_void_p(16 * 1024)  # never dereferenced: the checks fail first
+    # head_dim 96 is outside the supported set
+    st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 4, 2, 96, 16, 8, 0.1, 0, P, P, 1 << 20, None)
+    assert st == 6
+    # block size 64 unsupported
+    st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 4, 2, 128, 64, 8, 0.1, 0, P, P, 1 << 20, None)
+    assert st == 6
+    # H not a multiple of Hkv
+    st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 5, 2, 128, 16, 8, 0.1, 0, P, P, 1 << 20, None)
+    assert st == 6
+    # more than 16 query heads per KV head
+    st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 34, 2, 128, 16, 8, 0.1, 0, P, P, 1 << 20, None)
+    assert st == 6
+    # workspace too small
+    st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 4, 2, 128, 16, 8, 0.1, 0, P, P, 16, None)
+    assert st == 1
+    # empty batch is a no-op
+    st = lib.pa_decode(None, None, None, None, 4, None, 0, 0, 4, 2, 128, 16, 8, 0.1, 0, None,
+                       None, 0, None)
+    assert st == 0
+
+
+def test_workspace_size(lib):
+    assert lib.pa_decode_workspace_size(64, 40, 128) > 0
+    assert lib.pa_decode_workspace_size(64, 40, 96) == 0
+    a = lib.pa_decode_workspace_size(1, 8, 128)
+    b = lib.pa_decode_workspace_size(1000, 8, 128)
+    assert b > a
+
+
+def test_cache_op_host_checks(lib):
+    P = ctypes.c_void_p(16 * 1024)
+    assert lib.pa_reshape_and_cache(P, P, P, 0, P, P, 8, 16, 2, 64, 0, None) == 0   # T = 0
+    assert lib.pa_reshape_and_cache(P, P, P, -1, P, P, 8, 16, 2, 64, 0, None) == 1
+    assert lib.pa_reshape_and_cache(P, P, P, 1, P, P, 8, 16, 2, 64, 5, None) == 6   # dtype
+    assert lib.pa_copy_blocks(None, None, 0, None, 0, 4096, 8, None) == 0
+    assert lib.pa_copy_blocks(None, None, 1, None, 1, 4095, 8, None) == 1             # not x16
