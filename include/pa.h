@@ -222,6 +222,29 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
                            int32_t num_blocks, float scale, pa_dtype dtype, void* out,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* pa_decode without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: code running inside an allocator's own hooks, or in
+ * a process whose device memory is pre-partitioned by a host framework that
+ * forbids further cudaMalloc calls.  The paper has no counterpart to this
+ * entry point.  Arguments are those of pa_decode minus
+ * the workspace.  Scratch lives in one file-scope device array of
+ * PA_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading the library holds
+ * until the process exits; a batch whose pa_decode_workspace_size(B, H, d)
+ * exceeds it returns PA_ERR_UNSUPPORTED.  The call allocates nothing: the
+ * first call on a device looks up the array's device address (so make that
+ * first call before any stream capture), and every call clears the arrival
+ * counters with an async memset on `stream`.  All calls share the one array,
+ * which keeps the last call's partial results: calls that overlap on the GPU
+ * (different streams, or different host threads) race and must be serialised
+ * by the caller. */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   int32_t B, int32_t H, int32_t Hkv, int32_t d,
+                                   int32_t block_size, int32_t num_blocks, float scale,
+                                   pa_dtype dtype, void* out, void* stream);
+
 /* Synchronises `stream`, returns the current device's error word in *flags
  * (host, nullable) and clears it.  Returns PA_ERR_BOUNDS or PA_ERR_TIMEOUT if
  * any bit was set, PA_ERR_CUDA if the stream reports an error, else PA_OK. */

@@ -56,6 +56,8 @@ SIGNATURES = {
     "pa_decode_workspace_init": (_ST, [_P, _SZ, _P]),
     "pa_decode": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                         _F32, _ST, _P, _P, _SZ, _P]),
+    "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                _I32, _F32, _ST, _P, _P]),
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "pa_decode_grid_size": (_I32, []),
 }
@@ -178,6 +180,22 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
                             bs, N, float(scale), _dtype_code(q), _dev(out), _dev(workspace),
                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "pa_decode")
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                      scale: float, out, stream=None) -> None:
+    """``pa_decode`` for callers that cannot allocate: the scratch is the
+    library's own per-device array, so no workspace is passed.  Calls that
+    overlap on the GPU share that array and must be serialised."""
+    import torch
+    B, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    _check(load().pa_decode_noalloc(_dev(q), _dev(k_cache), _dev(v_cache),
+                                    _dev(block_tables, torch.int32), int(block_tables.shape[1]),
+                                    _dev(context_lens, torch.int32), int(max_context_len), B, H,
+                                    Hkv, d, bs, N, float(scale), _dtype_code(q), _dev(out),
+                                    _stream_ptr(stream)),
+           "pa_decode_noalloc")
 
 
 def pa_check_device_errors(stream=None) -> int:
