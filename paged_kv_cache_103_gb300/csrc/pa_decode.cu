@@ -46,7 +46,8 @@
 
 namespace {
 
-constexpr int kChunk = 32;           // tokens per pipeline stage
+constexpr int kChunk = 32;           // tokens per pipeline stage (16 or 32)
+constexpr int kKeyTiles = kChunk / 16;  // 16-key MMA tiles per chunk
 constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarps = 2;
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
@@ -142,9 +143,9 @@ __device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
 // column c of row r stored at column c ^ (r & 7)).  Byte offset of (token t,
 // half h, 16-byte column c) inside a tensor's chunk:
 __device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t c,
-                                                uint32_t halves, uint32_t bs_shift) {
-    const uint32_t b = t >> bs_shift, r = t & ((1u << bs_shift) - 1u);
-    return ((((b * halves + h) << bs_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
+                                                uint32_t halves, uint32_t rows_shift) {
+    const uint32_t b = t >> rows_shift, r = t & ((1u << rows_shift) - 1u);
+    return ((((b * halves + h) << rows_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
 }
 
 template <int D, bool kBF16, int NT>
@@ -172,7 +173,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int32_t max_len = p.max_blocks * bs;
-    const uint32_t bs_shift = (uint32_t)(31 - __clz(bs));
+    // Rows of one TMA box: a whole block, or a chunk-sized slice of a larger one.
+    const uint32_t rows_shift = (uint32_t)(31 - __clz(bs < kChunk ? bs : kChunk));
 
     // ---- prefix of chunk counts: prefix[i] = Hkv * sum_{i' < i} ceil(n_i' / 32)
     {
@@ -237,9 +239,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             pa::prefetch_tensormap(&vmap);
         }
         const uint64_t policy = pa::l2_policy_evict_first();
-        const int bpc = kChunk / bs;             // blocks per chunk
+        const int rows = bs < kChunk ? bs : kChunk;  // token rows per TMA box
+        const int bpc = kChunk / rows;               // boxes per chunk and tensor
+        const int nblk = (kChunk + bs - 1) / bs;     // table entries a chunk spans
         const int32_t oob_row = p.num_blocks * bs;
-        const int my_b = lane >> 1;              // the block this lane loads ...
+        const int my_b = lane >> 1;              // the box this lane loads ...
         const bool my_v = (lane & 1) != 0;       // ... and whether of K or of V
         const CUtensorMap* my_map = my_v ? &vmap : &kmap;
         int32_t k = 0;  // chunks of this CTA walked so far
@@ -252,8 +256,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             int32_t wbase = -1, went = -1;
             for (int32_t t = 0; t < s.len; ++t, ++k) {
                 if ((k & (kProducerWarps - 1)) != prod) continue;
-                const int32_t j0 = (s.c0 + t) * bpc;
-                if (wbase < 0 || j0 + bpc > wbase + 32) {
+                const int32_t tok_first = (s.c0 + t) * kChunk;
+                const int32_t j0 = tok_first / bs;
+                if (wbase < 0 || j0 + nblk > wbase + 32) {
                     wbase = j0;
                     const int32_t jj = wbase + lane;
                     went = jj < nb ? __ldg(trow + jj) : -1;
@@ -270,7 +275,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 unsigned char* base = smem + stage * L.stage_bytes + (my_v ? L.stage_bytes / 2 : 0);
                 if (lane == 0) pa::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
                 __syncwarp();
-                const int32_t jj = j0 + (my_b < bpc ? my_b : 0);
+                const int32_t tok = tok_first + (my_b < bpc ? my_b : 0) * rows;
+                const int32_t jj = tok / bs;
                 const int32_t blk = __shfl_sync(0xffffffffu, went, (jj - wbase) & 31);
                 if (my_b < bpc) {
                     bool ok = jj < nb;
@@ -278,8 +284,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         ok = false;
                         pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
                     }
-                    pa::tma_load_3d(base + ((uint32_t)my_b * kHalves << bs_shift) * 128, my_map,
-                                    &full[stage], 0, ok ? blk * bs : oob_row,
+                    pa::tma_load_3d(base + ((uint32_t)my_b * kHalves << rows_shift) * 128, my_map,
+                                    &full[stage], 0, ok ? blk * bs + (tok - jj * bs) : oob_row,
                                     s.g * (int32_t)kHalves, policy);
                 }
             }
@@ -352,17 +358,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const int h = e / per_half, rem = e - h * per_half;
                         const uint32_t tok = (uint32_t)(valid + (rem >> 3));
                         *reinterpret_cast<uint4*>(
-                            vbytes + tile_offset(tok, h, rem & 7, kHalves, bs_shift)) =
+                            vbytes + tile_offset(tok, h, rem & 7, kHalves, rows_shift)) =
                             make_uint4(0, 0, 0, 0);
                     }
                     pa::fence_proxy_async_smem();
                     __syncwarp();
                 }
 
-                // S^T = K Q^T: two 16-key m-tiles x NT 8-head n-tiles.
-                float st[2][NT][4];
+                // S^T = K Q^T: kChunk / 16 key m-tiles x NT 8-head n-tiles.
+                float st[kKeyTiles][NT][4];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int mt = 0; mt < kKeyTiles; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         st[mt][nt][0] = st[mt][nt][1] = st[mt][nt][2] = st[mt][nt][3] = 0.f;
@@ -370,11 +376,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t col = (uint32_t)((ks & 3) * 2 + (mi >> 1));
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
+                    for (int mt = 0; mt < kKeyTiles; ++mt) {
                         const uint32_t tok = (uint32_t)(mt * 16 + (mi & 1) * 8 + rr);
                         uint32_t a[4];
                         pa::ldsm_x4(kt + tile_offset(tok, (uint32_t)(ks >> 2), col, kHalves,
-                                                     bs_shift),
+                                                     rows_shift),
                                     a[0], a[1], a[2], a[3]);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
@@ -388,7 +394,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int nt = 0; nt < NT; ++nt) {
                     mx[nt][0] = mx[nt][1] = -INFINITY;
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
+                    for (int mt = 0; mt < kKeyTiles; ++mt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = mt * 16 + cr + 8 * (e >> 1);
@@ -425,9 +431,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         }
                 }
                 // P^T as MMA B fragments: exp2, pack to 16 bits, transpose 8x8 tiles.
-                uint32_t pb[2][NT][2];
+                uint32_t pb[kKeyTiles][NT][2];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int mt = 0; mt < kKeyTiles; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float e4[4];
@@ -440,9 +446,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         pb[mt][nt][1] = pa::movmatrix_trans(pa::pack2<kBF16>(e4[2], e4[3]));
                     }
 
-                // O^T += V^T P^T: head_dim in 16-row m-tiles, keys in two 16-key steps.
+                // O^T += V^T P^T: head_dim in 16-row m-tiles, keys in 16-key steps.
 #pragma unroll
-                for (int ks2 = 0; ks2 < 2; ++ks2) {
+                for (int ks2 = 0; ks2 < kKeyTiles; ++ks2) {
                     const uint32_t tok = (uint32_t)(ks2 * 16 + (mi >> 1) * 8 + rr);
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
@@ -450,7 +456,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         uint32_t a[4];
                         pa::ldsm_x4_trans(vt + tile_offset(tok, (uint32_t)(dd >> 6),
                                                            (uint32_t)((dd & 63) >> 3), kHalves,
-                                                           bs_shift),
+                                                           rows_shift),
                                           a[0], a[1], a[2], a[3]);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
@@ -615,7 +621,8 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int32_t rows, int32_t 
     if (!encode) return false;
     const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)Hkv * d / 64};
     const cuuint64_t strides[2] = {(cuuint64_t)Hkv * d * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)block_size, (cuuint32_t)(d / 64)};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(block_size < kChunk ? block_size : kChunk),
+                               (cuuint32_t)(d / 64)};
     const cuuint32_t elem[3] = {1, 1, 1};
     const CUresult r = encode(
         map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
