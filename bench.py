@@ -44,6 +44,23 @@ def algorithmic_bytes(lens, B, H, Hkv, d, bs, e=2):
     return kv_bytes(lens, Hkv, d, e) + 2 * B * H * d * e + table + 4 * B
 
 
+def max_over_ranks(value, dist, device):
+    """The largest `value` over all ranks (the slowest replica sets the time);
+    `dist` is torch.distributed or None for a single process."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units per second over all replicas: every rank processes its own copy
+    of the batch (weak scaling), timed by the slowest rank."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -67,7 +84,7 @@ def recorded_traffic(name):
                     fields[k.strip()] = v.strip()
         with open(src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        if fields.get("pa_decode.cu sha256[:16]") != sha:
+        if fields.get("pa_decode.cu sha256 prefix") != sha:
             return None
         return int(float(fields["dram bytes per launch"]))
     except Exception:
@@ -131,18 +148,52 @@ class ClockSampler:
                 "samples": len(sm), "window": note}
 
 
+WORKLOADS = {
+    "llama13b": lambda B: wl_mod().llama13b(B=B or 64),
+    "gqa7b_1x1024": lambda B: wl_mod().gqa7b(1, 1024),
+    "gqa7b_8x4096": lambda B: wl_mod().gqa7b(8, 4096),
+    "gqa7b_8x8192": lambda B: wl_mod().gqa7b(8, 8192),
+    "gqa7b_16x32768": lambda B: wl_mod().gqa7b(16, 32768),
+    "qwen_longtail_bs8": lambda B: wl_mod().qwen_longtail(8),
+    "qwen_longtail_bs16": lambda B: wl_mod().qwen_longtail(16),
+    "qwen_longtail_bs32": lambda B: wl_mod().qwen_longtail(32),
+    "prefix_share": lambda B: wl_mod().prefix_share(),
+}
+CONTEXT_MIX = {
+    "llama13b": "uniform[128,2048]",
+    "gqa7b_1x1024": "all 1024", "gqa7b_8x4096": "all 4096", "gqa7b_8x8192": "all 8192",
+    "gqa7b_16x32768": "all 32768",
+    "qwen_longtail_bs8": "95% lognormal(median 1500, sigma 1) <= 8192, 5% uniform[16384,24576]",
+    "qwen_longtail_bs16": "95% lognormal(median 1500, sigma 1) <= 8192, 5% uniform[16384,24576]",
+    "qwen_longtail_bs32": "95% lognormal(median 1500, sigma 1) <= 8192, 5% uniform[16384,24576]",
+    "prefix_share": "1024-token prefix shared by 256 sequences + uniform[64,512] suffixes",
+}
+
+
+def wl_mod():
+    from paged_kv_cache_103_gb300 import workloads
+    return workloads
+
+
 def setup_workload(args):
-    import numpy as np
-    import torch
-
+    """The named workload, its host tensors and the product allocator holding
+    every sequence's history; the step's own token is appended last, so the
+    decode reads context_lens[i] tokens including it."""
     from paged_kv_cache_103_gb300 import binding
-    from paged_kv_cache_103_gb300 import workloads as wl
 
-    w = wl.llama13b(B=args.batch)
-    host = wl.qkv(w)
+    w = WORKLOADS[args.workload](args.batch)
+    host = wl_mod().qkv(w)
     alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
-    for i in range(w.B):
-        alloc.alloc(i, int(w.context_lens[i]) - 1)
+    if w.prefix_len:
+        alloc.alloc(0, w.prefix_len)
+        for s in range(1, w.B):
+            alloc.fork(0, s)
+        for s in range(w.B):
+            for _ in range(int(w.context_lens[s]) - 1 - w.prefix_len):
+                alloc.append_slot(s)
+    else:
+        for i in range(w.B):
+            alloc.alloc(i, int(w.context_lens[i]) - 1)
     slots, pairs = alloc.append_batch(list(range(w.B)))
     assert len(pairs) == 0
     max_blocks = int(math.ceil((int(w.context_lens.max()) + args.e2e_extra) / w.block_size)) + 1
@@ -218,10 +269,7 @@ def run_gpu(args):
         dist.barrier()
     total_ms = ev[0].elapsed_time(ev[-1])
     decode_ms = [ev[1 + 2 * k].elapsed_time(ev[2 + 2 * k]) for k in range(K)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     if sampler:
         sampler.stop()
     flags = binding.pa_check_device_errors(stream)
@@ -230,7 +278,7 @@ def run_gpu(args):
 
     ms_per_step = total_ms / K
     kvb = kv_bytes(lens, w.Hkv, w.d)
-    value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(kvb, world, ms_per_step) / 1e9
     alg = algorithmic_bytes(lens, w.B, w.H, w.Hkv, w.d, w.block_size)
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     achieved = alg / (dec_avg_ms * 1e-3) / 1e9
@@ -239,16 +287,19 @@ def run_gpu(args):
     # ---- e2e leg through the C ABI: host allocator step, pinned H2D, kernels, D2H
     e2e = run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks)
 
+    l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9)
+               if kvb > 2 * 129e6 else "KV per step (%.3f GB) fits in L2: numbers include L2 hits"
+               % (kvb / 1e9))
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded N(0,1) Q/K/V, uniform context lengths, random block placement)",
-        "config": {"workload": "llama13b_mha_decode_layer_step", "batch": w.B,
+        "data": "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)",
+        "config": {"workload": args.workload + "_decode_layer_step", "batch": w.B,
                    "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
-                   "block_size": w.block_size, "context_lens": "uniform[128,2048]",
+                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
                    "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
-                   "l2": "inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9)},
+                   "l2": l2_note},
         "pct_of_hbm_peak": round(100 * value / peak, 1),
         "tokens_per_s": round(w.B / (ms_per_step * 1e-3 * w.layers), 1),
         "us_per_layer_step": round(ms_per_step * 1e3, 2),
@@ -259,7 +310,8 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
-                     "traffic": recorded_traffic("pa_decode_llama13b.txt"),
+                     "traffic": recorded_traffic("pa_decode_llama13b.txt")
+                     if args.workload == "llama13b" and w.B == 64 else None,
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
     }
@@ -349,31 +401,28 @@ def oracle_sample_run(w, host, tbl, lens, seqs, threads):
 
     sel = np.asarray(seqs)
     q = wl.bits(host["q"])[sel]
+    code = oracle.DTYPE_F16 if w.dtype == "f16" else oracle.DTYPE_BF16
     return oracle.decode(q, wl.bits(host["k_cache"]), wl.bits(host["v_cache"]), tbl[sel],
-                         lens[sel], w.scale, oracle.DTYPE_F16, num_threads=threads)
+                         lens[sel], w.scale, code, num_threads=threads)
 
 
 def cpu_baseline(w, host, tbl, lens, seconds):
     """The oracle on the host cores over a bounded sample of the same batch:
-    the first k sequences, k chosen from a one-sequence calibration so the
-    sample takes about `seconds`."""
+    whole-batch passes repeated until about `seconds` of wall time."""
     threads = os.cpu_count() or 1
+    seqs = list(range(w.B))
+    passes, dt = 0, 0.0
     t0 = time.perf_counter()
-    oracle_sample_run(w, host, tbl, lens, [0], 1)
-    one = max(time.perf_counter() - t0, 1e-3) / max(int(lens[0]), 1)   # s per token, 1 thread
-    per_seq = one * float(lens.mean()) / threads
-    k = int(max(threads, min(w.B, seconds / max(per_seq, 1e-6))))
-    k = min(k, w.B)
-    seqs = list(range(k))
-    t0 = time.perf_counter()
-    oracle_sample_run(w, host, tbl, lens, seqs, threads)
-    dt = time.perf_counter() - t0
-    kvb = kv_bytes(lens[:k], w.Hkv, w.d)
-    return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+    while passes == 0 or dt < seconds:
+        oracle_sample_run(w, host, tbl, lens, seqs, threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+    kvb = passes * kv_bytes(lens, w.Hkv, w.d)
+    return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": min(threads, w.B),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "first %d of %d sequences of the same batch (%d context tokens), all "
-                      "heads, fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()),
-                                                             threads)}
+            "sample": "%d passes over the whole %d-sequence batch (%d context tokens each), "
+                      "fp64 C oracle on %d threads" % (passes, w.B, int(lens.sum()),
+                                                      min(threads, w.B))}
 
 
 def run_reference(args):
@@ -385,21 +434,31 @@ def run_reference(args):
     from paged_kv_cache_103_gb300 import workloads as wl
     import numpy as np
 
-    w = wl.llama13b(B=args.batch)
+    w = WORKLOADS[args.workload](args.batch)
     host = wl.qkv(w)
     m = oracle.BlockManagerModel(w.num_blocks, w.block_size, w.free_order)
-    for i in range(w.B):
-        m.allocate(i, int(w.context_lens[i]) - 1)
+    if w.prefix_len:
+        m.allocate(0, w.prefix_len)
+        for s in range(1, w.B):
+            m.fork(0, s)
+        for s in range(w.B):
+            for _ in range(int(w.context_lens[s]) - 1 - w.prefix_len):
+                m.append_slot(s)
+    else:
+        for i in range(w.B):
+            m.allocate(i, int(w.context_lens[i]) - 1)
     slots, _ = m.append_batch(range(w.B))
     oracle.reshape_and_cache(host["k_new"], host["v_new"], slots, host["k_cache"],
                              host["v_cache"])
     tbl, lens = m.export(range(w.B))
     threads = os.cpu_count() or 1
-    # each step: a bounded sample of sequences, sized to about `ref_step_seconds`
+    # each step: a bounded sample of sequences, sized so that the whole run takes
+    # about two minutes (and a step at most `ref_step_seconds`)
+    per_step = min(args.ref_step_seconds, 120.0 / max(1, args.steps + args.warmup))
     t0 = time.perf_counter()
     oracle_sample_run(w, host, tbl, lens, [0], 1)
-    one = max(time.perf_counter() - t0, 1e-3)   # one sequence on one thread
-    k = int(max(1, min(w.B, threads * args.ref_step_seconds / one)))
+    one = max(time.perf_counter() - t0, 1e-4)   # one sequence on one thread
+    k = int(max(1, min(w.B, min(threads, w.B) * per_step / one)))
     seqs = list(range(k))
     for _ in range(args.warmup):
         oracle_sample_run(w, host, tbl, lens, seqs[:1], threads)
@@ -408,18 +467,19 @@ def run_reference(args):
         oracle_sample_run(w, host, tbl, lens, seqs, threads)
     dt = (time.perf_counter() - t0) / args.steps
     value = kv_bytes(lens[:k], w.Hkv, w.d) / dt / 1e9
+    used = min(threads, k)
     sample = ("first %d of %d sequences of the batch per step (%d context tokens), all heads, "
-              "fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()), threads))
+              "fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()), used))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) Q/K/V, uniform context lengths, random block placement)",
-        "config": {"workload": "llama13b_mha_decode_layer_step", "batch": w.B, "q_heads": w.H,
-                   "kv_heads": w.Hkv, "head_dim": w.d, "block_size": w.block_size,
-                   "context_lens": "uniform[128,2048]"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+        "data": "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)",
+        "config": {"workload": args.workload + "_decode_layer_step", "batch": w.B,
+                   "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
+                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -432,10 +492,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama13b")
+    ap.add_argument("--batch", type=int, default=None, help="batch of the llama13b workload")
     ap.add_argument("--e2e-extra", type=int, default=64,
                     help="e2e steps (each appends a token to every sequence)")
-    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

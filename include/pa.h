@@ -250,6 +250,14 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * any bit was set, PA_ERR_CUDA if the stream reports an error, else PA_OK. */
 PA_API pa_status pa_check_device_errors(void* stream, uint32_t* flags);
 
+/* Failure-path check: launches one CTA that waits, with the same bounded wait
+ * the decode pipeline uses on its mbarriers, on an mbarrier that nothing ever
+ * arrives on.  After limit_us microseconds (1 .. 1,000,000) the wait gives up
+ * and sets PA_DEVERR_TIMEOUT in the device error word; the context stays
+ * usable.  The paper has no counterpart; it lets a test exercise the timeout
+ * path without stalling a real pipeline. */
+PA_API pa_status pa_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* Number of decode CTAs pa_decode launches on the current device (one per SM
  * times the resident CTAs per SM), for launch accounting; 0 on error. */
 PA_API int32_t pa_decode_grid_size(void);

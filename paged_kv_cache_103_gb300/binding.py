@@ -60,6 +60,7 @@ SIGNATURES = {
                                 _I32, _F32, _ST, _P, _P]),
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "pa_decode_grid_size": (_I32, []),
+    "pa_selftest_wait_timeout": (_ST, [ctypes.c_uint32, _P]),
 }
 
 
@@ -205,6 +206,13 @@ def pa_check_device_errors(stream=None) -> int:
     if st not in (PA_OK, 4, 7):
         raise PaError(st, "pa_check_device_errors")
     return int(flags.value)
+
+
+def pa_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launches the bounded-wait self-test (see pa.h); read the result with
+    pa_check_device_errors()."""
+    _check(load().pa_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)),
+           "pa_selftest_wait_timeout")
 
 
 def pa_decode_grid_size() -> int:

@@ -57,6 +57,7 @@ constexpr int kMaxStages = 16;
 constexpr int kMaxG = 16;            // query heads per KV head (two 8-wide MMA tiles)
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxCtas = 512;
+constexpr int kMinChunksPerCta = 4;
 constexpr uint32_t kSmemBudget = 113 * 1024;   // dynamic shared memory per CTA (two per SM)
 constexpr uint64_t kWaitLimitNs = 1ull << 30;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
@@ -132,6 +133,20 @@ __device__ __forceinline__ int32_t cta_begin(int64_t c, int64_t W, int64_t C) {
 // its first slot if the pair is where its share begins, else its second.
 __device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t W, int64_t C, int32_t a) {
     return cta_begin(c, W, C) >= a ? 2 * c : 2 * c + 1;
+}
+
+// Folds the softmax state (m2, l2) into (m, l): row maxima in base 2, sums
+// relative to them.  An empty state has m = -inf.
+__device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) {
+        m = m2;
+        l = l2;
+        return;
+    }
+    const float mn = fmaxf(m, m2);
+    l = l * pa::fast_exp2(m - mn) + l2 * pa::fast_exp2(m2 - mn);
+    m = mn;
 }
 
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
@@ -226,7 +241,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 
     const int64_t W = prefix[B];
-    const int64_t C = W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x;
+    // CTAs in use: every one gets at least kMinChunksPerCta chunks, so short
+    // batches are not cut into more partials than their size pays for.
+    int64_t C = W / kMinChunksPerCta;
+    if (C > (int64_t)gridDim.x) C = gridDim.x;
+    if (C < 1) C = 1;
     if ((int64_t)blockIdx.x >= C) return;
     const int32_t lo = cta_begin(blockIdx.x, W, C);
     const int32_t hi = cta_begin(blockIdx.x + 1, W, C);
@@ -336,7 +355,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
         }
 
-        for (int32_t t = warp; t < s.len; t += kConsumerWarps) {
+        // Chunk k lives in stage k % S and stage s is always consumed by warp
+        // s % kConsumerWarps, so consecutive uses of a stage meet the same warp
+        // (a warp owning no stage, when S < kConsumerWarps, takes no chunk).
+        const int s0 = k % S;
+        const int d0 = (warp - s0 % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+        const int32_t first = warp >= S ? s.len : (s0 + d0 < S ? d0 : (S - s0) + warp);
+        for (int32_t t = first; t < s.len;) {
             const int32_t kk = k + t;
             const int stage = kk % S;
             const bool ready =
@@ -466,6 +491,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             __syncwarp();
             if (lane == 0) pa::mbar_arrive(&empty[stage]);
+            // next chunk whose stage belongs to this warp
+            const int next_stage = stage + kConsumerWarps;
+            t += next_stage < S ? kConsumerWarps : (S - stage) + warp;
         }
         k += s.len;
 
@@ -556,17 +584,45 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             pa::named_barrier_sync(1, kConsumerThreads);
             if (flags[1]) {
+                // Last CTA of a split pair: merge the n_cov partials.  Every
+                // thread folds the (m, l) of a strided subset of partials for
+                // all rows, then warps and the four warps combine.
                 __threadfence();
-                if (tid < G) {
-                    float M = -INFINITY;
-                    for (int64_t c = c_first; c <= c_last; ++c)
-                        M = fmaxf(M, __ldcg(p.partials + partial_slot(c, W, C, s.a) * kSlotFloats +
-                                            tid));
-                    float Lsum = 0.f;
-                    for (int64_t c = c_first; c <= c_last; ++c) {
-                        const float* q = p.partials + partial_slot(c, W, C, s.a) * kSlotFloats;
-                        Lsum += pa::fast_exp2(__ldcg(q + tid) - M) * __ldcg(q + kMaxG + tid);
+                const int ncov = (int)(c_last - c_first + 1);
+                // CTA c > c_first starts inside the pair (its first slot);
+                // c_first uses its first slot only if its share starts there.
+                const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == s.a ? 0 : 1);
+                float mr[kMaxG], lr[kMaxG];
+#pragma unroll
+                for (int r = 0; r < kMaxG; ++r) {
+                    mr[r] = -INFINITY;
+                    lr[r] = 0.f;
+                }
+                for (int c = tid; c < ncov; c += kConsumerThreads) {
+                    const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+#pragma unroll
+                    for (int r = 0; r < kMaxG; ++r)
+                        if (r < G) lse_combine(mr[r], lr[r], __ldcg(q + r), __ldcg(q + kMaxG + r));
+                }
+#pragma unroll
+                for (int r = 0; r < kMaxG; ++r) {
+                    if (r >= G) break;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, mr[r], off);
+                        const float l2 = __shfl_xor_sync(0xffffffffu, lr[r], off);
+                        lse_combine(mr[r], lr[r], m2, l2);
                     }
+                    if (lane == 0) {
+                        merge_m[warp * kMaxG + r] = mr[r];
+                        merge_l[warp * kMaxG + r] = lr[r];
+                    }
+                }
+                pa::named_barrier_sync(1, kConsumerThreads);
+                if (tid < G) {
+                    float M = -INFINITY, Lsum = 0.f;
+                    for (int w = 0; w < kConsumerWarps; ++w)
+                        lse_combine(M, Lsum, merge_m[w * kMaxG + tid], merge_l[w * kMaxG + tid]);
                     rowinfo[tid] = M;
                     rowinfo[kMaxG + tid] = 1.f / Lsum;
                 }
@@ -575,8 +631,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int r = e / (D / 2), dp = (e - r * (D / 2)) * 2;
                     const float M = rowinfo[r];
                     float v0 = 0.f, v1 = 0.f;
-                    for (int64_t c = c_first; c <= c_last; ++c) {
-                        const float* q = p.partials + partial_slot(c, W, C, s.a) * kSlotFloats;
+#pragma unroll 4
+                    for (int c = 0; c < ncov; ++c) {
+                        const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
                         const float f = pa::fast_exp2(__ldcg(q + r) - M);
                         const float2 ov =
                             __ldcg(reinterpret_cast<const float2*>(q + 2 * kMaxG + r * D + dp));
@@ -640,20 +697,22 @@ size_t counters_bytes(int32_t B, int32_t H) {
 
 // Pipeline depth that fits the shared-memory budget.  The stage waits use
 // mbarrier phase parity, which is only sound if use u + 1 of a stage is never
-// awaited before use u completed.  Chunk k is issued by producer k % 2 and
-// consumed by warp (segment-relative index) % kConsumerWarps, and chunks k and
-// k + S share a stage; with S a multiple of both warp counts, consecutive uses
-// of a stage always belong to the same producer and the same consumer warp
-// (across pairs, the consumer warps also meet at a barrier), so each waiter is
-// at most one phase ahead.
+// awaited before use u completed.  Chunks k and k + S share stage k % S; the
+// stage is issued by producer k % 2 (S is even) and consumed by warp
+// (k % S) % kConsumerWarps, so consecutive uses of a stage always belong to
+// the same producer and the same consumer warp, and each waiter is at most one
+// phase ahead.
 int choose_stages(int D, int G, int B) {
-    constexpr int kStep = kConsumerWarps % kProducerWarps == 0 ? kConsumerWarps
-                                                               : kConsumerWarps * kProducerWarps;
     const Layout L0 = make_layout(D, G, B, 0);
     if (L0.total >= kSmemBudget) return 0;
     int s = (int)((kSmemBudget - L0.total) / L0.stage_bytes);
     if (s > kMaxStages) s = kMaxStages;
-    return s - s % kStep;
+    s &= ~1;  // each producer owns every other stage
+    // Wider groups make the consumers the limit: give every consumer warp the
+    // same number of stages.  Narrow ones are bound by bytes in flight: keep
+    // the deepest ring.
+    if (G > 2 && s >= kConsumerWarps) s -= s % kConsumerWarps;
+    return s;
 }
 
 template <int D, bool kBF16, int NT>

@@ -19,6 +19,20 @@ std::mutex g_mu;
 unsigned int* g_error_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 
+// One CTA waits, with the pipelines' own bounded wait, on an mbarrier that
+// nothing ever arrives on; the wait gives up after limit_ns and reports it.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, unsigned int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        pa::mbar_init(&bar, 1);
+        pa::fence_barrier_init();
+    }
+    __syncthreads();
+    const bool done = pa::mbar_wait(&bar, 0, limit_ns);
+    if (!__all_sync(0xffffffffu, done) && threadIdx.x == 0)
+        pa::raise_error(err, PA_DEVERR_TIMEOUT);
+}
+
 }  // namespace
 
 namespace pa {
@@ -82,6 +96,15 @@ PA_API pa_status pa_check_device_errors(void* stream, uint32_t* flags) {
     if (host & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
     if (host) return PA_ERR_BOUNDS;
     return PA_OK;
+}
+
+PA_API pa_status pa_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 1000000) return PA_ERR_INVALID;
+    unsigned int* err = pa::device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (uint64_t)limit_us * 1000u, err);
+    return pa::cuda_status(cudaGetLastError());
 }
 
 PA_API pa_status pa_decode_workspace_init(void* workspace, size_t bytes, void* stream) {

@@ -325,3 +325,52 @@ def test_kv_concurrency_printed_on_the_page(oracle_mod):
     for budget, tok_bytes, max_len, expected in ([int(x) for x in l] for l in lines):
         assert tok_bytes == per_tok
         assert budget // (per_tok * max_len) == expected
+
+
+# ------------------------------------------------------- append and copy-on-write
+def test_scatter_at_allocator_slots_then_table_walk_is_contiguous(oracle_mod):
+    """K/V written with the oracle's scatter at the allocator's slots, read back
+    through the allocator's table, give SDPA on the contiguous rows."""
+    bs, N, n, Hkv, d = 16, 40, 37, 2, 64
+    order = np.random.default_rng(21).permutation(N)
+    m = oracle_mod.BlockManagerModel(N, bs, order)
+    m.allocate(0, 0)
+    slots = [m.append_slot(0)[0] for _ in range(n)]
+    g = torch.Generator().manual_seed(22)
+    K = torch.randn(n, Hkv, d, generator=g).to(torch.float16)
+    V = torch.randn(n, Hkv, d, generator=g).to(torch.float16)
+    q = torch.randn(1, 4, d, generator=g).to(torch.float16)
+    kc = torch.full((N, bs, Hkv, d), float("nan"), dtype=torch.float16)
+    vc = kc.clone()
+    oracle_mod.reshape_and_cache(K, V, np.array(slots), kc, vc)
+    tbl, lens = m.export([0])
+    out = oracle_mod.decode(_bits(q), _bits(kc), _bits(vc), tbl, lens, 0.125, F16)
+    ref = _contiguous_reference(q[0].double().numpy(), K.double().numpy(), V.double().numpy(),
+                                0.125, 2)
+    np.testing.assert_allclose(out[0], ref, rtol=1e-11, atol=1e-13)
+    # padding slots are skipped
+    kc2 = kc.clone()
+    oracle_mod.reshape_and_cache(K[:1] + 1, V[:1] + 1, np.array([-1]), kc2, vc)
+    assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16))
+
+
+def test_cow_copy_read_through_the_copy_equals_the_original(oracle_mod):
+    """After a fork and an append into the shared partial block, the copied
+    block holds the shared rows, so both sequences still see the same prefix."""
+    bs, N, Hkv, d = 16, 12, 2, 64
+    m = oracle_mod.BlockManagerModel(N, bs, np.random.default_rng(23).permutation(N))
+    m.allocate(0, 20)
+    m.fork(0, 1)
+    g = torch.Generator().manual_seed(24)
+    kc = torch.randn(N, bs, Hkv, d, generator=g).to(torch.bfloat16)
+    vc = torch.randn(N, bs, Hkv, d, generator=g).to(torch.bfloat16)
+    q = torch.randn(2, 4, d, generator=g).to(torch.bfloat16)
+    tbl0, lens0 = m.export([0, 1], 2)
+    before = oracle_mod.decode(_bits(q), _bits(kc), _bits(vc), tbl0, lens0, 0.125, BF16)
+    slot, cow = m.append_slot(1)
+    assert cow is not None
+    oracle_mod.copy_blocks([kc], [vc], [cow])
+    tbl1, _ = m.export([0, 1], 2)
+    assert tbl1[1, 1] == cow[1] and tbl1[0, 1] == cow[0]
+    after = oracle_mod.decode(_bits(q), _bits(kc), _bits(vc), tbl1, lens0, 0.125, BF16)
+    assert np.array_equal(before, after)
