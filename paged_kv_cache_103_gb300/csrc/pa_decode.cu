@@ -76,20 +76,22 @@ struct DecodeParams {
 
 // Dynamic shared-memory carve-up; the same function runs on host and device.
 struct Layout {
-    uint32_t stage_bytes, merge_o, merge_m, merge_l, fac, rowinfo, bars, flags, scan, prefix, total;
+    uint32_t stage_bytes, merge_o, merge_m, merge_l, rowinfo, bars, flags, scan, prefix, total;
 };
 
-__host__ __device__ inline Layout make_layout(int D, int G, int B, int stages) {
+// Merge slots (two when the warps merge asynchronously, pairs alternating;
+// one when they merge together): each holds every consumer warp's
+// unnormalised output [W][G][D], row maxima [W][16] and row sums [W][16].
+__host__ __device__ inline Layout make_layout(int D, int G, int B, int stages, int slots) {
     Layout L;
     L.stage_bytes = 2u * kChunk * D * 2;
-    L.merge_o = stages * L.stage_bytes;                              // [W][G][D] fp32
-    L.merge_m = L.merge_o + kConsumerWarps * G * D * 4;              // [W][16]
-    L.merge_l = L.merge_m + kConsumerWarps * kMaxG * 4;              // [W][16]
-    L.fac = L.merge_l + kConsumerWarps * kMaxG * 4;                  // [W][16]
-    L.rowinfo = L.fac + kConsumerWarps * kMaxG * 4;                  // [2][16]
-    L.bars = L.rowinfo + 2 * kMaxG * 4;                              // full[], empty[]
-    L.flags = L.bars + 2 * kMaxStages * 8;
-    L.scan = L.flags + 16;
+    L.merge_o = stages * L.stage_bytes;                              // [slots][W][G][D] fp32
+    L.merge_m = L.merge_o + slots * kConsumerWarps * G * D * 4;      // [slots][W][16]
+    L.merge_l = L.merge_m + slots * kConsumerWarps * kMaxG * 4;      // [slots][W][16]
+    L.rowinfo = L.merge_l + slots * kConsumerWarps * kMaxG * 4;      // [slots][2 + W][16]
+    L.bars = L.rowinfo + slots * (2 + kConsumerWarps) * kMaxG * 4;   // full[], empty[]
+    L.flags = L.bars + 2 * kMaxStages * 8;                           // count[2] free[2] flag[2]
+    L.scan = L.flags + 32;
     L.prefix = L.scan + 32 * 4;                                      // [B + 1] int32
     L.total = 1024 + L.prefix + (uint32_t)(B + 1) * 4;               // + alignment slack
     return L;
@@ -135,6 +137,20 @@ __device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t W, int64_t C,
     return cta_begin(c, W, C) >= a ? 2 * c : 2 * c + 1;
 }
 
+// Waits, for at most about limit_ns, until the shared-memory word holds
+// `value`; returns false if the limit ran out.
+__device__ __forceinline__ bool wait_flag(const int* flag, int value, uint64_t limit_ns) {
+    const volatile int* f = flag;
+    if (*f == value) return true;
+    const uint64_t t0 = pa::global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 64; ++k)
+            if (*f == value) return true;
+        if (pa::global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Folds the softmax state (m2, l2) into (m, l): row maxima in base 2, sums
 // relative to them.  An empty state has m = -inf.
 __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
@@ -163,24 +179,25 @@ __device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t
     return ((((b * halves + h) << rows_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
 }
 
-template <int D, bool kBF16, int NT>
+template <int D, bool kBF16, int NT, bool kAsync>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
     constexpr uint32_t kHalves = D / 64;
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
-    const Layout L = make_layout(D, G, B, S);
+    const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* merge_o = reinterpret_cast<float*>(smem + L.merge_o);
     float* merge_m = reinterpret_cast<float*>(smem + L.merge_m);
     float* merge_l = reinterpret_cast<float*>(smem + L.merge_l);
-    float* fac = reinterpret_cast<float*>(smem + L.fac);
-    float* rowinfo = reinterpret_cast<float*>(smem + L.rowinfo);  // M[16], 1/L or L [16]
+    float* rowinfo = reinterpret_cast<float*>(smem + L.rowinfo);  // per slot: M[16], 1/L[16]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kMaxStages;
-    int* flags = reinterpret_cast<int*>(smem + L.flags);
+    int* slot_count = reinterpret_cast<int*>(smem + L.flags);      // arrivals per merge slot
+    int* slot_free = slot_count + 2;  // a slot takes pair j once it holds the value j
+    int* slot_flag = slot_count + 4;  // "this CTA is the pair's last" for the slot's merge
     int32_t* scan = reinterpret_cast<int32_t*>(smem + L.scan);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
 
@@ -217,6 +234,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 pa::mbar_init(&empty[s], 1);
             }
             pa::fence_barrier_init();
+            slot_count[0] = slot_count[1] = 0;
+            slot_free[0] = 0;
+            slot_free[1] = 1;
         }
         __syncthreads();
         int32_t run = x - local;
@@ -326,23 +346,190 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     int32_t k = 0;
     bool dead = false;
 
-    for (int32_t pos = lo; pos < hi;) {
-        const Segment s = find_segment(prefix, B, Hkv, pos, hi);
-        const int32_t n = clamp_len(__ldg(p.context_lens + s.i), max_len);
-        const int32_t head0 = s.g * G;
-
-        // Q^T fragments (MMA B operand): lane holds query head 8 nt + cr.
-        uint32_t qb[NT][D / 16][2];
+    // Q^T fragments (MMA B operand) of a pair: lane holds query head 8 nt + cr.
+    uint32_t qb[NT][D / 16][2];
+    auto load_q = [&](const Segment& sg) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hq = 8 * nt + cr;
-            const uint16_t* qrow = p.q + ((int64_t)s.i * p.H + head0 + hq) * D + cc;
+            const uint16_t* qrow = p.q + ((int64_t)sg.i * p.H + sg.g * G + hq) * D + cc;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 qb[nt][ks][0] = hq < G ? ld_u32(qrow + ks * 16) : 0u;
                 qb[nt][ks][1] = hq < G ? ld_u32(qrow + ks * 16 + 8) : 0u;
             }
         }
+    };
+    constexpr int kSlotFloats = 2 * kMaxG + kMaxG * D;
+    // The merge of one pair by a group of `nthr` threads (`t` = index in the
+    // group, `sync` = the group's barrier): the final output if the pair lies
+    // in this CTA's share, else this CTA's partial, and, if this CTA is the
+    // pair's last, the merge of all CTAs' partials.  `so`, `sm`, `sl` hold the
+    // consumer warps' unnormalised outputs, row maxima and row sums; `rinfo`
+    // receives per row M = max_w m_w, L = sum_w 2^(m_w - M) l_w and the factors
+    // f_w = 2^(m_w - M) (times 1/L for a final output).
+    auto merge_pair = [&](const Segment& sg, int32_t h0, float* so, float* sm, float* sl,
+                          float* rinfo, int* flag, int t, int nthr, auto sync) {
+        const bool whole = sg.c0 == 0 && sg.len == sg.nc;
+        if (t < G) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm[w * kMaxG + t]);
+            float f[kConsumerWarps], Lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                f[w] = pa::fast_exp2(sm[w * kMaxG + t] - M);
+                Lsum += f[w] * sl[w * kMaxG + t];
+            }
+            const float scale = whole ? 1.f / Lsum : 1.f;
+            rinfo[t] = M;
+            rinfo[kMaxG + t] = Lsum;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) rinfo[(2 + w) * kMaxG + t] = f[w] * scale;
+        }
+        sync();
+        // 4 consecutive head-dim values of one row, combined over the warps.
+        auto combined4 = [&](int e) -> float4 {
+            const int r = e / (D / 4), d4 = (e - r * (D / 4)) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = rinfo[(2 + w) * kMaxG + r];
+                const float4 ov = *reinterpret_cast<const float4*>(&so[(w * G + r) * D + d4]);
+                v.x += f * ov.x;
+                v.y += f * ov.y;
+                v.z += f * ov.z;
+                v.w += f * ov.w;
+            }
+            return v;
+        };
+        auto store4 = [&](int r, int d4, float4 v) {
+            uint2 packed;
+            packed.x = pa::pack2<kBF16>(v.x, v.y);
+            packed.y = pa::pack2<kBF16>(v.z, v.w);
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)sg.i * p.H + h0 + r) * D + d4) = packed;
+        };
+        if (whole) {
+            for (int e = t; e < G * D / 4; e += nthr)
+                store4(e / (D / 4), (e % (D / 4)) * 4, combined4(e));
+            return;
+        }
+        // Partial result of this CTA for a pair split between CTAs.
+        const int64_t c_first = ((int64_t)(sg.a + 1) * C - 1) / W;
+        const int64_t c_last = ((int64_t)(sg.a + sg.nc) * C - 1) / W;
+        float* ps = p.partials + partial_slot(blockIdx.x, W, C, sg.a) * kSlotFloats;
+        for (int e = t; e < G * D / 4; e += nthr) {
+            const int r = e / (D / 4), d4 = (e - r * (D / 4)) * 4;
+            *reinterpret_cast<float4*>(&ps[2 * kMaxG + r * D + d4]) = combined4(e);
+        }
+        if (t < G) {
+            ps[t] = rinfo[t];
+            ps[kMaxG + t] = rinfo[kMaxG + t];
+        }
+        // Publish: the group barrier orders every thread's stores before thread
+        // 0's fence, whose release covers them (cumulativity); the ticket names
+        // the pair's last CTA.
+        sync();
+        if (t == 0) {
+            __threadfence();
+            int32_t* ctr = p.counters + (int64_t)sg.i * Hkv + sg.g;
+            const int prev = atomicAdd(ctr, 1);
+            const int last = prev == (int)(c_last - c_first);
+            if (last) {
+                atomicExch(ctr, 0);
+                __threadfence();
+            }
+            *flag = last;
+        }
+        sync();
+        if (!*flag) return;
+        // Last CTA of the pair: merge the n_cov partials.  Each thread folds the
+        // (m, l) of a strided subset of partials for every row, then warps, then
+        // (for four warps) the warps through shared memory.
+        const int ncov = (int)(c_last - c_first + 1);
+        // CTA c > c_first starts inside the pair (its first slot); c_first
+        // uses its first slot only if its share starts there.
+        const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == sg.a ? 0 : 1);
+        float mr[kMaxG], lr[kMaxG];
+#pragma unroll
+        for (int r = 0; r < kMaxG; ++r) {
+            mr[r] = -INFINITY;
+            lr[r] = 0.f;
+        }
+        for (int c = t; c < ncov; c += nthr) {
+            const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+#pragma unroll
+            for (int r = 0; r < kMaxG; ++r)
+                if (r < G) lse_combine(mr[r], lr[r], __ldcg(q + r), __ldcg(q + kMaxG + r));
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxG; ++r) {
+            if (r >= G) break;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, mr[r], off);
+                const float l2 = __shfl_xor_sync(0xffffffffu, lr[r], off);
+                lse_combine(mr[r], lr[r], m2, l2);
+            }
+            if (nthr > 32) {
+                if (lane == 0) {  // sm / sl are free again: reuse them per warp
+                    sm[warp * kMaxG + r] = mr[r];
+                    sl[warp * kMaxG + r] = lr[r];
+                }
+            } else if (lane == r) {
+                rinfo[r] = mr[r];
+                rinfo[kMaxG + r] = 1.f / lr[r];
+            }
+        }
+        if (nthr > 32) {
+            sync();
+            if (t < G) {
+                float M = -INFINITY, Lsum = 0.f;
+                for (int w = 0; w < nthr / 32; ++w)
+                    lse_combine(M, Lsum, sm[w * kMaxG + t], sl[w * kMaxG + t]);
+                rinfo[t] = M;
+                rinfo[kMaxG + t] = 1.f / Lsum;
+            }
+        }
+        sync();
+        // Per-partial factors 2^(m_c - M) / L, staged in `so` (its W * G * D
+        // floats are free now) when they fit, else recomputed.
+        const bool staged = ncov <= kConsumerWarps * D;
+        for (int e = t; staged && e < ncov * G; e += nthr) {
+            const int c = e / G, r = e - c * G;
+            const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+            so[e] = pa::fast_exp2(__ldcg(q + r) - rinfo[r]) * rinfo[kMaxG + r];
+        }
+        sync();
+        for (int e = t; e < G * D / 4; e += nthr) {
+            const int r = e / (D / 4), d4 = (e - r * (D / 4)) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int c = 0; c < ncov; ++c) {
+                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+                const float f = staged ? so[c * G + r]
+                                       : pa::fast_exp2(__ldcg(q + r) - rinfo[r]) * rinfo[kMaxG + r];
+                const float4 ov =
+                    __ldcg(reinterpret_cast<const float4*>(q + 2 * kMaxG + r * D + d4));
+                v.x += f * ov.x;
+                v.y += f * ov.y;
+                v.z += f * ov.z;
+                v.w += f * ov.w;
+            }
+            store4(r, d4, v);
+        }
+    };
+
+    Segment s{};
+    int32_t n = 0;
+    int32_t segn = 0;  // pairs this CTA has walked (selects the merge slot)
+    if (lo < hi) {
+        s = find_segment(prefix, B, Hkv, lo, hi);
+        n = clamp_len(__ldg(p.context_lens + s.i), max_len);
+        load_q(s);
+    }
+    for (int32_t pos = lo; pos < hi;) {
+        const int32_t head0 = s.g * G;
         // Running state for the heads 8 nt + cc + {0, 1} this lane tracks.
         float m_run[NT][2], l_run[NT][2];
         float o[D / 16][NT][4];  // O^T: rows = head_dim, columns = heads
@@ -497,7 +684,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         k += s.len;
 
-        // ---- merge the consumer warps' states for this pair
+        // ---- hand this warp's state for the pair to the pair's merge slot.
+        // The four warps do not wait for each other: each deposits its state
+        // in slot (pair index & 1) and the last to arrive merges the pair
+        // while the others go on to the next one.
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -506,10 +696,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 8);
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
+                l_run[nt][j] = v;
+            }
+        const int slot = kAsync ? (segn & 1) : 0;
+        const int slot_floats_o = kConsumerWarps * G * D;
+        float* so = merge_o + slot * slot_floats_o;
+        float* sm = merge_m + slot * (kConsumerWarps * kMaxG);
+        float* sl = merge_l + slot * (kConsumerWarps * kMaxG);
+        float* rinfo = rowinfo + slot * (2 + kConsumerWarps) * kMaxG;
+        if constexpr (kAsync) {
+            // The slot is free once the merge of pair segn - 2 has read it.
+            if (!__all_sync(0xffffffffu, wait_flag(&slot_free[slot], segn, kWaitLimitNs)) &&
+                lane == 0)
+                pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+            __threadfence_block();
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
                 const int h = 8 * nt + cc + j;
                 if (cr == 0 && h < G) {
-                    merge_m[warp * kMaxG + h] = m_run[nt][j];
-                    merge_l[warp * kMaxG + h] = v;
+                    sm[warp * kMaxG + h] = m_run[nt][j];
+                    sl[warp * kMaxG + h] = l_run[nt][j];
                 }
             }
 #pragma unroll
@@ -519,135 +728,51 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int h = 8 * nt + cc + (e & 1);
-                    if (h < G)
-                        merge_o[(warp * G + h) * D + mt * 16 + cr + 8 * (e >> 1)] = o[mt][nt][e];
+                    if (h < G) so[(warp * G + h) * D + mt * 16 + cr + 8 * (e >> 1)] = o[mt][nt][e];
                 }
-        pa::named_barrier_sync(1, kConsumerThreads);
 
-        const bool whole = (s.c0 == 0 && s.len == s.nc);
-        if (tid < G) {
-            float M = -INFINITY;
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxG + tid]);
-            float Lsum = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = pa::fast_exp2(merge_m[w * kMaxG + tid] - M);
-                fac[w * kMaxG + tid] = f;
-                Lsum += f * merge_l[w * kMaxG + tid];
-            }
-            rowinfo[tid] = M;
-            rowinfo[kMaxG + tid] = whole ? 1.f / Lsum : Lsum;
+        // The next pair's length and query fragments load while this one merges.
+        const int32_t npos = pos + s.len;
+        Segment sn = s;
+        int32_t n_next = n;
+        if (npos < hi) {
+            sn = find_segment(prefix, B, Hkv, npos, hi);
+            n_next = clamp_len(__ldg(p.context_lens + sn.i), max_len);
+            load_q(sn);
         }
-        pa::named_barrier_sync(1, kConsumerThreads);
 
-        constexpr int kSlotFloats = 2 * kMaxG + kMaxG * D;
-        if (whole) {
-            for (int e = tid; e < G * D / 2; e += kConsumerThreads) {
-                const int r = e / (D / 2), dp = (e - r * (D / 2)) * 2;
-                float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float f = fac[w * kMaxG + r];
-                    const float2 ov =
-                        *reinterpret_cast<const float2*>(&merge_o[(w * G + r) * D + dp]);
-                    v0 += f * ov.x;
-                    v1 += f * ov.y;
+        if constexpr (kAsync) {
+            // The four warps do not wait for each other: the last one to
+            // deposit its state merges the pair while the others go on.
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&slot_count[slot], 1) == kConsumerWarps - 1;
+                if (last) __threadfence_block();
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+                __syncwarp();
+                merge_pair(s, head0, so, sm, sl, rinfo, &slot_flag[slot], lane, 32,
+                           [] { __syncwarp(); });
+                __syncwarp();
+                if (lane == 0) {
+                    slot_count[slot] = 0;
+                    __threadfence_block();
+                    *reinterpret_cast<volatile int*>(&slot_free[slot]) = segn + 2;
                 }
-                const float inv = rowinfo[kMaxG + r];
-                *reinterpret_cast<uint32_t*>(p.out + ((int64_t)s.i * p.H + head0 + r) * D + dp) =
-                    pa::pack2<kBF16>(v0 * inv, v1 * inv);
             }
         } else {
-            // Partial result of this CTA for a pair split between CTAs.
-            const int64_t c_first = ((int64_t)(s.a + 1) * C - 1) / W;
-            const int64_t c_last = ((int64_t)(s.a + s.nc) * C - 1) / W;
-            float* ps = p.partials + partial_slot(blockIdx.x, W, C, s.a) * kSlotFloats;
-            if (tid < G) {
-                ps[tid] = rowinfo[tid];
-                ps[kMaxG + tid] = rowinfo[kMaxG + tid];
-            }
-            for (int e = tid; e < G * D; e += kConsumerThreads) {
-                const int r = e / D, dim = e - r * D;
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    v += fac[w * kMaxG + r] * merge_o[(w * G + r) * D + dim];
-                ps[2 * kMaxG + r * D + dim] = v;
-            }
-            __threadfence();
+            // All four warps meet and merge the pair together.
             pa::named_barrier_sync(1, kConsumerThreads);
-            if (tid == 0) {
-                int32_t* ctr = p.counters + (int64_t)s.i * Hkv + s.g;
-                const int prev = atomicAdd(ctr, 1);
-                const int last = prev == (int)(c_last - c_first);
-                if (last) atomicExch(ctr, 0);
-                flags[1] = last;
-            }
+            merge_pair(s, head0, so, sm, sl, rinfo, &slot_flag[slot], tid, kConsumerThreads,
+                       [] { pa::named_barrier_sync(1, kConsumerThreads); });
             pa::named_barrier_sync(1, kConsumerThreads);
-            if (flags[1]) {
-                // Last CTA of a split pair: merge the n_cov partials.  Every
-                // thread folds the (m, l) of a strided subset of partials for
-                // all rows, then warps and the four warps combine.
-                __threadfence();
-                const int ncov = (int)(c_last - c_first + 1);
-                // CTA c > c_first starts inside the pair (its first slot);
-                // c_first uses its first slot only if its share starts there.
-                const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == s.a ? 0 : 1);
-                float mr[kMaxG], lr[kMaxG];
-#pragma unroll
-                for (int r = 0; r < kMaxG; ++r) {
-                    mr[r] = -INFINITY;
-                    lr[r] = 0.f;
-                }
-                for (int c = tid; c < ncov; c += kConsumerThreads) {
-                    const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-#pragma unroll
-                    for (int r = 0; r < kMaxG; ++r)
-                        if (r < G) lse_combine(mr[r], lr[r], __ldcg(q + r), __ldcg(q + kMaxG + r));
-                }
-#pragma unroll
-                for (int r = 0; r < kMaxG; ++r) {
-                    if (r >= G) break;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float m2 = __shfl_xor_sync(0xffffffffu, mr[r], off);
-                        const float l2 = __shfl_xor_sync(0xffffffffu, lr[r], off);
-                        lse_combine(mr[r], lr[r], m2, l2);
-                    }
-                    if (lane == 0) {
-                        merge_m[warp * kMaxG + r] = mr[r];
-                        merge_l[warp * kMaxG + r] = lr[r];
-                    }
-                }
-                pa::named_barrier_sync(1, kConsumerThreads);
-                if (tid < G) {
-                    float M = -INFINITY, Lsum = 0.f;
-                    for (int w = 0; w < kConsumerWarps; ++w)
-                        lse_combine(M, Lsum, merge_m[w * kMaxG + tid], merge_l[w * kMaxG + tid]);
-                    rowinfo[tid] = M;
-                    rowinfo[kMaxG + tid] = 1.f / Lsum;
-                }
-                pa::named_barrier_sync(1, kConsumerThreads);
-                for (int e = tid; e < G * D / 2; e += kConsumerThreads) {
-                    const int r = e / (D / 2), dp = (e - r * (D / 2)) * 2;
-                    const float M = rowinfo[r];
-                    float v0 = 0.f, v1 = 0.f;
-#pragma unroll 4
-                    for (int c = 0; c < ncov; ++c) {
-                        const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-                        const float f = pa::fast_exp2(__ldcg(q + r) - M);
-                        const float2 ov =
-                            __ldcg(reinterpret_cast<const float2*>(q + 2 * kMaxG + r * D + dp));
-                        v0 += f * ov.x;
-                        v1 += f * ov.y;
-                    }
-                    const float inv = rowinfo[kMaxG + r];
-                    *reinterpret_cast<uint32_t*>(p.out + ((int64_t)s.i * p.H + head0 + r) * D +
-                                                 dp) = pa::pack2<kBF16>(v0 * inv, v1 * inv);
-                }
-            }
         }
-        pa::named_barrier_sync(1, kConsumerThreads);
-        pos += s.len;
+        ++segn;
+        s = sn;
+        n = n_next;
+        pos = npos;
     }
 }
 
@@ -702,8 +827,12 @@ size_t counters_bytes(int32_t B, int32_t H) {
 // (k % S) % kConsumerWarps, so consecutive uses of a stage always belong to
 // the same producer and the same consumer warp, and each waiter is at most one
 // phase ahead.
+// Narrow groups (G <= 2) merge asynchronously: per pair end the math is small
+// and the ring depth decides; wider groups merge with all four warps.
+bool async_merge(int G) { return G <= 2; }
+
 int choose_stages(int D, int G, int B) {
-    const Layout L0 = make_layout(D, G, B, 0);
+    const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1);
     if (L0.total >= kSmemBudget) return 0;
     int s = (int)((kSmemBudget - L0.total) / L0.stage_bytes);
     if (s > kMaxStages) s = kMaxStages;
@@ -715,10 +844,10 @@ int choose_stages(int D, int G, int B) {
     return s;
 }
 
-template <int D, bool kBF16, int NT>
+template <int D, bool kBF16, int NT, bool kAsync>
 pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& prm,
                  size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<D, kBF16, NT>;
+    auto kern = paged_decode_kernel<D, kBF16, NT, kAsync>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -733,8 +862,9 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParam
 template <int D, bool kBF16>
 pa_status launch_g(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& prm,
                    size_t smem, cudaStream_t stream) {
-    return prm.G <= 8 ? launch<D, kBF16, 1>(km, vm, prm, smem, stream)
-                      : launch<D, kBF16, 2>(km, vm, prm, smem, stream);
+    if (async_merge(prm.G)) return launch<D, kBF16, 1, true>(km, vm, prm, smem, stream);
+    return prm.G <= 8 ? launch<D, kBF16, 1, false>(km, vm, prm, smem, stream)
+                      : launch<D, kBF16, 2, false>(km, vm, prm, smem, stream);
 }
 
 }  // namespace
@@ -808,7 +938,7 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
     prm.num_blocks = num_blocks;
     prm.stages = stages;
     prm.scale_log2 = scale * kLog2e;
-    const size_t smem = make_layout(d, G, B, stages).total;
+    const size_t smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1).total;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 128)

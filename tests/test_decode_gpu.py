@@ -195,3 +195,14 @@ def test_bad_table_entries_are_flagged_not_followed():
     assert binding.pa_check_device_errors() == 0
     assert_close(out.cpu(), oracle_decode(w, host["q"], host["k_cache"], host["v_cache"], tbl,
                                           lens), "after-bad")
+
+
+def test_single_long_pair_split_over_every_cta_d64():
+    """One sequence, one KV head, head_dim 64: the pair is cut into as many
+    partials as there are CTAs, more than the merge can stage at once."""
+    w, host, tbl, lens = _custom(1, 2, 1, 64, 16, [200000], dtype=torch.bfloat16)
+    run = GpuRun(w, host)
+    out = run.decode(tbl, lens)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), oracle_decode(w, host["q"], host["k_cache"], host["v_cache"], tbl,
+                                          lens), "long-d64")
