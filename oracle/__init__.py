@@ -31,6 +31,8 @@ Contents:
 * :class:`BlockManagerModel` -- the allocator, restated from [P1] section 3.2
   and [P3] section 3.3.
 * :func:`kv_bytes_per_token` / :func:`kv_cache_bytes` -- the closed forms.
+* :func:`reshape_and_cache_fp8`, :func:`decode_fp8`, :func:`e4m3_encode` -- the
+  FP8 KV cache (a reading, see the comment above :data:`E4M3_MAX`).
 """
 from __future__ import annotations
 
@@ -83,6 +85,11 @@ def _load():
                                           i32, i32, P]
         lib.pa_oracle_to_double.restype = ctypes.c_int
         lib.pa_oracle_to_double.argtypes = [P, i64, i32, P]
+        lib.pa_oracle_e4m3_to_double.restype = ctypes.c_int
+        lib.pa_oracle_e4m3_to_double.argtypes = [P, i64, P]
+        lib.pa_oracle_decode_fp8.restype = ctypes.c_int
+        lib.pa_oracle_decode_fp8.argtypes = [P, i32, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                             i64, f64, P]
         _lib = lib
     return _lib
 
@@ -147,6 +154,103 @@ def weights(q, k_cache, block_tables, context_lens, scale: float, dtype: int, i:
     if rc:
         raise ValueError("pa_oracle_weights failed (%d)" % rc)
     return w[: int(lens[i])]
+
+
+# ----------------------------------------------------------------- FP8 KV cache
+# Reading (the pages only say that quantising the KV cache to 8 bits halves its
+# bytes, "LLM推理优化技术地图：从KV Cache到量化与投机解码" section 4.3): codes are OCP
+# FP8 E4M3 (bias 7, no infinities, NaN at S.1111.111, largest finite 448); each
+# (token, KV head) row of head_dim values gets its own fp32 scale
+# s = fl32(amax / 448), amax = max |x| over the row (exact in fp32), and code
+# = RNE-saturating E4M3 of fl32(x / s) (fp32 division); an all-zero row gets
+# s = 0 and zero codes.  Scales are laid out [num_blocks][Hkv][block_size].
+E4M3_MAX = 448.0
+
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """Exact values of E4M3 codes (uint8)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    y = np.empty(c.shape, dtype=np.float64)
+    _load().pa_oracle_e4m3_to_double(_ptr(c), c.size, _ptr(y))
+    return y
+
+
+_E4M3_POS = None
+
+
+def _e4m3_positive_table():
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        codes = np.arange(0x7F, dtype=np.uint8)          # 0x00 .. 0x7E: all finite >= 0
+        _E4M3_POS = e4m3_to_double(codes)
+    return _E4M3_POS
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round fp32 values to the nearest E4M3 code, ties to the even code,
+    saturating at +-448 (NaN maps to 0x7F with its sign)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals = _e4m3_positive_table()                         # ascending, 127 entries
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((hi & 1) == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == vals[hi], hi, code).astype(np.uint8)
+    code = code | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    code = np.where(np.isnan(x), (0x7F | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8), code)
+    return code.astype(np.uint8)
+
+
+def quantize_rows(x_fp32):
+    """Quantise rows (last axis) of fp32 values: returns (codes uint8, scales fp32)."""
+    x = np.asarray(x_fp32, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1).astype(np.float32)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1), s).astype(np.float32)
+    codes = e4m3_encode((x / safe[..., None]).astype(np.float32))
+    codes = np.where((s == 0)[..., None], 0, codes).astype(np.uint8)
+    return codes, s
+
+
+def reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_codes, v_codes, k_scale, v_scale):
+    """The FP8 KV append: token t's K/V rows [Hkv, d] (fp16/bf16 host tensors)
+    are quantised per KV head and written to slot s (codes at
+    [s // bs, s % bs, h, :], scale at [s // bs, h, s % bs]); negative slots skip."""
+    bs = k_codes.shape[1]
+    kq, ks = quantize_rows(k_new.float().numpy())
+    vq, vs = quantize_rows(v_new.float().numpy())
+    for t in range(k_new.shape[0]):
+        s = int(slot_mapping[t])
+        if s < 0:
+            continue
+        k_codes[s // bs, s % bs] = kq[t]
+        v_codes[s // bs, s % bs] = vq[t]
+        k_scale[s // bs, :, s % bs] = ks[t]
+        v_scale[s // bs, :, s % bs] = vs[t]
+
+
+def decode_fp8(q, q_dtype: int, k_codes, v_codes, k_scale, v_scale, block_tables,
+               context_lens, scale: float) -> np.ndarray:
+    """fp64 paged decode over an FP8 cache: the attention of :func:`decode` on
+    the dequantised rows code_value * scale."""
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    tbl = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, H, d = q.shape
+    N, bs, Hkv, _ = kc.shape
+    out = np.empty((B, H, d), dtype=np.float64)
+    rc = _load().pa_oracle_decode_fp8(_ptr(q), q_dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                      _ptr(tbl), tbl.shape[1], _ptr(lens), B, H, Hkv, d, bs, N,
+                                      float(scale), _ptr(out))
+    if rc:
+        raise ValueError("pa_oracle_decode_fp8 failed (%d)" % rc)
+    return out
 
 
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache) -> None:

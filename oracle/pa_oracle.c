@@ -237,3 +237,88 @@ int pa_oracle_to_double(const uint16_t* x, int64_t count, int32_t dtype, double*
     for (int64_t t = 0; t < count; ++t) y[t] = orc_elem(x, t, dtype);
     return ORC_OK;
 }
+
+/*
+ * FP8 KV cache (OCP 8-bit floating point, E4M3: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits, no infinities, 0x7F / 0xFF are NaN, largest
+ * finite 448).  The cache holds codes [num_blocks][bs][Hkv][d] and one fp32
+ * scale per token and KV head, laid out [num_blocks][Hkv][bs]; element j of
+ * K is code_value * scale.  Same attention as pa_oracle_decode otherwise.
+ */
+static double orc_e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);          /* (m / 8) * 2^-6 */
+    else
+        v = ldexp((double)(m + 8), e - 10); /* (1 + m / 8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+int pa_oracle_e4m3_to_double(const uint8_t* x, int64_t count, double* y) {
+    for (int64_t t = 0; t < count; ++t) y[t] = orc_e4m3_to_double(x[t]);
+    return ORC_OK;
+}
+
+int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_codes,
+                         const uint8_t* v_codes, const float* k_scale, const float* v_scale,
+                         const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* context_lens, int32_t B, int32_t H, int32_t Hkv,
+                         int32_t d, int32_t block_size, int64_t num_blocks, double scale,
+                         double* out) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || d <= 0 || block_size <= 0 ||
+        (q_dtype != 0 && q_dtype != 1))
+        return ORC_ERR_ARG;
+    const int32_t G = H / Hkv;
+    int32_t nmax = 1;
+    for (int32_t i = 0; i < B; ++i) {
+        if (context_lens[i] < 0) return ORC_ERR_ARG;
+        if (context_lens[i] > nmax) nmax = context_lens[i];
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    if (!s) return ORC_ERR_ARG;
+    for (int32_t i = 0; i < B; ++i) {
+        const int32_t n = context_lens[i];
+        for (int32_t h = 0; h < H; ++h) {
+            const int32_t g = h / G;
+            double* o = out + ((int64_t)i * H + h) * d;
+            for (int32_t k = 0; k < d; ++k) o[k] = 0.0;
+            if (n == 0) continue;
+            const int64_t qoff = ((int64_t)i * H + h) * d;
+            for (int32_t j = 0; j < n; ++j) {
+                int32_t lb = j / block_size;
+                if (lb >= max_blocks) { free(s); return ORC_ERR_TABLE; }
+                int32_t pb = block_tables[(int64_t)i * max_blocks + lb];
+                if (pb < 0 || (int64_t)pb >= num_blocks) { free(s); return ORC_ERR_TABLE; }
+                int64_t row = (((int64_t)pb * block_size + (j % block_size)) * Hkv + g) * d;
+                double ks = (double)k_scale[((int64_t)pb * Hkv + g) * block_size + j % block_size];
+                double acc = 0.0;
+                for (int32_t k = 0; k < d; ++k)
+                    acc += orc_elem(q, qoff + k, q_dtype) * (orc_e4m3_to_double(k_codes[row + k]) * ks);
+                s[j] = scale * acc;
+            }
+            double m = s[0];
+            for (int32_t j = 1; j < n; ++j)
+                if (s[j] > m) m = s[j];
+            double sum = 0.0;
+            for (int32_t j = 0; j < n; ++j) {
+                s[j] = exp(s[j] - m);
+                sum += s[j];
+            }
+            for (int32_t j = 0; j < n; ++j) {
+                int32_t pb = block_tables[(int64_t)i * max_blocks + j / block_size];
+                int64_t row = (((int64_t)pb * block_size + (j % block_size)) * Hkv + g) * d;
+                double vs = (double)v_scale[((int64_t)pb * Hkv + g) * block_size + j % block_size];
+                double w = s[j] / sum;
+                for (int32_t k = 0; k < d; ++k)
+                    o[k] += w * (orc_e4m3_to_double(v_codes[row + k]) * vs);
+            }
+        }
+    }
+    free(s);
+    return ORC_OK;
+}
