@@ -12,6 +12,11 @@ device->host copy of the output.
 
 The metric is KV-cache bytes attended per second (GB/s): the K and V bytes of
 every context token, divided by the step time.  One JSON line is printed.
+
+With ``--kv-format fp8`` the cache holds E4M3 codes with one fp32 scale per
+(token, KV head) (pa_reshape_and_cache_fp8 / pa_decode_fp8); the bytes are
+then the codes and scales actually read, and ``tokens_per_s`` compares the
+two formats.
 """
 from __future__ import annotations
 
@@ -34,15 +39,20 @@ L2_BYTES = 129 * 10 ** 6
 FALLBACK_HBM_GBS = 6800.0
 
 
-def kv_bytes(lens, Hkv, d, e=2):
-    return 2 * int(sum(int(n) for n in lens)) * Hkv * d * e
+def kv_bytes(lens, Hkv, d, e=2, fp8=False):
+    """K and V bytes of every context token: 16-bit values, or E4M3 codes plus
+    one fp32 scale per (token, KV head)."""
+    tokens = int(sum(int(n) for n in lens))
+    if fp8:
+        return 2 * tokens * Hkv * (d + 4)
+    return 2 * tokens * Hkv * d * e
 
 
-def algorithmic_bytes(lens, B, H, Hkv, d, bs, e=2):
-    """Bytes pa_decode must move: K and V of every context token, Q and the
+def algorithmic_bytes(lens, B, H, Hkv, d, bs, e=2, fp8=False):
+    """Bytes the decode must move: K and V of every context token, Q and the
     output, the used table entries and the lengths."""
     table = sum((int(n) + bs - 1) // bs for n in lens) * 4
-    return kv_bytes(lens, Hkv, d, e) + 2 * B * H * d * e + table + 4 * B
+    return kv_bytes(lens, Hkv, d, e, fp8) + 2 * B * H * d * 2 + table + 4 * B
 
 
 def max_over_ranks(value, dist, device):
@@ -183,7 +193,10 @@ def setup_workload(args):
     from paged_kv_cache_103_gb300 import binding
 
     w = WORKLOADS[args.workload](args.batch)
-    host = wl_mod().qkv(w)
+    fp8 = args.kv_format == "fp8"
+    host = wl_mod().qkv(w, with_cache=not fp8)
+    if fp8:
+        host.update(wl_mod().fp8_cache(w))
     alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
     if w.prefix_len:
         alloc.alloc(0, w.prefix_len)
@@ -221,12 +234,19 @@ def run_gpu(args):
         dist.init_process_group("nccl")
 
     w, host, alloc, slots, tbl, lens, max_blocks = setup_workload(args)
+    fp8 = args.kv_format == "fp8"
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         q = host["q"].to(dev)
-        kc = host["k_cache"].to(dev)
-        vc = host["v_cache"].to(dev)
+        if fp8:
+            kc = host["k_codes"].to(dev)
+            vc = host["v_codes"].to(dev)
+            ks = host["k_scale"].to(dev)
+            vs = host["v_scale"].to(dev)
+        else:
+            kc = host["k_cache"].to(dev)
+            vc = host["v_cache"].to(dev)
         kn = host["k_new"].to(dev)
         vn = host["v_new"].to(dev)
         slots_d = torch.from_numpy(slots).to(dev)
@@ -239,9 +259,24 @@ def run_gpu(args):
     stream.synchronize()
     max_len = int(lens.max())
 
+    # the step's two calls through the C ABI, for either cache format
+    if fp8:
+        def append(kn_, vn_, slots_):
+            binding.pa_reshape_and_cache_fp8(kn_, vn_, slots_, kc, vc, ks, vs, stream)
+
+        def decode(q_, tbl_, lens_, max_len_, out_):
+            binding.pa_decode_fp8(q_, kc, vc, ks, vs, tbl_, lens_, max_len_, w.scale, out_, ws,
+                                  stream)
+    else:
+        def append(kn_, vn_, slots_):
+            binding.pa_reshape_and_cache(kn_, vn_, slots_, kc, vc, stream)
+
+        def decode(q_, tbl_, lens_, max_len_, out_):
+            binding.pa_decode(q_, kc, vc, tbl_, lens_, max_len_, w.scale, out_, ws, stream)
+
     def step():
-        binding.pa_reshape_and_cache(kn, vn, slots_d, kc, vc, stream)
-        binding.pa_decode(q, kc, vc, tbl_d, lens_d, max_len, w.scale, out, ws, stream)
+        append(kn, vn, slots_d)
+        decode(q, tbl_d, lens_d, max_len, out)
 
     for _ in range(args.warmup):
         step()
@@ -252,14 +287,14 @@ def run_gpu(args):
     # replayed from its own CUDA graph (no host launch cost in the way) with an
     # event on either side; when the step's KV bytes would fit in L2, a 512 MiB
     # write and read-back between steps evicts them, outside the timed kernels.
-    kvb = kv_bytes(lens, w.Hkv, w.d)
+    kvb = kv_bytes(lens, w.Hkv, w.d, fp8=fp8)
     flush_l2 = kvb < 2 * L2_BYTES
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
     g_append, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_append, stream=stream):
-        binding.pa_reshape_and_cache(kn, vn, slots_d, kc, vc, stream)
+        append(kn, vn, slots_d)
     with torch.cuda.graph(g_decode, stream=stream):
-        binding.pa_decode(q, kc, vc, tbl_d, lens_d, max_len, w.scale, out, ws, stream)
+        decode(q, tbl_d, lens_d, max_len, out)
     with torch.cuda.stream(stream):
         for _ in range(3):
             g_append.replay()
@@ -301,13 +336,14 @@ def run_gpu(args):
 
     ms_per_step = total_ms / K
     value = whole_job_rate(kvb, world, ms_per_step) / 1e9
-    alg = algorithmic_bytes(lens, w.B, w.H, w.Hkv, w.d, w.block_size)
+    alg = algorithmic_bytes(lens, w.B, w.H, w.Hkv, w.d, w.block_size, fp8=fp8)
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     achieved = alg / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
 
     # ---- e2e leg through the C ABI: host allocator step, pinned H2D, kernels, D2H
-    e2e = run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks)
+    e2e = run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode,
+                  fp8)
 
     l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9) if not flush_l2
                else "L2 flushed between steps (512 MiB write + read outside the timed kernels; %.3f GB "
@@ -315,9 +351,14 @@ def run_gpu(args):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)",
-        "config": {"workload": args.workload + "_decode_layer_step", "batch": w.B,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV, f16 MMA, fp32 accumulate" if fp8 else w.dtype,
+        "data": ("synthetic (seeded N(0,1) Q and new K/V, seeded E4M3 codes and scales, seeded "
+                 "context lengths, random block placement)" if fp8 else
+                 "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)"),
+        "config": {"workload": args.workload + ("_fp8kv" if fp8 else "") + "_decode_layer_step",
+                   "batch": w.B, "kv_format": "e4m3 + fp32 scale per (token, KV head)"
+                   if fp8 else w.dtype,
                    "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
                    "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
                    "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
@@ -329,28 +370,29 @@ def run_gpu(args):
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "timing": "CUDA-graph replay per kernel, CUDA events on the launching stream",
-        "roofline": {"kernel": "pa_decode", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "pa_decode_fp8" if fp8 else "pa_decode", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
                      "traffic": recorded_traffic("pa_decode_llama13b.txt")
-                     if args.workload == "llama13b" and w.B == 64 else None,
+                     if args.workload == "llama13b" and w.B == 64 and not fp8 else None,
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds, fp8)
     if rank == 0:
         print(json.dumps(result))
     if dist:
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks):
+def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode, fp8):
     """Real decode steps through the C ABI with host buffers: each step appends
     one token per sequence in the host allocator, exports the tables into
     pinned memory, copies them and the step's q / new K / new V to the device,
-    runs the append and the decode, and reads the output back."""
+    runs the append and the decode, and reads the output back.  (Copy-on-write
+    pairs cannot arise here: no sequence shares a partial block.)"""
     import numpy as np
     import torch
 
@@ -392,18 +434,19 @@ def run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks):
                 dst.copy_(src, non_blocking=True)
                 h2d += src.numel() * src.element_size()
             if len(pairs):
+                if fp8:
+                    raise RuntimeError("unexpected copy-on-write pairs in the e2e leg")
                 d_pairs[: len(pairs)].copy_(h_pairs[: len(pairs)], non_blocking=True)
                 h2d += len(pairs) * 8
                 binding.pa_copy_blocks([kc], [vc], d_pairs[: len(pairs)], stream)
                 launches += 1
-            binding.pa_reshape_and_cache(d_kn, d_vn, d_slots, kc, vc, stream)
-            binding.pa_decode(d_q, kc, vc, d_tbl, d_lens, int(n_lens.max()), w.scale, d_out, ws,
-                              stream)
+            append(d_kn, d_vn, d_slots)
+            decode(d_q, d_tbl, d_lens, int(n_lens.max()), d_out)
             launches += 2
             h_out.copy_(d_out, non_blocking=True)
             d2h += d_out.numel() * d_out.element_size()
         stream.synchronize()
-        kv_total += kv_bytes(n_lens, Hkv, d)
+        kv_total += kv_bytes(n_lens, Hkv, d, fp8=fp8)
     t1 = time.perf_counter()
     if binding.pa_check_device_errors(stream):
         raise RuntimeError("device error flags set in the e2e leg")
@@ -415,7 +458,7 @@ def run_e2e(args, w, host, alloc, q, kc, vc, ws, stream, dev, max_blocks):
                         "slots, reshape_and_cache, decode, D2H of out, stream sync per step"}
 
 
-def oracle_sample_run(w, host, tbl, lens, seqs, threads):
+def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):
     """Runs the oracle on the sequences `seqs` (cache taken as it stands)."""
     import numpy as np
 
@@ -425,22 +468,26 @@ def oracle_sample_run(w, host, tbl, lens, seqs, threads):
     sel = np.asarray(seqs)
     q = wl.bits(host["q"])[sel]
     code = oracle.DTYPE_F16 if w.dtype == "f16" else oracle.DTYPE_BF16
+    if fp8:   # the FP8 oracle runs on one thread
+        return oracle.decode_fp8(q, code, host["k_codes"].numpy(), host["v_codes"].numpy(),
+                                 host["k_scale"].numpy(), host["v_scale"].numpy(), tbl[sel],
+                                 lens[sel], w.scale)
     return oracle.decode(q, wl.bits(host["k_cache"]), wl.bits(host["v_cache"]), tbl[sel],
                          lens[sel], w.scale, code, num_threads=threads)
 
 
-def cpu_baseline(w, host, tbl, lens, seconds):
+def cpu_baseline(w, host, tbl, lens, seconds, fp8=False):
     """The oracle on the host cores over a bounded sample of the same batch:
     whole-batch passes repeated until about `seconds` of wall time."""
-    threads = os.cpu_count() or 1
+    threads = 1 if fp8 else os.cpu_count() or 1
     seqs = list(range(w.B))
     passes, dt = 0, 0.0
     t0 = time.perf_counter()
     while passes == 0 or dt < seconds:
-        oracle_sample_run(w, host, tbl, lens, seqs, threads)
+        oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8)
         passes += 1
         dt = time.perf_counter() - t0
-    kvb = passes * kv_bytes(lens, w.Hkv, w.d)
+    kvb = passes * kv_bytes(lens, w.Hkv, w.d, fp8=fp8)
     return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": min(threads, w.B),
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": "%d passes over the whole %d-sequence batch (%d context tokens each), "
@@ -522,6 +569,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", choices=["native", "fp8"], default="native",
+                    help="cache in the workload's 16-bit dtype, or E4M3 codes + fp32 scales")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

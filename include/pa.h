@@ -174,6 +174,27 @@ PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
                                       void* v_cache, int32_t num_blocks, int32_t block_size,
                                       int32_t Hkv, int32_t d, pa_dtype dtype, void* stream);
 
+/* FP8 KV append ([P4] section 4.3: quantising the KV cache to 8 bits halves
+ * its bytes; the pages fix no format, so this library takes OCP FP8 E4M3 with
+ * one fp32 scale per (token, KV head) row).  For t in [0, T) with
+ * slot = slot_mapping[t] >= 0 and every KV head h, with x = k_new[t][h][:]
+ * widened to fp32:
+ *   s = fl32(max_i |x_i| / 448)
+ *   k_cache[slot / bs][slot % bs][h][i] = E4M3(fl32(x_i / s))   (RNE, saturating)
+ *   k_scale[slot / bs][h][slot % bs] = s
+ * (IEEE fp32 divisions); an all-zero row stores s = 0 and zero codes.  The
+ * same for V.  A negative slot is padding and is skipped; a slot >=
+ * num_blocks * block_size is skipped and sets PA_DEVERR_SLOT.
+ *   k_new, v_new     (device) [T][Hkv][d] fp16/bf16 (dtype), d = 128
+ *   slot_mapping     (device) [T] int64
+ *   k_cache, v_cache (device) [num_blocks][block_size][Hkv][d] uint8 codes
+ *   k_scale, v_scale (device) [num_blocks][Hkv][block_size] fp32, 16-byte aligned */
+PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                          void* v_cache, float* k_scale, float* v_scale,
+                                          int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                                          int32_t d, pa_dtype dtype, void* stream);
+
 /* Copy-on-write block copies ([P3] section 3.3): for every layer l and pair p,
  * block pairs[p][1] of k_caches[l] and v_caches[l] becomes a bit copy of
  * block pairs[p][0].  block_bytes = block_size * Hkv * d * element size and
@@ -221,6 +242,26 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
                            int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
                            int32_t num_blocks, float scale, pa_dtype dtype, void* out,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/* pa_decode over an FP8 cache written by pa_reshape_and_cache_fp8 ([P4]
+ * section 4.3).  Computes what pa_decode computes with
+ *   K_j = k_scale[b][h / G][j % bs] * E4M3(k_cache[b][j % bs][h / G][:]),
+ *   V_j likewise,  b = block_tables[i][j / bs],
+ * for d = 128 only.  q and out are fp16/bf16 (dtype).  Both products run on
+ * f16 tensor-core MMAs with fp32 accumulation: the codes widen exactly; a bf16
+ * q is scaled by a power of two into f16 range first (exact for its elements
+ * down to 2^-29 of its largest).  A table entry outside the pool reads zero
+ * codes and scales and sets PA_DEVERR_BLOCK_ID.  Other arguments, the
+ * workspace and the errors are those of pa_decode.
+ *   k_cache, v_cache (device) [num_blocks][block_size][Hkv][128] uint8
+ *   k_scale, v_scale (device) [num_blocks][Hkv][block_size] fp32, 16-byte aligned */
+PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                               int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                               int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                               void* workspace, size_t ws_bytes, void* stream);
 
 /* pa_decode without a caller-supplied workspace, for callers that cannot
  * allocate device memory: code running inside an allocator's own hooks, or in

@@ -51,11 +51,15 @@ SIGNATURES = {
     "pa_free_list": (_ST, [_P, _P, _I32, _P]),
     "pa_alloc_stats_get": (_ST, [_P, ctypes.POINTER(AllocStats)]),
     "pa_reshape_and_cache": (_ST, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _ST, _P]),
+    "pa_reshape_and_cache_fp8": (_ST, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                       _ST, _P]),
     "pa_copy_blocks": (_ST, [_P, _P, _I32, _P, _I32, _I64, _I32, _P]),
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "pa_decode_workspace_init": (_ST, [_P, _SZ, _P]),
     "pa_decode": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                         _F32, _ST, _P, _P, _SZ, _P]),
+    "pa_decode_fp8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                            _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                 _I32, _F32, _ST, _P, _P]),
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -145,6 +149,19 @@ def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, stream=No
            "pa_reshape_and_cache")
 
 
+def pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                             stream=None) -> None:
+    """Quantising append: ``k_new/v_new [T, Hkv, 128]`` fp16/bf16, caches
+    ``[N, bs, Hkv, 128]`` uint8 (E4M3 codes), scales ``[N, Hkv, bs]`` float32."""
+    import torch
+    T, Hkv, d = k_new.shape
+    N, bs = k_cache.shape[0], k_cache.shape[1]
+    _check(load().pa_reshape_and_cache_fp8(
+        _dev(k_new), _dev(v_new), _dev(slot_mapping, torch.int64), T, _dev(k_cache, torch.uint8),
+        _dev(v_cache, torch.uint8), _dev(k_scale, torch.float32), _dev(v_scale, torch.float32),
+        N, bs, Hkv, d, _dtype_code(k_new), _stream_ptr(stream)), "pa_reshape_and_cache_fp8")
+
+
 def pa_copy_blocks(k_caches, v_caches, pairs, stream=None) -> None:
     """Copies block ``pairs[p][0]`` onto ``pairs[p][1]`` in every layer's caches."""
     import torch
@@ -181,6 +198,23 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
                             bs, N, float(scale), _dtype_code(q), _dev(out), _dev(workspace),
                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "pa_decode")
+
+
+def pa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                  max_context_len: int, scale: float, out, workspace, stream=None) -> None:
+    """``pa_decode`` over an FP8 cache: ``k_cache/v_cache [N, bs, Hkv, 128]`` uint8
+    codes and ``k_scale/v_scale [N, Hkv, bs]`` float32 scales."""
+    import torch
+    B, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    _check(load().pa_decode_fp8(_dev(q), _dev(k_cache, torch.uint8), _dev(v_cache, torch.uint8),
+                                _dev(k_scale, torch.float32), _dev(v_scale, torch.float32),
+                                _dev(block_tables, torch.int32), int(block_tables.shape[1]),
+                                _dev(context_lens, torch.int32), int(max_context_len), B, H, Hkv,
+                                d, bs, N, float(scale), _dtype_code(q), _dev(out),
+                                _dev(workspace), workspace.numel() * workspace.element_size(),
+                                _stream_ptr(stream)),
+           "pa_decode_fp8")
 
 
 def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,

@@ -7,6 +7,8 @@
 // (each new token's K/V goes into the physical block its current logical block
 // points to); "vLLM 深度拆解：当大模型推理学会「分页注意力」", section 3.3
 // (append_slot; shared blocks copied only when a sharer writes).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pa.h"
@@ -37,6 +39,71 @@ reshape_and_cache_kernel(const uint4* __restrict__ k_new, const uint4* __restric
         const int64_t dst = slot * vecs_per_token + v;
         k_cache[dst] = __ldg(k_new + idx);
         v_cache[dst] = __ldg(v_new + idx);
+    }
+}
+
+// Two fp32 values -> two OCP E4M3 codes, round to nearest even, saturating at
+// +-448; `lo` goes to the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// FP8 KV append: one warp per (token, KV head) row of 128 values, each lane
+// four consecutive values.  scale = fl32(amax / 448) and code =
+// e4m3_rne_sat(fl32(x / scale)) with IEEE fp32 division; an all-zero row gets
+// scale 0 and zero codes.  Codes go to cache[slot / bs][slot % bs][h][:], the
+// scale to scale[slot / bs][h][slot % bs].
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+reshape_and_cache_fp8_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
+                             const int64_t* __restrict__ slot_mapping, int32_t T_tokens,
+                             int32_t Hkv, int32_t block_size, uint32_t* __restrict__ k_cache,
+                             uint32_t* __restrict__ v_cache, float* __restrict__ k_scale,
+                             float* __restrict__ v_scale, int64_t num_slots,
+                             unsigned int* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)T_tokens * Hkv;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
+         row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t t = row / Hkv;
+        const int32_t h = (int32_t)(row - t * Hkv);
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (lane == 0) pa::raise_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size, off = slot - blk * block_size;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const T* src = (which ? v_new : k_new) + row * 128 + lane * 4;
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = to_f32<T>(src[e]);
+            float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float s = __fdiv_rn(amax, 448.0f);
+            uint32_t packed = 0;
+            if (s != 0.f) {
+                const uint16_t lo = e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+                const uint16_t hi = e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+                packed = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            uint32_t* dst = (which ? v_cache : k_cache) + (slot * Hkv + h) * 32 + lane;
+            *dst = packed;
+            if (lane == 0)
+                ((which ? v_scale : k_scale))[(blk * Hkv + h) * block_size + off] = s;
+        }
     }
 }
 
@@ -96,6 +163,41 @@ PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, T, vecs,
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
         (int64_t)num_blocks * block_size, err);
+    return pa::cuda_status(cudaGetLastError());
+}
+
+PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                          void* v_cache, float* k_scale, float* v_scale,
+                                          int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                                          int32_t d, pa_dtype dtype, void* stream) {
+    if (T < 0 || num_blocks < 0 || block_size <= 0 || Hkv <= 0) return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (d != 128) return PA_ERR_UNSUPPORTED;
+    if (T == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return PA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID;
+    unsigned int* err = pa::device_error_word();
+    const int sms = pa::device_sm_count();
+    if (!err || !sms) return PA_ERR_CUDA;
+    const int64_t warps = (int64_t)T * Hkv;
+    int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
+    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t slots = (int64_t)num_blocks * block_size;
+    if (dtype == PA_BF16)
+        reshape_and_cache_fp8_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+            slot_mapping, T, Hkv, block_size, static_cast<uint32_t*>(k_cache),
+            static_cast<uint32_t*>(v_cache), k_scale, v_scale, slots, err);
+    else
+        reshape_and_cache_fp8_kernel<__half><<<(unsigned)blocks, kThreads, 0, st>>>(
+            static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), slot_mapping, T,
+            Hkv, block_size, static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache),
+            k_scale, v_scale, slots, err);
     return pa::cuda_status(cudaGetLastError());
 }
 

@@ -33,6 +33,19 @@
 //    in base 2 per head, transposes P in registers (movmatrix) and accumulates
 //    O^T = V^T P^T with MMAs -- each K/V byte is read from HBM once for the
 //    whole GQA group.  At a pair's end the warps' states merge in shared memory.
+//
+// The same kernel reads an FP8 cache (pa_decode_fp8; "LLM推理优化技术地图：从KV
+// Cache到量化与投机解码", section 4.3, KV cache quantisation): E4M3 codes
+// [num_blocks][block_size][Hkv][128] plus one fp32 scale per (token, KV head),
+// laid out [num_blocks][Hkv][block_size].  A stage then holds 32 code rows of
+// 128 bytes per tensor and the chunk's 2 x 32 scales (their own TMA boxes).
+// Both products run as f16 MMAs: codes widen to f16 exactly; a bf16 query is
+// scaled by a power of two into f16 range (the factor leaves the scores through
+// the score multiplier); the V scale is folded into P, and P is kept in f16
+// range by a running power-of-two factor on the accumulator.  Because the
+// head-dim and key orders of an MMA are free, the code bytes are read in
+// permuted orders that make each lane's loads contiguous and conflict-free,
+// and the output rows are put back in order when the state is deposited.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -61,6 +74,10 @@ constexpr int kMinChunksPerCta = 4;
 constexpr uint32_t kSmemBudget = 113 * 1024;   // dynamic shared memory per CTA (two per SM)
 constexpr uint64_t kWaitLimitNs = 1ull << 30;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
+// FP8 stages: per tensor four 128-byte scale slots (one TMA box of block_size
+// fp32 each; a chunk spans at most four blocks).
+constexpr uint32_t kScaleSlotBytes = 128;
+constexpr uint32_t kScaleStageBytes = 2 * 4 * kScaleSlotBytes;
 
 struct DecodeParams {
     const uint16_t* q;
@@ -76,16 +93,18 @@ struct DecodeParams {
 
 // Dynamic shared-memory carve-up; the same function runs on host and device.
 struct Layout {
-    uint32_t stage_bytes, merge_o, merge_m, merge_l, rowinfo, bars, flags, scan, prefix, total;
+    uint32_t stage_bytes, scales, merge_o, merge_m, merge_l, rowinfo, bars, flags, scan, prefix, total;
 };
 
 // Merge slots (two when the warps merge asynchronously, pairs alternating;
 // one when they merge together): each holds every consumer warp's
 // unnormalised output [W][G][D], row maxima [W][16] and row sums [W][16].
-__host__ __device__ inline Layout make_layout(int D, int G, int B, int stages, int slots) {
+__host__ __device__ inline Layout make_layout(int D, int G, int B, int stages, int slots,
+                                              bool fp8) {
     Layout L;
-    L.stage_bytes = 2u * kChunk * D * 2;
-    L.merge_o = stages * L.stage_bytes;                              // [slots][W][G][D] fp32
+    L.stage_bytes = 2u * kChunk * D * (fp8 ? 1 : 2);
+    L.scales = stages * L.stage_bytes;                               // fp8: [stages][2][4][32] fp32
+    L.merge_o = L.scales + (fp8 ? stages * kScaleStageBytes : 0);    // [slots][W][G][D] fp32
     L.merge_m = L.merge_o + slots * kConsumerWarps * G * D * 4;      // [slots][W][16]
     L.merge_l = L.merge_m + slots * kConsumerWarps * kMaxG * 4;      // [slots][W][16]
     L.rowinfo = L.merge_l + slots * kConsumerWarps * kMaxG * 4;      // [slots][2 + W][16]
@@ -165,6 +184,10 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
     m = mn;
 }
 
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
     return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
@@ -179,13 +202,18 @@ __device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t
     return ((((b * halves + h) << rows_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
 }
 
-template <int D, bool kBF16, int NT, bool kAsync>
+// kFp8: the cache holds E4M3 codes with per-(token, KV head) scales (ksmap,
+// vsmap); otherwise the cache has the dtype of q and the scale maps are unused.
+template <int D, bool kBF16, int NT, bool kAsync, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-    constexpr uint32_t kHalves = D / 64;
+                    const __grid_constant__ CUtensorMap vmap,
+                    const __grid_constant__ CUtensorMap ksmap,
+                    const __grid_constant__ CUtensorMap vsmap, const DecodeParams p) {
+    static_assert(!kFp8 || D == 128, "FP8 rows are one 128-byte swizzle row");
+    constexpr uint32_t kHalves = kFp8 ? 1 : D / 64;  // 128-byte pieces of a token row
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
-    const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1);
+    const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1, kFp8);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -276,15 +304,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         if (lane == 0 && prod == 0) {
             pa::prefetch_tensormap(&kmap);
             pa::prefetch_tensormap(&vmap);
+            if constexpr (kFp8) {
+                pa::prefetch_tensormap(&ksmap);
+                pa::prefetch_tensormap(&vsmap);
+            }
         }
         const uint64_t policy = pa::l2_policy_evict_first();
         const int rows = bs < kChunk ? bs : kChunk;  // token rows per TMA box
         const int bpc = kChunk / rows;               // boxes per chunk and tensor
         const int nblk = (kChunk + bs - 1) / bs;     // table entries a chunk spans
         const int32_t oob_row = p.num_blocks * bs;
-        const int my_b = lane >> 1;              // the box this lane loads ...
-        const bool my_v = (lane & 1) != 0;       // ... and whether of K or of V
-        const CUtensorMap* my_map = my_v ? &vmap : &kmap;
+        const int my_b = kFp8 ? (lane & 15) >> 1 : lane >> 1;  // the box this lane loads,
+        const bool my_v = (lane & 1) != 0;                      // whether of K or of V,
+        const bool my_scale = kFp8 && lane >= 16;               // and whether codes or scales
+        const CUtensorMap* my_map =
+            my_scale ? (my_v ? &vsmap : &ksmap) : (my_v ? &vmap : &kmap);
+        const uint32_t tx_bytes = L.stage_bytes + (kFp8 ? 2 * kChunk * 4 : 0);
         int32_t k = 0;  // chunks of this CTA walked so far
         bool dead = false;
         for (int32_t pos = lo; pos < hi && !dead;) {
@@ -312,7 +347,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                 }
                 unsigned char* base = smem + stage * L.stage_bytes + (my_v ? L.stage_bytes / 2 : 0);
-                if (lane == 0) pa::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+                if (lane == 0) pa::mbar_arrive_expect_tx(&full[stage], tx_bytes);
                 __syncwarp();
                 const int32_t tok = tok_first + (my_b < bpc ? my_b : 0) * rows;
                 const int32_t jj = tok / bs;
@@ -323,9 +358,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         ok = false;
                         pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
                     }
-                    pa::tma_load_3d(base + ((uint32_t)my_b * kHalves << rows_shift) * 128, my_map,
-                                    &full[stage], 0, ok ? blk * bs + (tok - jj * bs) : oob_row,
-                                    s.g * (int32_t)kHalves, policy);
+                    if (!my_scale)
+                        pa::tma_load_3d(base + ((uint32_t)my_b * kHalves << rows_shift) * 128,
+                                        my_map, &full[stage], 0,
+                                        ok ? blk * bs + (tok - jj * bs) : oob_row,
+                                        s.g * (int32_t)kHalves, policy);
+                    else  // block_size scales of (block, KV head); zeros past the pool
+                        pa::tma_load_3d(smem + L.scales + stage * kScaleStageBytes +
+                                            ((my_v ? 4u : 0u) + (uint32_t)my_b) * kScaleSlotBytes,
+                                        my_map, &full[stage], 0, s.g, ok ? blk : p.num_blocks,
+                                        policy);
                 }
             }
             pos += s.len;
@@ -348,15 +390,60 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
     // Q^T fragments (MMA B operand) of a pair: lane holds query head 8 nt + cr.
     uint32_t qb[NT][D / 16][2];
+    // Multiplier from an MMA score to the base-2 logit (FP8: times the K scale).
+    float qsc = p.scale_log2;
     auto load_q = [&](const Segment& sg) {
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int hq = 8 * nt + cr;
-            const uint16_t* qrow = p.q + ((int64_t)sg.i * p.H + sg.g * G + hq) * D + cc;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hq = 8 * nt + cr;
+                const uint16_t* qrow = p.q + ((int64_t)sg.i * p.H + sg.g * G + hq) * D + cc;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                qb[nt][ks][0] = hq < G ? ld_u32(qrow + ks * 16) : 0u;
-                qb[nt][ks][1] = hq < G ? ld_u32(qrow + ks * 16 + 8) : 0u;
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    qb[nt][ks][0] = hq < G ? ld_u32(qrow + ks * 16) : 0u;
+                    qb[nt][ks][1] = hq < G ? ld_u32(qrow + ks * 16 + 8) : 0u;
+                }
+            }
+        } else {
+            // Head-dim order of the FP8 path: in k-step ks, the lane with
+            // c4 = lane % 4 holds dims 32 c4 + 4 ks + {0, 1} (b0) and {2, 3}
+            // (b1), so its 32 dims are contiguous.  A bf16 query is scaled by
+            // 2^e (max |q| of the group into [2^14, 2^15)) and rounded to f16,
+            // exact for elements down to 2^-29 of the largest.
+            const int c4 = lane & 3;
+            float amax = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hq = 8 * nt + cr;
+                const uint16_t* qrow = p.q + ((int64_t)sg.i * p.H + sg.g * G + hq) * D + 32 * c4;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    qb[nt][ks][0] = hq < G ? ld_u32(qrow + 4 * ks) : 0u;
+                    qb[nt][ks][1] = hq < G ? ld_u32(qrow + 4 * ks + 2) : 0u;
+                    if constexpr (kBF16)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            amax = fmaxf(amax,
+                                         fmaxf(fabsf(__uint_as_float(qb[nt][ks][j] << 16)),
+                                               fabsf(__uint_as_float(qb[nt][ks][j] & 0xFFFF0000u))));
+                }
+            }
+            if constexpr (kBF16) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const int e = min(141 - pa::biased_exponent(amax), 126);
+                const float up = pa::exp2_int(e);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            qb[nt][ks][j] =
+                                pa::pack2<false>(__uint_as_float(qb[nt][ks][j] << 16) * up,
+                                                 __uint_as_float(qb[nt][ks][j] & 0xFFFF0000u) * up);
+                qsc = p.scale_log2 * pa::exp2_int(-e);
             }
         }
     };
@@ -533,6 +620,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         // Running state for the heads 8 nt + cc + {0, 1} this lane tracks.
         float m_run[NT][2], l_run[NT][2];
         float o[D / 16][NT][4];  // O^T: rows = head_dim, columns = heads
+        // FP8: o holds the output times 2^vexp (P scaled by the V scales and by
+        // 2^vexp stays below 2^15, inside f16 range).
+        int vexp = 126;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             m_run[nt][0] = m_run[nt][1] = -INFINITY;
@@ -577,6 +667,52 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     __syncwarp();
                 }
 
+                // Per-token factors of this lane's key rows 16 mt + cr + 8 h:
+                // kmul takes an MMA score to a base-2 logit, vmul scales P.
+                float kmul[kKeyTiles][2], vmul[kKeyTiles][2];
+                float rs = 1.f;  // extra factor on o this chunk
+                if constexpr (kFp8) {
+                    const uint32_t sk = smem_base + L.scales + (uint32_t)stage * kScaleStageBytes;
+                    float vmax = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < kKeyTiles; ++mt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t tok = (uint32_t)(mt * 16 + cr + 8 * h);
+                            const uint32_t off =
+                                ((tok >> rows_shift) * (kScaleSlotBytes / 4) +
+                                 (tok & ((1u << rows_shift) - 1u))) * 4;
+                            kmul[mt][h] = pa::lds_f32(sk + off) * qsc;
+                            const float sv = (int)tok < valid
+                                                 ? pa::lds_f32(sk + 4 * kScaleSlotBytes + off)
+                                                 : 0.f;
+                            vmul[mt][h] = sv;
+                            vmax = fmaxf(vmax, sv);
+                        }
+                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+                    if (vmax > 0.f) {
+                        const int e = min(vexp, 141 - pa::biased_exponent(vmax));
+                        if (e < vexp) {
+                            rs = e - vexp >= -126 ? pa::exp2_int(e - vexp) : 0.f;
+                            vexp = e;
+                        }
+                    }
+                    const float f = pa::exp2_int(vexp);
+#pragma unroll
+                    for (int mt = 0; mt < kKeyTiles; ++mt) {
+                        vmul[mt][0] *= f;
+                        vmul[mt][1] *= f;
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < kKeyTiles; ++mt) {
+                        kmul[mt][0] = kmul[mt][1] = p.scale_log2;
+                        vmul[mt][0] = vmul[mt][1] = 1.f;
+                    }
+                }
+
                 // S^T = K Q^T: kChunk / 16 key m-tiles x NT 8-head n-tiles.
                 float st[kKeyTiles][NT][4];
 #pragma unroll
@@ -584,8 +720,35 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         st[mt][nt][0] = st[mt][nt][1] = st[mt][nt][2] = st[mt][nt][3] = 0.f;
+                if constexpr (kFp8) {
+                    // Rows 16 mt + cr (+ 8): 16-byte columns 2 c4 and 2 c4 + 1
+                    // (stored at column ^ cr) hold the 32 dims of the lane's
+                    // k-order; 8 lanes of a phase hit 8 distinct columns.
+                    const uint32_t c4 = (uint32_t)(lane & 3);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
+                    for (int mt = 0; mt < kKeyTiles; ++mt) {
+                        uint4 w[2][2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t tok = (uint32_t)(mt * 16 + cr + 8 * h);
+                                w[h][j] = pa::lds128(kt + (tok << 7) +
+                                                     (((2 * c4 + j) ^ (uint32_t)cr) << 4));
+                            }
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            uint32_t a[4];
+                            pa::e4m3x4_to_f16(u4_word(w[0][ks >> 2], ks & 3), a[0], a[2]);
+                            pa::e4m3x4_to_f16(u4_word(w[1][ks >> 2], ks & 3), a[1], a[3]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                pa::mma_16816<false>(st[mt][nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int ks = 0; ks < (kFp8 ? 0 : D / 16); ++ks) {
                     const uint32_t col = (uint32_t)((ks & 3) * 2 + (mi >> 1));
 #pragma unroll
                     for (int mt = 0; mt < kKeyTiles; ++mt) {
@@ -610,7 +773,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = mt * 16 + cr + 8 * (e >> 1);
-                            const float x = tok < valid ? st[mt][nt][e] * p.scale_log2 : -INFINITY;
+                            const float x =
+                                tok < valid ? st[mt][nt][e] * kmul[mt][e >> 1] : -INFINITY;
                             st[mt][nt][e] = x;
                             mx[nt][e & 1] = fmaxf(mx[nt][e & 1], x);
                         }
@@ -631,7 +795,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         m_run[nt][j] = m_new;
                         l_run[nt][j] *= alpha[nt][j];
                     }
-                if (__any_sync(0xffffffffu, grew)) {
+                if (__any_sync(0xffffffffu, grew) || rs != 1.f) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        alpha[nt][0] *= rs;
+                        alpha[nt][1] *= rs;
+                    }
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -654,13 +823,65 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             e4[e] = pa::fast_exp2(st[mt][nt][e] - m_run[nt][e & 1]);
                             l_run[nt][e & 1] += e4[e];
                         }
-                        pb[mt][nt][0] = pa::movmatrix_trans(pa::pack2<kBF16>(e4[0], e4[1]));
-                        pb[mt][nt][1] = pa::movmatrix_trans(pa::pack2<kBF16>(e4[2], e4[3]));
+                        if constexpr (kFp8) {
+                            // V scale folded into P; rows past the context get
+                            // exactly 0 (vmul = 0 there).
+                            e4[0] *= vmul[mt][0];
+                            e4[1] *= vmul[mt][0];
+                            e4[2] *= vmul[mt][1];
+                            e4[3] *= vmul[mt][1];
+                        }
+                        constexpr bool kPbf16 = kBF16 && !kFp8;
+                        pb[mt][nt][0] = pa::movmatrix_trans(pa::pack2<kPbf16>(e4[0], e4[1]));
+                        pb[mt][nt][1] = pa::movmatrix_trans(pa::pack2<kPbf16>(e4[2], e4[3]));
                     }
 
                 // O^T += V^T P^T: head_dim in 16-row m-tiles, keys in 16-key steps.
+                if constexpr (kFp8) {
+                    // Row rho of m-tile mt is head dim 8 rho + mt, so the lane's
+                    // rows cr and cr + 8 of all eight m-tiles are 8 contiguous
+                    // bytes (dims 8 cr .. and 64 + 8 cr ..) of each key row it
+                    // needs: keys 16 ks2 + 2 c4 + {0, 1, 8, 9}.
+                    const uint32_t c4 = (uint32_t)(lane & 3);
+                    const uint32_t part = (uint32_t)(cr & 1) * 8;
 #pragma unroll
-                for (int ks2 = 0; ks2 < kKeyTiles; ++ks2) {
+                    for (int ks2 = 0; ks2 < kKeyTiles; ++ks2) {
+                        uint2 lo[4], hi[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t tok = 16 * ks2 + 2 * c4 + (u & 1) + 8 * (u >> 1);
+                            const uint32_t row = vt + (tok << 7) + part;
+                            lo[u] = pa::lds64(row + ((((uint32_t)cr >> 1) ^ (tok & 7)) << 4));
+                            hi[u] = pa::lds64(row + (((4 + ((uint32_t)cr >> 1)) ^ (tok & 7)) << 4));
+                        }
+#pragma unroll
+                        for (int q4 = 0; q4 < 2; ++q4) {
+                            // A fragment u of m-tiles 4 q4 .. 4 q4 + 3: keys of
+                            // fragment u from rows (lo | hi)[2 (u >> 1)] and
+                            // [2 (u >> 1) + 1], interleaved byte by byte.
+                            uint32_t af[4][4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const uint2* src = (u & 1) ? hi : lo;
+                                const uint32_t x = q4 ? src[2 * (u >> 1)].y : src[2 * (u >> 1)].x;
+                                const uint32_t y =
+                                    q4 ? src[2 * (u >> 1) + 1].y : src[2 * (u >> 1) + 1].x;
+                                pa::e4m3x4_to_f16(__byte_perm(x, y, 0x5140), af[u][0], af[u][1]);
+                                pa::e4m3x4_to_f16(__byte_perm(x, y, 0x7362), af[u][2], af[u][3]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t a[4] = {af[0][i], af[1][i], af[2][i], af[3][i]};
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    pa::mma_16816<false>(o[4 * q4 + i][nt], a, pb[ks2][nt][0],
+                                                         pb[ks2][nt][1]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int ks2 = 0; ks2 < (kFp8 ? 0 : kKeyTiles); ++ks2) {
                     const uint32_t tok = (uint32_t)(ks2 * 16 + (mi >> 1) * 8 + rr);
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
@@ -721,15 +942,35 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     sl[warp * kMaxG + h] = l_run[nt][j];
                 }
             }
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt)
+        if constexpr (kFp8) {
+            // o[mt][nt][e] is head dim 8 (cr + 8 (e >> 1)) + mt, scaled by 2^vexp.
+            const float inv = pa::exp2_int(-vexp);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int h = 8 * nt + cc + (e & 1);
-                    if (h < G) so[(warp * G + h) * D + mt * 16 + cr + 8 * (e >> 1)] = o[mt][nt][e];
+                    if (h < G) {
+                        float4* dst = reinterpret_cast<float4*>(
+                            &so[(warp * G + h) * D + 8 * cr + 64 * (e >> 1)]);
+                        dst[0] = make_float4(o[0][nt][e] * inv, o[1][nt][e] * inv,
+                                             o[2][nt][e] * inv, o[3][nt][e] * inv);
+                        dst[1] = make_float4(o[4][nt][e] * inv, o[5][nt][e] * inv,
+                                             o[6][nt][e] * inv, o[7][nt][e] * inv);
+                    }
                 }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = 8 * nt + cc + (e & 1);
+                        if (h < G)
+                            so[(warp * G + h) * D + mt * 16 + cr + 8 * (e >> 1)] = o[mt][nt][e];
+                    }
+        }
 
         // The next pair's length and query fragments load while this one merges.
         const int32_t npos = pos + s.len;
@@ -814,6 +1055,41 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int32_t rows, int32_t 
     return r == CUDA_SUCCESS;
 }
 
+// FP8 codes: x = the 128 code bytes of a (token, KV head) row, y = token row
+// of the pool (stride Hkv * 128 bytes), z = KV head (stride 128 bytes).  A box
+// of {128, block_size, 1} at (0, block * block_size, head) is one block of one
+// KV head, [row][128 bytes] in shared memory with the 128-byte swizzle.
+bool encode_code_map(CUtensorMap* map, const void* base, int32_t rows, int32_t Hkv,
+                     int32_t block_size) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)Hkv * 128, 128};
+    const cuuint32_t box[3] = {128, (cuuint32_t)(block_size < kChunk ? block_size : kChunk), 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP8 scales [num_blocks][Hkv][block_size] fp32: a box of {block_size, 1, 1}
+// at (0, head, block) is the block's scales for one KV head; a block index of
+// num_blocks lies outside and arrives as zeros.
+bool encode_scale_map(CUtensorMap* map, const float* base, int32_t num_blocks, int32_t Hkv,
+                      int32_t block_size) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)block_size, (cuuint64_t)Hkv, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[2] = {(cuuint64_t)block_size * 4, (cuuint64_t)Hkv * block_size * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)block_size, 1, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t slot_floats(int32_t d) { return 2 * kMaxG + (size_t)kMaxG * d; }
 
 size_t counters_bytes(int32_t B, int32_t H) {
@@ -831,10 +1107,11 @@ size_t counters_bytes(int32_t B, int32_t H) {
 // and the ring depth decides; wider groups merge with all four warps.
 bool async_merge(int G) { return G <= 2; }
 
-int choose_stages(int D, int G, int B) {
-    const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1);
+int choose_stages(int D, int G, int B, bool fp8) {
+    const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1, fp8);
     if (L0.total >= kSmemBudget) return 0;
-    int s = (int)((kSmemBudget - L0.total) / L0.stage_bytes);
+    const uint32_t per_stage = L0.stage_bytes + (fp8 ? kScaleStageBytes : 0);
+    int s = (int)((kSmemBudget - L0.total) / per_stage);
     if (s > kMaxStages) s = kMaxStages;
     s &= ~1;  // each producer owns every other stage
     // Wider groups make the consumers the limit: give every consumer warp the
@@ -844,10 +1121,11 @@ int choose_stages(int D, int G, int B) {
     return s;
 }
 
-template <int D, bool kBF16, int NT, bool kAsync>
-pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& prm,
-                 size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<D, kBF16, NT, kAsync>;
+template <int D, bool kBF16, int NT, bool kAsync, bool kFp8>
+pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& ksm,
+                 const CUtensorMap& vsm, const DecodeParams& prm, size_t smem,
+                 cudaStream_t stream) {
+    auto kern = paged_decode_kernel<D, kBF16, NT, kAsync, kFp8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -855,16 +1133,52 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParam
                                         (int)kSmemBudget);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    kern<<<pa_decode_grid_size(), kThreads, smem, stream>>>(km, vm, prm);
+    kern<<<pa_decode_grid_size(), kThreads, smem, stream>>>(km, vm, ksm, vsm, prm);
     return pa::cuda_status(cudaGetLastError());
 }
 
-template <int D, bool kBF16>
-pa_status launch_g(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& prm,
-                   size_t smem, cudaStream_t stream) {
-    if (async_merge(prm.G)) return launch<D, kBF16, 1, true>(km, vm, prm, smem, stream);
-    return prm.G <= 8 ? launch<D, kBF16, 1, false>(km, vm, prm, smem, stream)
-                      : launch<D, kBF16, 2, false>(km, vm, prm, smem, stream);
+template <int D, bool kBF16, bool kFp8>
+pa_status launch_g(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& ksm,
+                   const CUtensorMap& vsm, const DecodeParams& prm, size_t smem,
+                   cudaStream_t stream) {
+    if (async_merge(prm.G))
+        return launch<D, kBF16, 1, true, kFp8>(km, vm, ksm, vsm, prm, smem, stream);
+    return prm.G <= 8 ? launch<D, kBF16, 1, false, kFp8>(km, vm, ksm, vsm, prm, smem, stream)
+                      : launch<D, kBF16, 2, false, kFp8>(km, vm, ksm, vsm, prm, smem, stream);
+}
+
+// Checks shared by pa_decode and pa_decode_fp8; fills everything of prm but the
+// pointers and returns the shared-memory size in *smem.
+pa_status prepare(int32_t max_blocks, int32_t max_context_len, int32_t B, int32_t H, int32_t Hkv,
+                  int32_t d, int32_t block_size, int32_t num_blocks, float scale, pa_dtype dtype,
+                  size_t ws_bytes, bool fp8, DecodeParams* prm, size_t* smem) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (H % Hkv != 0 || H / Hkv > kMaxG) return PA_ERR_UNSUPPORTED;
+    if (d != 128 && (fp8 || d != 64)) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    // Flattened chunk indices are int32: every sequence's chunks times Hkv.
+    const int64_t max_chunks = ((int64_t)max_blocks * block_size + kChunk - 1) / kChunk;
+    if ((int64_t)B * Hkv * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
+    const int G = H / Hkv;
+    const int stages = choose_stages(d, G, B, fp8);
+    if (stages < 2) return PA_ERR_UNSUPPORTED;
+    if (B > 0 && ws_bytes < pa_decode_workspace_size(B, H, d)) return PA_ERR_INVALID;
+    prm->max_blocks = max_blocks;
+    prm->B = B;
+    prm->H = H;
+    prm->Hkv = Hkv;
+    prm->G = G;
+    prm->bs = block_size;
+    prm->num_blocks = num_blocks;
+    prm->stages = stages;
+    prm->scale_log2 = scale * kLog2e;
+    *smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1, fp8).total;
+    return PA_OK;
 }
 
 }  // namespace
@@ -887,29 +1201,17 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
                            int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
                            int32_t num_blocks, float scale, pa_dtype dtype, void* out,
                            void* workspace, size_t ws_bytes, void* stream) {
-    if (B < 0 || H <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 ||
-        max_context_len < 0 || !std::isfinite(scale))
-        return PA_ERR_INVALID;
-    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (H % Hkv != 0 || H / Hkv > kMaxG) return PA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128) return PA_ERR_UNSUPPORTED;
-    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
-    if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
-    if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
-    if (B == 0) return PA_OK;
+    DecodeParams prm;
+    size_t smem = 0;
+    const pa_status st0 = prepare(max_blocks, max_context_len, B, H, Hkv, d, block_size,
+                                  num_blocks, scale, dtype, ws_bytes, false, &prm, &smem);
+    if (st0 != PA_OK || B == 0) return st0;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return PA_ERR_INVALID;
-    if (ws_bytes < pa_decode_workspace_size(B, H, d)) return PA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
         return PA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 15u))
         return PA_ERR_INVALID;
-    // Flattened chunk indices are int32: every sequence's chunks times Hkv.
-    const int64_t max_chunks = ((int64_t)max_blocks * block_size + kChunk - 1) / kChunk;
-    if ((int64_t)B * Hkv * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
-    const int G = H / Hkv;
-    const int stages = choose_stages(d, G, B);
-    if (stages < 2) return PA_ERR_UNSUPPORTED;
 
     unsigned int* err = pa::device_error_word();
     if (!err || pa_decode_grid_size() <= 0) return PA_ERR_CUDA;
@@ -920,7 +1222,6 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
         !encode_cache_map(&vm, v_cache, rows, Hkv, d, block_size, dtype))
         return PA_ERR_CUDA;
 
-    DecodeParams prm;
     prm.q = static_cast<const uint16_t*>(q);
     prm.out = static_cast<uint16_t*>(out);
     prm.block_tables = block_tables;
@@ -929,23 +1230,60 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
     prm.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
                                             counters_bytes(B, H));
     prm.err = err;
-    prm.max_blocks = max_blocks;
-    prm.B = B;
-    prm.H = H;
-    prm.Hkv = Hkv;
-    prm.G = G;
-    prm.bs = block_size;
-    prm.num_blocks = num_blocks;
-    prm.stages = stages;
-    prm.scale_log2 = scale * kLog2e;
-    const size_t smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1).total;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 128)
-        return dtype == PA_BF16 ? launch_g<128, true>(km, vm, prm, smem, st)
-                                : launch_g<128, false>(km, vm, prm, smem, st);
-    return dtype == PA_BF16 ? launch_g<64, true>(km, vm, prm, smem, st)
-                            : launch_g<64, false>(km, vm, prm, smem, st);
+        return dtype == PA_BF16 ? launch_g<128, true, false>(km, vm, km, vm, prm, smem, st)
+                                : launch_g<128, false, false>(km, vm, km, vm, prm, smem, st);
+    return dtype == PA_BF16 ? launch_g<64, true, false>(km, vm, km, vm, prm, smem, st)
+                            : launch_g<64, false, false>(km, vm, km, vm, prm, smem, st);
+}
+
+PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                               int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                               int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    DecodeParams prm;
+    size_t smem = 0;
+    const pa_status st0 = prepare(max_blocks, max_context_len, B, H, Hkv, d, block_size,
+                                  num_blocks, scale, dtype, ws_bytes, true, &prm, &smem);
+    if (st0 != PA_OK || B == 0) return st0;
+    if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens ||
+        !out || !workspace)
+        return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) &
+        15u)
+        return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+        return PA_ERR_INVALID;
+
+    unsigned int* err = pa::device_error_word();
+    if (!err || pa_decode_grid_size() <= 0) return PA_ERR_CUDA;
+
+    CUtensorMap km, vm, ksm, vsm;
+    const int32_t rows = num_blocks * block_size;
+    if (!encode_code_map(&km, k_cache, rows, Hkv, block_size) ||
+        !encode_code_map(&vm, v_cache, rows, Hkv, block_size) ||
+        !encode_scale_map(&ksm, k_scale, num_blocks, Hkv, block_size) ||
+        !encode_scale_map(&vsm, v_scale, num_blocks, Hkv, block_size))
+        return PA_ERR_CUDA;
+
+    prm.q = static_cast<const uint16_t*>(q);
+    prm.out = static_cast<uint16_t*>(out);
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.counters = static_cast<int32_t*>(workspace);
+    prm.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                            counters_bytes(B, H));
+    prm.err = err;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return dtype == PA_BF16 ? launch_g<128, true, true>(km, vm, ksm, vsm, prm, smem, st)
+                            : launch_g<128, false, true>(km, vm, ksm, vsm, prm, smem, st);
 }
 
 }  // extern "C"

@@ -139,19 +139,38 @@ def normal_tensor(shape, dtype, seed: int, chunk: int = 1 << 26) -> torch.Tensor
     return out.view(*shape)
 
 
-def qkv(w: Workload, with_new: bool = True):
-    """Seeded tensors on the host: ``q [B,H,d]``, ``k_cache``/``v_cache
-    [N,bs,Hkv,d]`` and, with ``with_new``, one new token's ``k_new``/``v_new
-    [B,Hkv,d]`` per sequence."""
+def qkv(w: Workload, with_new: bool = True, with_cache: bool = True):
+    """Seeded tensors on the host: ``q [B,H,d]``, with ``with_cache`` the
+    ``k_cache``/``v_cache [N,bs,Hkv,d]`` and, with ``with_new``, one new
+    token's ``k_new``/``v_new [B,Hkv,d]`` per sequence."""
     dt = w.torch_dtype
-    out = {
-        "q": normal_tensor((w.B, w.H, w.d), dt, w.seed * 16 + 1),
-        "k_cache": normal_tensor((w.num_blocks, w.block_size, w.Hkv, w.d), dt, w.seed * 16 + 2),
-        "v_cache": normal_tensor((w.num_blocks, w.block_size, w.Hkv, w.d), dt, w.seed * 16 + 3),
-    }
+    out = {"q": normal_tensor((w.B, w.H, w.d), dt, w.seed * 16 + 1)}
+    if with_cache:
+        out["k_cache"] = normal_tensor((w.num_blocks, w.block_size, w.Hkv, w.d), dt,
+                                       w.seed * 16 + 2)
+        out["v_cache"] = normal_tensor((w.num_blocks, w.block_size, w.Hkv, w.d), dt,
+                                       w.seed * 16 + 3)
     if with_new:
         out["k_new"] = normal_tensor((w.B, w.Hkv, w.d), dt, w.seed * 16 + 4)
         out["v_new"] = normal_tensor((w.B, w.Hkv, w.d), dt, w.seed * 16 + 5)
+    return out
+
+
+def fp8_cache(w: Workload, seed_offset: int = 0):
+    """Seeded FP8 cache contents on the host, drawn directly (no quantisation):
+    ``k_codes``/``v_codes [N,bs,Hkv,d]`` uint8 with the magnitude code uniform
+    over the 127 finite E4M3 magnitudes (0x00..0x7E) and a random sign bit, and
+    ``k_scale``/``v_scale [N,Hkv,bs]`` float32 uniform in [0.004, 0.012] (the
+    size of amax / 448 for N(0, 1) rows of 128)."""
+    rng = np.random.default_rng(w.seed * 16 + 6 + seed_offset)
+    shape = (w.num_blocks, w.block_size, w.Hkv, w.d)
+    out = {}
+    for name in ("k", "v"):
+        mag = rng.integers(0, 0x7F, size=shape, dtype=np.uint8)
+        sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << 7
+        out[name + "_codes"] = torch.from_numpy(mag | sign)
+        out[name + "_scale"] = torch.from_numpy(
+            rng.uniform(0.004, 0.012, size=(w.num_blocks, w.Hkv, w.block_size)).astype(np.float32))
     return out
 
 
