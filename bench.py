@@ -374,8 +374,9 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
-                     "traffic": recorded_traffic("pa_decode_llama13b.txt")
-                     if args.workload == "llama13b" and w.B == 64 and not fp8 else None,
+                     "traffic": recorded_traffic("pa_decode_fp8_llama13b.txt" if fp8
+                                                 else "pa_decode_llama13b.txt")
+                     if args.workload == "llama13b" and w.B == 64 else None,
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
     }

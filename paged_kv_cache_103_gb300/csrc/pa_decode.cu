@@ -22,12 +22,13 @@
 //        M = max m_p,  out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
 //  * Two producer warps (even and odd chunks) walk the same list and stream K
 //    and V chunks into a shared-memory ring with 3-D TMA tile loads: one box per
-//    block and tensor (block_size rows x head_dim, 128-byte swizzle), each box
-//    issued by its own lane, completion counted on the stage's mbarrier.  The
-//    table is read 32 entries at a time.  Blocks past a context's end, and
-//    out-of-pool ids, are loaded from outside the tensor map and arrive as
-//    zeros, so no address outside the cache is ever formed.
-//  * Four consumer warps take the chunks round-robin.  A warp computes
+//    block and tensor (block_size rows x head_dim, 128-byte swizzle), all of a
+//    chunk's boxes issued by one lane, completion counted on the stage's
+//    mbarrier.  The table is read 32 entries at a time, one window and one
+//    pair ahead of use.  Blocks past a context's end, and out-of-pool ids, are
+//    loaded from outside the tensor map and arrive as zeros, so no address
+//    outside the cache is ever formed.
+//  * Four consumer warps take the chunks; stage s always goes to warp s % 4.  A warp computes
 //    S^T = K Q^T for 32 keys with m16n8k16 tensor-core MMAs (keys are the M
 //    rows, the group's G query heads the N columns), runs the online softmax
 //    in base 2 per head, transposes P in registers (movmatrix) and accumulates
@@ -74,10 +75,9 @@ constexpr int kMinChunksPerCta = 4;
 constexpr uint32_t kSmemBudget = 113 * 1024;   // dynamic shared memory per CTA (two per SM)
 constexpr uint64_t kWaitLimitNs = 1ull << 30;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
-// FP8 stages: per tensor four 128-byte scale slots (one TMA box of block_size
-// fp32 each; a chunk spans at most four blocks).
+// FP8 stages: per tensor one 128-byte scale slot per block of the chunk (one
+// TMA box of block_size fp32 each).
 constexpr uint32_t kScaleSlotBytes = 128;
-constexpr uint32_t kScaleStageBytes = 2 * 4 * kScaleSlotBytes;
 
 struct DecodeParams {
     const uint16_t* q;
@@ -93,18 +93,20 @@ struct DecodeParams {
 
 // Dynamic shared-memory carve-up; the same function runs on host and device.
 struct Layout {
-    uint32_t stage_bytes, scales, merge_o, merge_m, merge_l, rowinfo, bars, flags, scan, prefix, total;
+    uint32_t stage_bytes, scale_stage, scales, merge_o, merge_m, merge_l, rowinfo, bars, flags, scan, prefix, total;
 };
 
 // Merge slots (two when the warps merge asynchronously, pairs alternating;
 // one when they merge together): each holds every consumer warp's
 // unnormalised output [W][G][D], row maxima [W][16] and row sums [W][16].
 __host__ __device__ inline Layout make_layout(int D, int G, int B, int stages, int slots,
-                                              bool fp8) {
+                                              bool fp8, int bs) {
     Layout L;
     L.stage_bytes = 2u * kChunk * D * (fp8 ? 1 : 2);
-    L.scales = stages * L.stage_bytes;                               // fp8: [stages][2][4][32] fp32
-    L.merge_o = L.scales + (fp8 ? stages * kScaleStageBytes : 0);    // [slots][W][G][D] fp32
+    // fp8: [stages][K, V][blocks per chunk][32] fp32
+    L.scale_stage = fp8 ? 2u * (kChunk / (bs < kChunk ? bs : kChunk)) * kScaleSlotBytes : 0u;
+    L.scales = stages * L.stage_bytes;
+    L.merge_o = L.scales + stages * L.scale_stage;                   // [slots][W][G][D] fp32
     L.merge_m = L.merge_o + slots * kConsumerWarps * G * D * 4;      // [slots][W][16]
     L.merge_l = L.merge_m + slots * kConsumerWarps * kMaxG * 4;      // [slots][W][16]
     L.rowinfo = L.merge_l + slots * kConsumerWarps * kMaxG * 4;      // [slots][2 + W][16]
@@ -213,7 +215,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     static_assert(!kFp8 || D == 128, "FP8 rows are one 128-byte swizzle row");
     constexpr uint32_t kHalves = kFp8 ? 1 : D / 64;  // 128-byte pieces of a token row
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
-    const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1, kFp8);
+    const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1, kFp8, bs);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,67 +312,102 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             }
         }
         const uint64_t policy = pa::l2_policy_evict_first();
-        const int rows = bs < kChunk ? bs : kChunk;  // token rows per TMA box
-        const int bpc = kChunk / rows;               // boxes per chunk and tensor
-        const int nblk = (kChunk + bs - 1) / bs;     // table entries a chunk spans
+        const int bs_shift = 31 - __clz(bs);          // block_size is 8, 16 or 32
+        const int bpc = kChunk >> rows_shift;         // blocks (TMA boxes per tensor) per chunk
         const int32_t oob_row = p.num_blocks * bs;
-        const int my_b = kFp8 ? (lane & 15) >> 1 : lane >> 1;  // the box this lane loads,
-        const bool my_v = (lane & 1) != 0;                      // whether of K or of V,
-        const bool my_scale = kFp8 && lane >= 16;               // and whether codes or scales
-        const CUtensorMap* my_map =
-            my_scale ? (my_v ? &vsmap : &ksmap) : (my_v ? &vmap : &kmap);
         const uint32_t tx_bytes = L.stage_bytes + (kFp8 ? 2 * kChunk * 4 : 0);
-        int32_t k = 0;  // chunks of this CTA walked so far
+        // A pair's table entries are read 32 at a time into a register window
+        // (lane l holds entry wbase + l).  The window after it, and the next
+        // pair's length and first window, are loaded one step ahead, so no
+        // chunk waits on a table read.  Entries past the context (up to the
+        // table width) are read but never used.
+        struct Walk {
+            Segment s;
+            int32_t n_raw, wbase, went, wnext;
+            const int32_t* trow;
+        };
+        auto open = [&](int32_t at) {
+            Walk w;
+            w.s = find_segment(prefix, B, Hkv, at, hi);
+            w.n_raw = __ldg(p.context_lens + w.s.i);
+            w.trow = p.block_tables + (int64_t)w.s.i * p.max_blocks;
+            w.wbase = (w.s.c0 * kChunk) >> bs_shift;
+            const int32_t j = w.wbase + lane;
+            w.went = j < p.max_blocks ? __ldg(w.trow + j) : -1;
+            w.wnext = j + 32 < p.max_blocks ? __ldg(w.trow + j + 32) : -1;
+            return w;
+        };
+        int32_t k = 0;      // chunks of this CTA walked so far
+        int stage = 0;      // k % S
+        uint32_t use = 0;   // (k / S) & 1: parity of the stage's current use
         bool dead = false;
+        Walk cur{}, nxt{};
+        if (lo < hi) cur = open(lo);
         for (int32_t pos = lo; pos < hi && !dead;) {
-            const Segment s = find_segment(prefix, B, Hkv, pos, hi);
-            const int32_t n = clamp_len(__ldg(p.context_lens + s.i), max_len);
-            const int32_t nb = (n + bs - 1) / bs;
-            const int32_t* trow = p.block_tables + (int64_t)s.i * p.max_blocks;
-            int32_t wbase = -1, went = -1;
-            for (int32_t t = 0; t < s.len; ++t, ++k) {
-                if ((k & (kProducerWarps - 1)) != prod) continue;
-                const int32_t tok_first = (s.c0 + t) * kChunk;
-                const int32_t j0 = tok_first / bs;
-                if (wbase < 0 || j0 + nblk > wbase + 32) {
-                    wbase = j0;
-                    const int32_t jj = wbase + lane;
-                    went = jj < nb ? __ldg(trow + jj) : -1;
-                }
-                const int stage = k % S;
-                if (k >= S) {
-                    const uint32_t par = (uint32_t)((k / S - 1) & 1);
-                    if (!__all_sync(0xffffffffu, pa::mbar_wait(&empty[stage], par, kWaitLimitNs))) {
+            const int32_t npos = pos + cur.s.len;
+            if (npos < hi) nxt = open(npos);
+            const int32_t nb = (clamp_len(cur.n_raw, max_len) + bs - 1) >> bs_shift;
+            for (int32_t t = 0; t < cur.s.len; ++t, ++k) {
+                if ((k & (kProducerWarps - 1)) == prod) {
+                    // Blocks j0 .. j0 + bpc - 1 of the chunk lie in one window
+                    // (windows start at multiples of bpc); a producer moves at
+                    // most 2 bpc <= 8 blocks per chunk, so one step suffices.
+                    const int32_t j0 = ((cur.s.c0 + t) * kChunk) >> bs_shift;
+                    if (j0 + bpc > cur.wbase + 32) {
+                        cur.wbase += 32;
+                        cur.went = cur.wnext;
+                        const int32_t j = cur.wbase + 32 + lane;
+                        cur.wnext = j < p.max_blocks ? __ldg(cur.trow + j) : -1;
+                    }
+                    if (k >= S && !__all_sync(0xffffffffu,
+                                              pa::mbar_wait(&empty[stage], use ^ 1u, kWaitLimitNs))) {
                         dead = true;
                         if (lane == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
                         break;
                     }
-                }
-                unsigned char* base = smem + stage * L.stage_bytes + (my_v ? L.stage_bytes / 2 : 0);
-                if (lane == 0) pa::mbar_arrive_expect_tx(&full[stage], tx_bytes);
-                __syncwarp();
-                const int32_t tok = tok_first + (my_b < bpc ? my_b : 0) * rows;
-                const int32_t jj = tok / bs;
-                const int32_t blk = __shfl_sync(0xffffffffu, went, (jj - wbase) & 31);
-                if (my_b < bpc) {
-                    bool ok = jj < nb;
-                    if (ok && (blk < 0 || blk >= p.num_blocks)) {
-                        ok = false;
-                        pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    int32_t blk[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        blk[b] = __shfl_sync(0xffffffffu, cur.went, (j0 - cur.wbase + b) & 31);
+                    // One lane issues the chunk's boxes: per block, K then V
+                    // (and, for FP8, their scales).  Blocks past the context
+                    // and out-of-pool ids load from outside the map: zeros.
+                    if (lane == 0) {
+                        pa::mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                        unsigned char* kdst = smem + stage * L.stage_bytes;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            if (b >= bpc) break;
+                            bool ok = j0 + b < nb;
+                            if (ok && (blk[b] < 0 || blk[b] >= p.num_blocks)) {
+                                ok = false;
+                                pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                            }
+                            const uint32_t off = ((uint32_t)b * kHalves << rows_shift) * 128;
+                            const int32_t row = ok ? blk[b] * bs : oob_row;
+                            const int32_t z = cur.s.g * (int32_t)kHalves;
+                            pa::tma_load_3d(kdst + off, &kmap, &full[stage], 0, row, z, policy);
+                            pa::tma_load_3d(kdst + L.stage_bytes / 2 + off, &vmap, &full[stage], 0,
+                                            row, z, policy);
+                            if constexpr (kFp8) {
+                                unsigned char* sdst = smem + L.scales + stage * L.scale_stage +
+                                                      (uint32_t)b * kScaleSlotBytes;
+                                const int32_t sb = ok ? blk[b] : p.num_blocks;
+                                pa::tma_load_3d(sdst, &ksmap, &full[stage], 0, cur.s.g, sb, policy);
+                                pa::tma_load_3d(sdst + L.scale_stage / 2, &vsmap, &full[stage], 0,
+                                                cur.s.g, sb, policy);
+                            }
+                        }
                     }
-                    if (!my_scale)
-                        pa::tma_load_3d(base + ((uint32_t)my_b * kHalves << rows_shift) * 128,
-                                        my_map, &full[stage], 0,
-                                        ok ? blk * bs + (tok - jj * bs) : oob_row,
-                                        s.g * (int32_t)kHalves, policy);
-                    else  // block_size scales of (block, KV head); zeros past the pool
-                        pa::tma_load_3d(smem + L.scales + stage * kScaleStageBytes +
-                                            ((my_v ? 4u : 0u) + (uint32_t)my_b) * kScaleSlotBytes,
-                                        my_map, &full[stage], 0, s.g, ok ? blk : p.num_blocks,
-                                        policy);
+                    __syncwarp();
+                }
+                if (++stage == S) {
+                    stage = 0;
+                    use ^= 1u;
                 }
             }
-            pos += s.len;
+            cur = nxt;
+            pos = npos;
         }
         // Every load this warp issued has landed before the CTA may exit.
         for (int s = prod; s < S && s < k; s += kProducerWarps) {
@@ -672,7 +709,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 float kmul[kKeyTiles][2], vmul[kKeyTiles][2];
                 float rs = 1.f;  // extra factor on o this chunk
                 if constexpr (kFp8) {
-                    const uint32_t sk = smem_base + L.scales + (uint32_t)stage * kScaleStageBytes;
+                    const uint32_t sk = smem_base + L.scales + (uint32_t)stage * L.scale_stage;
                     float vmax = 0.f;
 #pragma unroll
                     for (int mt = 0; mt < kKeyTiles; ++mt)
@@ -684,7 +721,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                  (tok & ((1u << rows_shift) - 1u))) * 4;
                             kmul[mt][h] = pa::lds_f32(sk + off) * qsc;
                             const float sv = (int)tok < valid
-                                                 ? pa::lds_f32(sk + 4 * kScaleSlotBytes + off)
+                                                 ? pa::lds_f32(sk + L.scale_stage / 2 + off)
                                                  : 0.f;
                             vmul[mt][h] = sv;
                             vmax = fmaxf(vmax, sv);
@@ -1067,9 +1104,11 @@ bool encode_code_map(CUtensorMap* map, const void* base, int32_t rows, int32_t H
     const cuuint64_t strides[2] = {(cuuint64_t)Hkv * 128, 128};
     const cuuint32_t box[3] = {128, (cuuint32_t)(block_size < kChunk ? block_size : kChunk), 1};
     const cuuint32_t elem[3] = {1, 1, 1};
+    // 128-byte promotion: a row of one KV head is 128 bytes; 256 would pull in
+    // the next head's row, which another CTA reads much later.
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1107,10 +1146,10 @@ size_t counters_bytes(int32_t B, int32_t H) {
 // and the ring depth decides; wider groups merge with all four warps.
 bool async_merge(int G) { return G <= 2; }
 
-int choose_stages(int D, int G, int B, bool fp8) {
-    const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1, fp8);
+int choose_stages(int D, int G, int B, bool fp8, int bs) {
+    const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1, fp8, bs);
     if (L0.total >= kSmemBudget) return 0;
-    const uint32_t per_stage = L0.stage_bytes + (fp8 ? kScaleStageBytes : 0);
+    const uint32_t per_stage = L0.stage_bytes + L0.scale_stage;
     int s = (int)((kSmemBudget - L0.total) / per_stage);
     if (s > kMaxStages) s = kMaxStages;
     s &= ~1;  // each producer owns every other stage
@@ -1165,7 +1204,7 @@ pa_status prepare(int32_t max_blocks, int32_t max_context_len, int32_t B, int32_
     const int64_t max_chunks = ((int64_t)max_blocks * block_size + kChunk - 1) / kChunk;
     if ((int64_t)B * Hkv * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
     const int G = H / Hkv;
-    const int stages = choose_stages(d, G, B, fp8);
+    const int stages = choose_stages(d, G, B, fp8, block_size);
     if (stages < 2) return PA_ERR_UNSUPPORTED;
     if (B > 0 && ws_bytes < pa_decode_workspace_size(B, H, d)) return PA_ERR_INVALID;
     prm->max_blocks = max_blocks;
@@ -1177,7 +1216,7 @@ pa_status prepare(int32_t max_blocks, int32_t max_context_len, int32_t B, int32_
     prm->num_blocks = num_blocks;
     prm->stages = stages;
     prm->scale_log2 = scale * kLog2e;
-    *smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1, fp8).total;
+    *smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1, fp8, block_size).total;
     return PA_OK;
 }
 
