@@ -169,6 +169,7 @@ WORKLOADS = {
     "qwen_longtail_bs16": lambda B: wl_mod().qwen_longtail(16),
     "qwen_longtail_bs32": lambda B: wl_mod().qwen_longtail(32),
     "prefix_share": lambda B: wl_mod().prefix_share(),
+    "multiturn_prefix": lambda B: wl_mod().multiturn_prefix(convs=B or 128),
 }
 CONTEXT_MIX = {
     "llama13b": "uniform[128,2048]",
@@ -178,6 +179,8 @@ CONTEXT_MIX = {
     "qwen_longtail_bs16": "95% lognormal(median 1500, sigma 1) <= 8192, 5% uniform[16384,24576]",
     "qwen_longtail_bs32": "95% lognormal(median 1500, sigma 1) <= 8192, 5% uniform[16384,24576]",
     "prefix_share": "1024-token prefix shared by 256 sequences + uniform[64,512] suffixes",
+    "multiturn_prefix": "end of 4-turn conversations: 1024-token shared system prompt, user "
+                        "U[32,256] and reply U[64,512] tokens per turn, prefix-cached allocation",
 }
 
 
@@ -186,10 +189,47 @@ def wl_mod():
     return workloads
 
 
+def play_trace(alloc, tr):
+    """Runs a multi-turn trace through the product allocator with prefix
+    caching (pa_alloc_prompt, pa_append_batch_tokens, pa_free) and times the
+    host calls (ctypes overhead included)."""
+    import numpy as np
+    t_prompt = t_append = 0.0
+    prompts = prompt_tokens = cached_tokens = appended = 0
+    for turn in tr["turns"]:
+        for sid, prompt in turn["prompts"]:
+            p = np.asarray(prompt, dtype=np.int32)
+            t0 = time.perf_counter()
+            cached_tokens += alloc.alloc_prompt(sid, p)
+            t_prompt += time.perf_counter() - t0
+            prompts += 1
+            prompt_tokens += len(prompt)
+        for step in turn["replies"]:
+            ids = np.asarray([s for s, _ in step], dtype=np.int64)
+            tok = np.asarray([t for _, t in step], dtype=np.int32)
+            t0 = time.perf_counter()
+            alloc.append_batch(ids, tokens=tok)
+            t_append += time.perf_counter() - t0
+            appended += len(step)
+        for sid in turn["free"]:
+            alloc.free(sid)
+    st = alloc.prefix_stats()
+    return {"prompts": prompts, "prompt_tokens": prompt_tokens, "cached_tokens": cached_tokens,
+            "token_hit_rate": round(cached_tokens / max(prompt_tokens, 1), 4),
+            "block_hit_rate": round(st["hits"] / max(st["lookups"], 1), 4),
+            "us_per_prompt": round(t_prompt * 1e6 / max(prompts, 1), 2),
+            "us_per_appended_token": round(t_append * 1e6 / max(appended, 1), 3),
+            "cache_entries": st["entries"], "evicted": st["evicted"],
+            "note": "host allocator via ctypes; the cached tokens skip prefill"}
+
+
 def setup_workload(args):
     """The named workload, its host tensors and the product allocator holding
     every sequence's history; the step's own token is appended last, so the
-    decode reads context_lens[i] tokens including it."""
+    decode reads context_lens[i] tokens including it.  Returns the decode
+    batch's sequence ids too."""
+    import numpy as np
+
     from paged_kv_cache_103_gb300 import binding
 
     w = WORKLOADS[args.workload](args.batch)
@@ -198,6 +238,17 @@ def setup_workload(args):
     if fp8:
         host.update(wl_mod().fp8_cache(w))
     alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
+    if "trace" in w.extra:
+        tr = w.extra["trace"]
+        w.extra["prefix_cache"] = play_trace(alloc, tr)
+        seqs = [tr["last"][c] for c in range(w.B)]
+        step_tok = np.random.default_rng(w.seed).integers(0, tr["vocab"], w.B).astype(np.int32)
+        slots, pairs = alloc.append_batch(seqs, tokens=step_tok)
+        assert len(pairs) == 0
+        max_blocks = int(math.ceil((int(w.context_lens.max()) + 1 + args.e2e_extra)
+                                   / w.block_size)) + 1
+        tbl, lens = alloc.export(seqs, max_blocks)
+        return w, host, alloc, slots, tbl, lens, max_blocks, seqs
     if w.prefix_len:
         alloc.alloc(0, w.prefix_len)
         for s in range(1, w.B):
@@ -208,11 +259,12 @@ def setup_workload(args):
     else:
         for i in range(w.B):
             alloc.alloc(i, int(w.context_lens[i]) - 1)
-    slots, pairs = alloc.append_batch(list(range(w.B)))
+    seqs = list(range(w.B))
+    slots, pairs = alloc.append_batch(seqs)
     assert len(pairs) == 0
     max_blocks = int(math.ceil((int(w.context_lens.max()) + args.e2e_extra) / w.block_size)) + 1
-    tbl, lens = alloc.export(list(range(w.B)), max_blocks)
-    return w, host, alloc, slots, tbl, lens, max_blocks
+    tbl, lens = alloc.export(seqs, max_blocks)
+    return w, host, alloc, slots, tbl, lens, max_blocks, seqs
 
 
 def run_gpu(args):
@@ -233,7 +285,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    w, host, alloc, slots, tbl, lens, max_blocks = setup_workload(args)
+    w, host, alloc, slots, tbl, lens, max_blocks, seqs = setup_workload(args)
     fp8 = args.kv_format == "fp8"
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
@@ -343,7 +395,7 @@ def run_gpu(args):
 
     # ---- e2e leg through the C ABI: host allocator step, pinned H2D, kernels, D2H
     e2e = run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode,
-                  fp8)
+                  fp8, seqs)
 
     l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9) if not flush_l2
                else "L2 flushed between steps (512 MiB write + read outside the timed kernels; %.3f GB "
@@ -380,6 +432,8 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
     }
+    if "prefix_cache" in w.extra:
+        result["prefix_cache"] = w.extra["prefix_cache"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds, fp8)
     if rank == 0:
@@ -388,7 +442,8 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode, fp8):
+def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode, fp8,
+            seqs):
     """Real decode steps through the C ABI with host buffers: each step appends
     one token per sequence in the host allocator, exports the tables into
     pinned memory, copies them and the step's q / new K / new V to the device,
@@ -418,7 +473,7 @@ def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, de
     d_slots = torch.empty(B, dtype=torch.int64, device=dev)
     d_pairs = torch.empty((B, 2), dtype=torch.int32, device=dev)
     d_out = torch.empty_like(q)
-    ids = list(range(B))
+    ids = list(seqs)
     n_tbl, n_lens, n_slots, n_pairs = (h_tbl.numpy(), h_lens.numpy(), h_slots.numpy(),
                                       h_pairs.numpy())
     h2d = d2h = 0

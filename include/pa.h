@@ -8,6 +8,7 @@
  *   [P3] "vLLM 深度拆解：当大模型推理学会「分页注意力」——PagedAttention、连续批处理与
  *        V1 引擎如何重写 GPU 推理服务的心智模型" (chenxutan.com/d/4834.html)
  *   [P4] "LLM推理优化技术地图：从KV Cache到量化与投机解码" (qwbw.cn/news/280730)
+ *   [P5] the untitled Qwen2.5-7B-on-vLLM deployment page (mhpq.cn/news/468822)
  *
  * Conventions
  *   - Every call returns a pa_status; nothing throws across the ABI.
@@ -154,6 +155,60 @@ PA_API pa_status pa_block_ref(const pa_allocator* a, int32_t block, int32_t* ref
 /* Copies the free list, front first, into out (host, capacity cap). */
 PA_API pa_status pa_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
 PA_API pa_status pa_alloc_stats_get(const pa_allocator* a, pa_alloc_stats* out);
+
+/* ------------------------------------------------------------------------
+ * Automatic prefix caching ([P5] section 3.2: a prompt is cut into blocks of
+ * block_size tokens, each block's KV is cached under a hash of its token ids,
+ * and a request reuses the cached KV of a prefix that matches token for token
+ * and is aligned to block boundaries; [P1] section 4.2: reuse across requests,
+ * e.g. the turns of a conversation).
+ *
+ * A full block is cached under the key (id of the cache entry holding the
+ * previous block's content, or 0 for the first block, the block's token ids),
+ * so a key names the whole prefix up to the block; entry ids are never reused.
+ * A freed block keeps its entry while it waits on the free list, and a hit
+ * takes it back off the list; a block the free list hands out again (from its
+ * front, oldest freed first) loses its entry.  Only sequences created by
+ * pa_alloc_prompt and grown by pa_append_token / pa_append_batch_tokens know
+ * their token ids; pa_alloc, pa_append_slot and pa_append_batch on a sequence
+ * stop its registering.  The cache costs host memory only (one entry of
+ * block_size token ids per cached block).
+ * ---------------------------------------------------------------------- */
+typedef struct pa_prefix_stats {
+    int64_t lookups;      /* prompt blocks looked up (each walk stops at its first miss) */
+    int64_t hits;         /* of which found */
+    int64_t registered;   /* blocks entered into the cache */
+    int64_t evicted;      /* entries dropped because their block was handed out again */
+    int64_t entries;      /* entries now in the cache */
+    int64_t cached_free;  /* free-list blocks that still hold an entry */
+} pa_prefix_stats;
+
+/* Creates sequence seq_id (which must be new) holding the prompt
+ * tokens[0..num_tokens) (host int32 token ids).  The prompt's full blocks are
+ * looked up in order; each one found is shared (count +1, taken off the free
+ * list if it was there) until the first miss.  The remaining blocks come from
+ * the front of the free list, and each new full block is entered into the
+ * cache (its K/V must be written, e.g. by pa_reshape_and_cache at the slots
+ * of pa_seq_slots, before another sequence reads it).  *cached_tokens
+ * (nullable) receives the number of leading tokens whose K/V is already in
+ * the cache (a multiple of block_size): the caller computes and writes only
+ * the rest.  All or nothing: PA_ERR_OOM leaves every state unchanged. */
+PA_API pa_status pa_alloc_prompt(pa_allocator* a, int64_t seq_id, const int32_t* tokens,
+                                 int32_t num_tokens, int32_t* cached_tokens);
+
+/* pa_append_slot that also records the appended token's id: when the token
+ * fills its block, the block is entered into the cache (unless the same key
+ * is cached already, in which case the sequence's chain continues from that
+ * entry). */
+PA_API pa_status pa_append_token(pa_allocator* a, int64_t seq_id, int32_t token,
+                                 int64_t* slot_out, int32_t* cow_src, int32_t* cow_dst);
+
+/* pa_append_batch with one token id per sequence (tokens: host, B int32). */
+PA_API pa_status pa_append_batch_tokens(pa_allocator* a, const int64_t* seq_ids,
+                                        const int32_t* tokens, int32_t B, int64_t* slot_mapping,
+                                        int32_t* cow_pairs, int32_t* num_cow);
+
+PA_API pa_status pa_prefix_stats_get(const pa_allocator* a, pa_prefix_stats* out);
 
 /* ------------------------------------------------------------------------
  * Device operations.

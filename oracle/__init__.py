@@ -33,6 +33,9 @@ Contents:
 * :func:`kv_bytes_per_token` / :func:`kv_cache_bytes` -- the closed forms.
 * :func:`reshape_and_cache_fp8`, :func:`decode_fp8`, :func:`e4m3_encode` -- the
   FP8 KV cache (a reading, see the comment above :data:`E4M3_MAX`).
+* ``BlockManagerModel.allocate_prompt`` / ``append_token`` -- automatic prefix
+  caching of full blocks ([P5] section 3.2, [P1] section 4.2; a reading, see
+  the class docstring).
 """
 from __future__ import annotations
 
@@ -323,6 +326,26 @@ class BlockManagerModel:
     new block from the front of the free list, the pair (old, new) is reported
     for a copy and the old block's count drops by one -- the last sharer left
     writes in place.
+
+    Automatic prefix caching ([P5] section 3.2: a prompt is cut into blocks of
+    block_size tokens, each block's KV is cached under a hash of its token ids,
+    and a new request reuses the cached blocks of a prefix that matches token
+    for token and is aligned to block boundaries -- a change in the first block
+    invalidates every later one; [P1] section 4.2: the reuse spans requests,
+    e.g. turns of a conversation).  Reading: a FULL block's key is (the id of
+    the cache entry holding the previous block's content, or 0 for the first
+    block, the block's token ids), so a key names its whole prefix; entry ids
+    are never reused.  ``allocate_prompt`` walks the prompt's full blocks and
+    reuses each block found (reference +1; a block found on the free list is
+    taken off it) until the first miss, then allocates the rest from the front
+    of the free list and registers every new full block.  ``append_token``
+    appends like ``append_slot`` and registers the sequence's block when it
+    becomes full (if its key is already cached, the sequence's chain continues
+    from that entry and its own block stays unregistered).  A freed block keeps
+    its entry while it waits on the free list; a block taken from the front of
+    the free list loses its entry (eviction, oldest freed first).  Sequences
+    created or grown without token ids (``allocate``, ``append_slot``,
+    ``append_batch``) are not tracked and register nothing.
     """
 
     def __init__(self, num_blocks: int, block_size: int, init_free_order=None):
@@ -337,6 +360,27 @@ class BlockManagerModel:
         self.allocated: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
         self.ref = [0] * num_blocks
+        # prefix cache
+        self.cache: dict[tuple, tuple[int, int]] = {}   # key -> (entry id, block)
+        self.block_key: dict[int, tuple] = {}           # block -> key of its entry
+        self.next_entry = 1
+        self.tracked: dict[int, bool] = {}
+        self.pending: dict[int, list[int]] = {}         # token ids of the partial last block
+        self.chain: dict[int, int] = {}                 # entry id of the last full block's content
+        self.pstats = {"lookups": 0, "hits": 0, "registered": 0, "evicted": 0}
+
+    def _take_front(self) -> int:
+        b = self.free_blocks.popleft()
+        key = self.block_key.pop(b, None)
+        if key is not None:
+            del self.cache[key]
+            self.pstats["evicted"] += 1
+        self.ref[b] = 1
+        return b
+
+    def _untrack(self, seq_id: int) -> None:
+        self.tracked[seq_id] = False
+        self.pending[seq_id] = []
 
     # -- [P1] section 3.2 -------------------------------------------------
     def allocate(self, seq_id: int, num_tokens: int) -> None:
@@ -353,10 +397,11 @@ class BlockManagerModel:
             if len(self.free_blocks) < need:
                 raise OracleOOM("need %d blocks, %d free" % (need, len(self.free_blocks)))
             for _ in range(need):
-                b = self.free_blocks.popleft()
-                self.ref[b] = 1
-                table.append(b)
+                table.append(self._take_front())
         self.allocated[seq_id] = table
+        if num_tokens > cur_len or seq_id not in self.tracked:
+            self._untrack(seq_id)
+            self.chain.setdefault(seq_id, 0)
         self.lens[seq_id] = max(cur_len, num_tokens)
 
     def free(self, seq_id: int) -> None:
@@ -368,6 +413,7 @@ class BlockManagerModel:
                 self.free_blocks.append(b)
         del self.allocated[seq_id]
         del self.lens[seq_id]
+        del self.tracked[seq_id], self.pending[seq_id], self.chain[seq_id]
 
     # -- [P3] section 3.3 -------------------------------------------------
     def _blocks_needed_for_append(self, seq_id: int, ref_view) -> int:
@@ -386,6 +432,7 @@ class BlockManagerModel:
             raise OracleInvalid("unknown sequence")
         if self._blocks_needed_for_append(seq_id, lambda b: self.ref[b]) > len(self.free_blocks):
             raise OracleOOM("no free block")
+        self._untrack(seq_id)
         return self._append_unchecked(seq_id)
 
     def _append_unchecked(self, seq_id: int):
@@ -394,29 +441,29 @@ class BlockManagerModel:
         pos = self.lens[seq_id]
         cow = None
         if pos == len(table) * bs:
-            b = self.free_blocks.popleft()
-            self.ref[b] = 1
-            table.append(b)
+            table.append(self._take_front())
         else:
             last = table[pos // bs]
             if self.ref[last] > 1:
-                new = self.free_blocks.popleft()
+                new = self._take_front()
                 self.ref[last] -= 1
-                self.ref[new] = 1
                 table[pos // bs] = new
                 cow = (last, new)
         self.lens[seq_id] = pos + 1
         slot = table[pos // bs] * bs + pos % bs
         return slot, cow
 
-    def append_batch(self, seq_ids):
+    def append_batch(self, seq_ids, tokens=None):
         """One new token for each sequence of a decode batch, all or nothing.
 
         Sequences are served in the given order (so with k sharers of one
         partial block in the batch, the first k-1 copy it and the last writes
-        in place).  Returns ``(slots, cow_pairs)``.
+        in place).  Returns ``(slots, cow_pairs)``.  With ``tokens`` (one token
+        id per sequence) each append is an :meth:`append_token`.
         """
         seq_ids = [int(s) for s in seq_ids]
+        if tokens is not None and len(tokens) != len(seq_ids):
+            raise OracleInvalid("one token per sequence")
         if len(set(seq_ids)) != len(seq_ids):
             raise OracleInvalid("duplicate sequence in batch")
         for s in seq_ids:
@@ -436,12 +483,98 @@ class BlockManagerModel:
         if need > len(self.free_blocks):
             raise OracleOOM("batch needs %d blocks, %d free" % (need, len(self.free_blocks)))
         slots, pairs = [], []
-        for s in seq_ids:
-            slot, cow = self._append_unchecked(s)
+        for r, s in enumerate(seq_ids):
+            if tokens is None:
+                self._untrack(s)
+                slot, cow = self._append_unchecked(s)
+            else:
+                slot, cow = self._append_token_unchecked(s, int(tokens[r]))
             slots.append(slot)
             if cow is not None:
                 pairs.append(cow)
         return slots, pairs
+
+    # -- automatic prefix caching ([P5] section 3.2, [P1] section 4.2) ---------
+    def allocate_prompt(self, seq_id: int, tokens) -> int:
+        """Creates ``seq_id`` holding the prompt ``tokens``; returns how many of
+        its tokens were found in the cache (a multiple of block_size)."""
+        tokens = [int(t) for t in tokens]
+        if seq_id in self.allocated:
+            raise OracleInvalid("sequence exists")
+        bs = self.block_size
+        n = len(tokens)
+        full = n // bs
+        chain, hits = 0, []
+        for i in range(full):          # the walk stops at the first miss
+            self.pstats["lookups"] += 1
+            key = (chain, tuple(tokens[i * bs:(i + 1) * bs]))
+            found = self.cache.get(key)
+            if found is None:
+                break
+            chain = found[0]
+            hits.append(found[1])
+        revive = sum(1 for b in hits if self.ref[b] == 0)
+        need = math.ceil(n / bs) - len(hits)
+        if need > len(self.free_blocks) - revive:
+            self.pstats["lookups"] -= min(full, len(hits) + 1)
+            raise OracleOOM("need %d blocks, %d free" % (need, len(self.free_blocks) - revive))
+        self.pstats["hits"] += len(hits)
+        table = []
+        for b in hits:
+            if self.ref[b] == 0:
+                self.free_blocks.remove(b)
+            self.ref[b] += 1
+            table.append(b)
+        for i in range(len(hits), math.ceil(n / bs)):
+            b = self._take_front()
+            table.append(b)
+            if i < full:
+                chain = self._register(chain, tokens[i * bs:(i + 1) * bs], b)
+        self.allocated[seq_id] = table
+        self.lens[seq_id] = n
+        self.tracked[seq_id] = True
+        self.pending[seq_id] = tokens[full * bs:]
+        self.chain[seq_id] = chain
+        return len(hits) * bs
+
+    def _register(self, chain: int, block_tokens, block: int) -> int:
+        key = (chain, tuple(block_tokens))
+        found = self.cache.get(key)
+        if found is not None:
+            return found[0]
+        eid = self.next_entry
+        self.next_entry += 1
+        self.cache[key] = (eid, block)
+        self.block_key[block] = key
+        self.pstats["registered"] += 1
+        return eid
+
+    def append_token(self, seq_id: int, token: int):
+        """:meth:`append_slot` that also records the token id; returns
+        ``(slot, cow)``."""
+        if seq_id not in self.allocated:
+            raise OracleInvalid("unknown sequence")
+        if self._blocks_needed_for_append(seq_id, lambda b: self.ref[b]) > len(self.free_blocks):
+            raise OracleOOM("no free block")
+        return self._append_token_unchecked(seq_id, int(token))
+
+    def _append_token_unchecked(self, seq_id: int, token: int):
+        slot, cow = self._append_unchecked(seq_id)
+        if self.tracked[seq_id]:
+            pend = self.pending[seq_id]
+            pend.append(token)
+            if len(pend) == self.block_size:
+                pos = self.lens[seq_id] - 1
+                block = self.allocated[seq_id][pos // self.block_size]
+                self.chain[seq_id] = self._register(self.chain[seq_id], pend, block)
+                self.pending[seq_id] = []
+        return slot, cow
+
+    def prefix_stats(self) -> dict:
+        d = dict(self.pstats)
+        d["entries"] = len(self.cache)
+        d["cached_free"] = sum(1 for b in self.free_blocks if b in self.block_key)
+        return d
 
     def fork(self, parent: int, child: int) -> None:
         """[P4] section 3.3 / [P3] section 3.3: the child shares the parent's
@@ -453,6 +586,9 @@ class BlockManagerModel:
             self.ref[b] += 1
         self.allocated[child] = table
         self.lens[child] = self.lens[parent]
+        self.tracked[child] = self.tracked[parent]
+        self.pending[child] = list(self.pending[parent])
+        self.chain[child] = self.chain[parent]
 
     # -- exports ------------------------------------------------------------
     def slot_of(self, seq_id: int, pos: int) -> int:

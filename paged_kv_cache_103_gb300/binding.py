@@ -34,6 +34,12 @@ class AllocStats(ctypes.Structure):
                 ("num_tokens", ctypes.c_int64)]
 
 
+class PrefixStats(ctypes.Structure):
+    _fields_ = [("lookups", ctypes.c_int64), ("hits", ctypes.c_int64),
+                ("registered", ctypes.c_int64), ("evicted", ctypes.c_int64),
+                ("entries", ctypes.c_int64), ("cached_free", ctypes.c_int64)]
+
+
 SIGNATURES = {
     "pa_status_str": (ctypes.c_char_p, [_ST]),
     "pa_version": (_I32, []),
@@ -50,6 +56,10 @@ SIGNATURES = {
     "pa_block_ref": (_ST, [_P, _I32, _P]),
     "pa_free_list": (_ST, [_P, _P, _I32, _P]),
     "pa_alloc_stats_get": (_ST, [_P, ctypes.POINTER(AllocStats)]),
+    "pa_alloc_prompt": (_ST, [_P, _I64, _P, _I32, _P]),
+    "pa_append_token": (_ST, [_P, _I64, _I32, _P, _P, _P]),
+    "pa_append_batch_tokens": (_ST, [_P, _P, _P, _I32, _P, _P, _P]),
+    "pa_prefix_stats_get": (_ST, [_P, ctypes.POINTER(PrefixStats)]),
     "pa_reshape_and_cache": (_ST, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _ST, _P]),
     "pa_reshape_and_cache_fp8": (_ST, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                        _ST, _P]),
@@ -292,17 +302,46 @@ class Allocator:
                                         ctypes.byref(dst)), "pa_append_slot")
         return slot.value, (None if src.value < 0 else (src.value, dst.value))
 
-    def append_batch(self, seq_ids, slot_mapping=None, cow_pairs=None):
+    def append_batch(self, seq_ids, slot_mapping=None, cow_pairs=None, tokens=None):
         """Returns ``(slot_mapping int64 [B], cow_pairs int32 [P, 2])``; output arrays may
-        be passed in (e.g. pinned host memory as numpy views)."""
+        be passed in (e.g. pinned host memory as numpy views).  With ``tokens`` (one id
+        per sequence) this is ``pa_append_batch_tokens``."""
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
         B = ids.shape[0]
         slots = np.empty(B, np.int64) if slot_mapping is None else slot_mapping
         pairs = np.empty((max(B, 1), 2), np.int32) if cow_pairs is None else cow_pairs
         n = ctypes.c_int32()
-        _check(self._lib.pa_append_batch(self._h, _np_ptr(ids), B, _np_ptr(slots),
-                                         _np_ptr(pairs), ctypes.byref(n)), "pa_append_batch")
+        if tokens is None:
+            _check(self._lib.pa_append_batch(self._h, _np_ptr(ids), B, _np_ptr(slots),
+                                             _np_ptr(pairs), ctypes.byref(n)), "pa_append_batch")
+        else:
+            tok = np.ascontiguousarray(tokens, dtype=np.int32)
+            if tok.shape[0] != B:
+                raise ValueError("one token per sequence")
+            _check(self._lib.pa_append_batch_tokens(self._h, _np_ptr(ids), _np_ptr(tok), B,
+                                                    _np_ptr(slots), _np_ptr(pairs),
+                                                    ctypes.byref(n)), "pa_append_batch_tokens")
         return slots, pairs[: n.value]
+
+    def alloc_prompt(self, seq_id: int, tokens) -> int:
+        """``pa_alloc_prompt``: returns the number of leading tokens already cached."""
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        cached = ctypes.c_int32()
+        _check(self._lib.pa_alloc_prompt(self._h, seq_id, _np_ptr(tok) if tok.size else None,
+                                         int(tok.shape[0]), ctypes.byref(cached)),
+               "pa_alloc_prompt")
+        return cached.value
+
+    def append_token(self, seq_id: int, token: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_append_token(self._h, seq_id, int(token), ctypes.byref(slot),
+                                         ctypes.byref(src), ctypes.byref(dst)), "pa_append_token")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def prefix_stats(self) -> dict:
+        s = PrefixStats()
+        _check(self._lib.pa_prefix_stats_get(self._h, ctypes.byref(s)), "pa_prefix_stats_get")
+        return {f: getattr(s, f) for f, _ in PrefixStats._fields_}
 
     def fork(self, parent: int, child: int) -> None:
         _check(self._lib.pa_fork(self._h, parent, child), "pa_fork")

@@ -25,6 +25,13 @@ The shapes follow the pages' own examples:
 * ``prefix_share``: 256 sequences sharing a 1024-token prefix (64 blocks of
   16) plus unique suffixes uniform in [64, 512]; ``prefix_share_cow`` uses a
   1000-token prefix with no suffix, so the shared last block is partial.
+* ``multiturn_trace`` / ``multiturn_prefix``: conversations that all start
+  with the same system prompt, several turns each; turn t's prompt is the
+  conversation so far plus a new user message, the reply is generated token
+  by token, and the previous turn's sequence is freed once the next exists --
+  the multi-turn, shared-system-prompt case the prefix-caching pages describe
+  ("LLM推理优化：vLLM PagedAttention深度解析与工程实践", section 4.2).  Token ids are
+  uniform over a small vocabulary; the sizes are this module's choice.
 
 Pools hold 1.25 x the blocks the lengths need and are handed out in a seeded
 random order, so blocks land scattered over the pool.
@@ -125,6 +132,57 @@ def prefix_share(seed: int = 1005, B: int = 256, prefix_len: int = 1024,
     name = "prefix_share" if with_suffix else "prefix_share_cow"
     return Workload(name, B, 28, 4, 128, bs, "bf16", lens, N, _perm(N, seed + 1), seed,
                     layers=28, prefix_len=prefix_len, suffix_lens=suffix)
+
+
+def multiturn_trace(seed: int, convs: int, turns: int, system: int, user=(8, 60),
+                    reply=(4, 40), vocab: int = 500, block_size: int = 16,
+                    pool_factor: float = 2.5) -> dict:
+    """A multi-turn serving trace (token ids only).
+
+    ``turns`` is a list of turns; each holds ``prompts`` [(seq_id, tokens)],
+    ``replies`` (decode steps, each a list of (seq_id, token) for the
+    conversations still generating) and ``free`` (the previous turn's
+    sequence ids).  ``history`` holds each conversation's final tokens,
+    ``last`` its final sequence id; ``N`` and ``order`` size and order a pool.
+    """
+    rng = np.random.default_rng(seed)
+    sys_p = rng.integers(0, vocab, system).tolist()
+    hist = {c: list(sys_p) for c in range(convs)}
+    sid, cur, out = 0, {}, []
+    for _ in range(turns):
+        prompts, old = [], dict(cur)
+        for c in range(convs):
+            hist[c] += rng.integers(0, vocab, int(rng.integers(user[0], user[1]))).tolist()
+            prompts.append((sid, list(hist[c])))
+            cur[c] = sid
+            sid += 1
+        lens = {c: int(rng.integers(reply[0], reply[1])) for c in range(convs)}
+        replies = []
+        for k in range(max(lens.values())):
+            step = []
+            for c in range(convs):
+                if k < lens[c]:
+                    tok = int(rng.integers(0, vocab))
+                    hist[c].append(tok)
+                    step.append((cur[c], tok))
+            replies.append(step)
+        out.append({"prompts": prompts, "replies": replies, "free": sorted(old.values())})
+    need = sum(math.ceil(len(h) / block_size) for h in hist.values())
+    N = int(need * pool_factor)
+    return {"turns": out, "history": hist, "last": dict(cur), "N": N, "vocab": vocab,
+            "order": np.random.default_rng(seed + 1).permutation(N).astype(np.int32)}
+
+
+def multiturn_prefix(seed: int = 1006, convs: int = 128, turns: int = 4) -> Workload:
+    """Decode batch at the end of a multi-turn trace: ``convs`` conversations,
+    a 1024-token system prompt, user messages U[32, 256], replies U[64, 512],
+    Qwen2.5-7B shape (28 / 4 heads of 128, bf16, block 16)."""
+    bs = 16
+    tr = multiturn_trace(seed, convs, turns, 1024, user=(32, 257), reply=(64, 513),
+                         vocab=32000, block_size=bs)
+    lens = np.array([len(tr["history"][c]) for c in range(convs)], dtype=np.int32)
+    return Workload("multiturn_prefix", convs, 28, 4, 128, bs, "bf16", lens, tr["N"],
+                    tr["order"], seed, layers=28, extra={"trace": tr})
 
 
 def normal_tensor(shape, dtype, seed: int, chunk: int = 1 << 26) -> torch.Tensor:
