@@ -612,6 +612,93 @@ def run_reference(args):
     }))
 
 
+def run_swap(args):
+    """Swap bandwidth: one pa_swap_blocks launch moves the blocks of 16 of the
+    llama13b batch's sequences (all 8 layers' K and V: 16 pools) from the
+    device pools to a pinned host pool, and another moves them back; each is
+    timed with CUDA events over repeated launches (the copies are idempotent).
+    Baselines on the same box: one cudaMemcpyAsync of a contiguous buffer of
+    the same bytes (the copy engines' rate over the host link) and one
+    cudaMemcpyAsync per block and pool."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+    from paged_kv_cache_103_gb300 import build as pa_build
+
+    pa_build.build()
+    binding.load()
+    w = wl_mod().llama13b()
+    layers, nseq = 8, 16
+    alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
+    for i in range(w.B):
+        alloc.alloc(i, int(w.context_lens[i]))
+    blocks = sum(alloc.seq_info(i)[1] for i in range(nseq))
+    alloc.set_swap_pool(blocks)
+    pairs = np.concatenate([alloc.swap_out(i) for i in range(nseq)])
+    dev = torch.device("cuda")
+    shape = (w.num_blocks, w.block_size, w.Hkv, w.d)
+    pools = [torch.empty(shape, dtype=torch.float16, device=dev).normal_()
+             for _ in range(2 * layers)]
+    host = [torch.empty((blocks,) + shape[1:], dtype=torch.float16).pin_memory()
+            for _ in range(2 * layers)]
+    out_pairs = torch.from_numpy(pairs.astype(np.int32)).to(dev)
+    in_pairs = torch.from_numpy(pairs[:, ::-1].copy().astype(np.int32)).to(dev)
+    block_bytes = pools[0][0].numel() * 2
+    moved = blocks * block_bytes * 2 * layers
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(3, min(args.steps, 20))
+    t_out = timed(lambda: binding.pa_swap_blocks(pools, host, out_pairs), reps)
+    t_in = timed(lambda: binding.pa_swap_blocks(host, pools, in_pairs), reps)
+    flags = binding.pa_check_device_errors()
+    if flags:
+        raise RuntimeError("device error flags 0x%x" % flags)
+    # bit check of one pool after the round trip
+    src_idx = torch.from_numpy(pairs[:, 0].astype(np.int64)).to(dev)
+    ok = torch.equal(host[0].to(dev), pools[0][src_idx])
+    flat_d = torch.empty(moved // 2, dtype=torch.float16, device=dev)
+    flat_h = torch.empty(moved // 2, dtype=torch.float16).pin_memory()
+    t_cd2h = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), reps)
+    t_ch2d = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), reps)
+    sub = pairs[: max(1, len(pairs) // 8)]          # per-block copies: an eighth of the blocks
+
+    def per_block():
+        for p, h in zip(pools, host):
+            for s, d in sub:
+                h[int(d)].copy_(p[int(s)], non_blocking=True)
+    t_pb = timed(per_block, 2) * 8
+    gbs = lambda t: round(moved / (t * 1e-3) / 1e9, 1)
+    print(json.dumps({
+        "metric": "KV swap GB/s (device->host; host->device in h2d)", "value": gbs(t_out),
+        "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": 3, "ms_per_step": round(t_out, 4),
+        "higher_is_better": True, "dtype": "f16 (bit copies)", "data": "synthetic",
+        "h2d": {"value": gbs(t_in), "ms": round(t_in, 4)},
+        "bit_exact_round_trip": bool(ok),
+        "contiguous_memcpy": {"d2h": gbs(t_cd2h), "h2d": gbs(t_ch2d),
+                              "note": "one cudaMemcpyAsync of the same bytes, pinned host"},
+        "per_block_memcpy": {"d2h": gbs(t_pb),
+                             "note": "one cudaMemcpyAsync per block and pool (scaled from 1/8)"},
+        "roofline": {"bound": "host link", "achieved": gbs(t_out), "peak": gbs(t_cd2h),
+                     "unit": "GB/s", "frac": round(t_cd2h / t_out, 3),
+                     "peak_source": "contiguous cudaMemcpyAsync device->pinned host, same run"},
+        "gpu_launches": 2 * reps,
+        "config": {"workload": "swap of 16 llama13b sequences x 8 layers (K and V)",
+                   "blocks": int(blocks), "pools": 2 * layers, "block_bytes": int(block_bytes),
+                   "bytes_per_direction": int(moved)}}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -627,11 +714,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-format", choices=["native", "fp8"], default="native",
                     help="cache in the workload's 16-bit dtype, or E4M3 codes + fp32 scales")
+    ap.add_argument("--measure", choices=["decode", "swap"], default="decode",
+                    help="swap: device<->host block swap bandwidth instead of the decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.measure == "swap":
+        run_swap(args)
     else:
         run_gpu(args)
 

@@ -211,6 +211,50 @@ PA_API pa_status pa_append_batch_tokens(pa_allocator* a, const int64_t* seq_ids,
 PA_API pa_status pa_prefix_stats_get(const pa_allocator* a, pa_prefix_stats* out);
 
 /* ------------------------------------------------------------------------
+ * Swap space ([P1] section 3.2: an allocation that finds too few free blocks
+ * calls for swap or preemption; [P2] section 4: with swap space enabled the
+ * KV cache moves to CPU memory, at a cost in speed).
+ *
+ * The allocator keeps a host pool of num_host_blocks blocks with its own free
+ * list (taken from the front, returned to the back).  A swapped-out sequence
+ * holds host blocks instead of device blocks; it cannot be appended to,
+ * forked, grown or exported until it is swapped back in; pa_free releases its
+ * host blocks.  The caller moves the data with pa_swap_blocks (device pool ->
+ * host pool before the device blocks are reused; host -> device after a swap
+ * in, before the sequence is read).
+ * ---------------------------------------------------------------------- */
+typedef struct pa_swap_stats {
+    int32_t host_blocks;   /* host pool size */
+    int32_t host_free;     /* host blocks on the host free list */
+    int32_t swapped_seqs;  /* sequences now swapped out */
+} pa_swap_stats;
+
+/* Sets the host pool size (once; host blocks 0..num_host_blocks-1 in order). */
+PA_API pa_status pa_alloc_set_swap_pool(pa_allocator* a, int32_t num_host_blocks);
+
+/* Swaps a sequence out: each block of its table, in order, takes a host block
+ * from the front of the host free list; pairs (host, capacity cap pairs of
+ * int32) receives {device block, host block} per block and *n their count.
+ * Each device block's count then drops by one (blocks reaching zero go to the
+ * back of the device free list, as in pa_free), so a block still shared with
+ * live sequences stays on the device and the swapped sequence keeps its own
+ * host copy.  All or nothing: PA_ERR_OOM (host pool full) leaves every state
+ * unchanged. */
+PA_API pa_status pa_swap_out(pa_allocator* a, int64_t seq_id, int32_t* pairs, int32_t cap,
+                             int32_t* n);
+
+/* Swaps a sequence back in: one device block from the front of the free list
+ * per host block, in table order; pairs receives {host block, device block};
+ * the host blocks return to the back of the host free list.  All or nothing
+ * (PA_ERR_OOM).  The sequence's blocks are private afterwards. */
+PA_API pa_status pa_swap_in(pa_allocator* a, int64_t seq_id, int32_t* pairs, int32_t cap,
+                            int32_t* n);
+
+PA_API pa_status pa_swap_stats_get(const pa_allocator* a, pa_swap_stats* out);
+/* Copies the host free list, front first, into out (host, capacity cap). */
+PA_API pa_status pa_host_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n);
+
+/* ------------------------------------------------------------------------
  * Device operations.
  * ---------------------------------------------------------------------- */
 
@@ -260,6 +304,23 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
 PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                                 int32_t num_layers, const int32_t* pairs, int32_t num_pairs,
                                 int64_t block_bytes, int32_t num_blocks, void* stream);
+
+/* Block copies between two pools, for swapping: for each pool pair l in
+ * [0, num_pools) (a layer's K or V) and each pair p, block pairs[p][1] of
+ * dst_pools[l] becomes a bit copy of block pairs[p][0] of src_pools[l].  A
+ * pool is device memory or pinned (page-locked) host memory the device can
+ * address (e.g. cudaHostAlloc / torch pin_memory); the kernel moves the data
+ * itself, so one launch covers every block of every layer.  block_bytes is
+ * the bytes of one block of one pool (block_size * Hkv * d * element size,
+ * a multiple of 16); pointers must be 16-byte aligned.  A pair whose source
+ * is outside [0, src_blocks) or destination outside [0, dst_blocks) is
+ * skipped and sets PA_DEVERR_PAIR.  Destinations must be distinct.
+ *   src_pools, dst_pools (host) arrays of num_pools pointers
+ *   pairs                (device or pinned host) [num_pairs][2] int32 {src, dst} */
+PA_API pa_status pa_swap_blocks(const void* const* src_pools, void* const* dst_pools,
+                                int32_t num_pools, const int32_t* pairs, int32_t num_pairs,
+                                int64_t block_bytes, int32_t src_blocks, int32_t dst_blocks,
+                                void* stream);
 
 /* Bytes of workspace pa_decode needs for batch B, H query heads and head dim
  * d; 0 for unsupported sizes.  The workspace holds per-(sequence, KV head)

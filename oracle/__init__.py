@@ -36,6 +36,9 @@ Contents:
 * ``BlockManagerModel.allocate_prompt`` / ``append_token`` -- automatic prefix
   caching of full blocks ([P5] section 3.2, [P1] section 4.2; a reading, see
   the class docstring).
+* ``BlockManagerModel.swap_out`` / ``swap_in`` and :func:`swap_blocks` --
+  moving a sequence's blocks to a host pool and back ([P1] section 3.2, [P2]
+  section 4; a reading, see ``swap_out``).
 """
 from __future__ import annotations
 
@@ -256,6 +259,15 @@ def decode_fp8(q, q_dtype: int, k_codes, v_codes, k_scale, v_scale, block_tables
     return out
 
 
+def swap_blocks(src_pools, dst_pools, pairs) -> None:
+    """The swap copies: for every pool pair (a layer's K or V, on the device
+    and in host memory) and every pair ``(s, d)``, block ``d`` of the
+    destination becomes a copy of block ``s`` of the source."""
+    for src, dst in zip(src_pools, dst_pools):
+        for s, d in pairs:
+            dst[int(d)] = src[int(s)]
+
+
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache) -> None:
     """The KV append, in place: token t goes to ``cache[s // bs, s % bs]``.
 
@@ -368,6 +380,10 @@ class BlockManagerModel:
         self.pending: dict[int, list[int]] = {}         # token ids of the partial last block
         self.chain: dict[int, int] = {}                 # entry id of the last full block's content
         self.pstats = {"lookups": 0, "hits": 0, "registered": 0, "evicted": 0}
+        # swap space
+        self.host_free: deque[int] = deque()
+        self.host_blocks = 0
+        self.swapped: dict[int, list[int]] = {}          # seq -> host blocks in table order
 
     def _take_front(self) -> int:
         b = self.free_blocks.popleft()
@@ -384,8 +400,8 @@ class BlockManagerModel:
 
     # -- [P1] section 3.2 -------------------------------------------------
     def allocate(self, seq_id: int, num_tokens: int) -> None:
-        if num_tokens < 0:
-            raise OracleInvalid("negative token count")
+        if num_tokens < 0 or seq_id in self.swapped:
+            raise OracleInvalid("negative token count or swapped sequence")
         table = self.allocated.get(seq_id, [])
         cur_len = self.lens.get(seq_id, 0)
         already_used = len(table) * self.block_size
@@ -407,6 +423,8 @@ class BlockManagerModel:
     def free(self, seq_id: int) -> None:
         if seq_id not in self.allocated:
             raise OracleInvalid("unknown sequence")
+        for h in self.swapped.pop(seq_id, []):
+            self.host_free.append(h)
         for b in self.allocated[seq_id]:
             self.ref[b] -= 1
             if self.ref[b] == 0:
@@ -428,8 +446,8 @@ class BlockManagerModel:
 
         Returns ``(slot, cow)`` where ``cow`` is ``None`` or ``(src, dst)``.
         """
-        if seq_id not in self.allocated:
-            raise OracleInvalid("unknown sequence")
+        if seq_id not in self.allocated or seq_id in self.swapped:
+            raise OracleInvalid("unknown or swapped sequence")
         if self._blocks_needed_for_append(seq_id, lambda b: self.ref[b]) > len(self.free_blocks):
             raise OracleOOM("no free block")
         self._untrack(seq_id)
@@ -467,8 +485,8 @@ class BlockManagerModel:
         if len(set(seq_ids)) != len(seq_ids):
             raise OracleInvalid("duplicate sequence in batch")
         for s in seq_ids:
-            if s not in self.allocated:
-                raise OracleInvalid("unknown sequence")
+            if s not in self.allocated or s in self.swapped:
+                raise OracleInvalid("unknown or swapped sequence")
         # count the blocks the whole batch takes, with the counts it changes
         delta: dict[int, int] = {}
         need = 0
@@ -552,8 +570,8 @@ class BlockManagerModel:
     def append_token(self, seq_id: int, token: int):
         """:meth:`append_slot` that also records the token id; returns
         ``(slot, cow)``."""
-        if seq_id not in self.allocated:
-            raise OracleInvalid("unknown sequence")
+        if seq_id not in self.allocated or seq_id in self.swapped:
+            raise OracleInvalid("unknown or swapped sequence")
         if self._blocks_needed_for_append(seq_id, lambda b: self.ref[b]) > len(self.free_blocks):
             raise OracleOOM("no free block")
         return self._append_token_unchecked(seq_id, int(token))
@@ -570,6 +588,53 @@ class BlockManagerModel:
                 self.pending[seq_id] = []
         return slot, cow
 
+    # -- swapping ([P1] section 3.2, [P2] section 4) -------------------------
+    def set_swap_pool(self, num_host_blocks: int) -> None:
+        if self.host_blocks or num_host_blocks < 0:
+            raise OracleInvalid("swap pool already set")
+        self.host_blocks = num_host_blocks
+        self.host_free = deque(range(num_host_blocks))
+
+    def swap_out(self, seq_id: int):
+        """Moves a sequence out of device memory ([P1] section 3.2: allocation
+        that finds too few free blocks needs swap or preemption; [P2] section
+        4: with swap space the KV cache goes to CPU memory).  Reading: the unit
+        is one sequence; every block of its table, in order, gets a host block
+        from the front of the host free list (all or nothing); each device
+        block's count drops by one and blocks reaching zero go to the back of
+        the device free list.  Returns the copies ``[(device, host)]`` to make
+        before the device blocks are reused."""
+        if seq_id not in self.allocated or seq_id in self.swapped:
+            raise OracleInvalid("unknown or swapped sequence")
+        table = self.allocated[seq_id]
+        if len(table) > len(self.host_free):
+            raise OracleOOM("swap space full")
+        hosts = [self.host_free.popleft() for _ in table]
+        for b in table:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free_blocks.append(b)
+        self.swapped[seq_id] = hosts
+        self.allocated[seq_id] = []
+        return list(zip(table, hosts))
+
+    def swap_in(self, seq_id: int):
+        """Brings a swapped sequence back: one block from the front of the
+        device free list per host block (all or nothing), host blocks return
+        to the back of the host free list in table order.  Returns the copies
+        ``[(host, device)]``; the sequence's blocks are private afterwards."""
+        if seq_id not in self.swapped:
+            raise OracleInvalid("sequence is not swapped out")
+        hosts = self.swapped[seq_id]
+        if len(hosts) > len(self.free_blocks):
+            raise OracleOOM("no device blocks to swap in")
+        table = [self._take_front() for _ in hosts]
+        for h in hosts:
+            self.host_free.append(h)
+        del self.swapped[seq_id]
+        self.allocated[seq_id] = table
+        return list(zip(hosts, table))
+
     def prefix_stats(self) -> dict:
         d = dict(self.pstats)
         d["entries"] = len(self.cache)
@@ -579,7 +644,7 @@ class BlockManagerModel:
     def fork(self, parent: int, child: int) -> None:
         """[P4] section 3.3 / [P3] section 3.3: the child shares the parent's
         blocks; only the table is copied."""
-        if parent not in self.allocated or child in self.allocated:
+        if parent not in self.allocated or child in self.allocated or parent in self.swapped:
             raise OracleInvalid("bad fork")
         table = list(self.allocated[parent])
         for b in table:
@@ -603,6 +668,8 @@ class BlockManagerModel:
         tbl = np.full((len(seq_ids), max_blocks), -1, dtype=np.int32)
         lens = np.zeros(len(seq_ids), dtype=np.int32)
         for r, s in enumerate(seq_ids):
+            if s in self.swapped:
+                raise OracleInvalid("swapped sequence")
             t = self.allocated[s]
             if len(t) > max_blocks:
                 raise OracleInvalid("table wider than max_blocks")

@@ -34,6 +34,11 @@ class AllocStats(ctypes.Structure):
                 ("num_tokens", ctypes.c_int64)]
 
 
+class SwapStats(ctypes.Structure):
+    _fields_ = [("host_blocks", ctypes.c_int32), ("host_free", ctypes.c_int32),
+                ("swapped_seqs", ctypes.c_int32)]
+
+
 class PrefixStats(ctypes.Structure):
     _fields_ = [("lookups", ctypes.c_int64), ("hits", ctypes.c_int64),
                 ("registered", ctypes.c_int64), ("evicted", ctypes.c_int64),
@@ -60,6 +65,12 @@ SIGNATURES = {
     "pa_append_token": (_ST, [_P, _I64, _I32, _P, _P, _P]),
     "pa_append_batch_tokens": (_ST, [_P, _P, _P, _I32, _P, _P, _P]),
     "pa_prefix_stats_get": (_ST, [_P, ctypes.POINTER(PrefixStats)]),
+    "pa_alloc_set_swap_pool": (_ST, [_P, _I32]),
+    "pa_swap_out": (_ST, [_P, _I64, _P, _I32, _P]),
+    "pa_swap_in": (_ST, [_P, _I64, _P, _I32, _P]),
+    "pa_swap_stats_get": (_ST, [_P, ctypes.POINTER(SwapStats)]),
+    "pa_host_free_list": (_ST, [_P, _P, _I32, _P]),
+    "pa_swap_blocks": (_ST, [_P, _P, _I32, _P, _I32, _I64, _I32, _I32, _P]),
     "pa_reshape_and_cache": (_ST, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _ST, _P]),
     "pa_reshape_and_cache_fp8": (_ST, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                        _ST, _P]),
@@ -183,6 +194,33 @@ def pa_copy_blocks(k_caches, v_caches, pairs, stream=None) -> None:
     block_bytes = ref[0].numel() * ref.element_size()
     _check(load().pa_copy_blocks(kc, vc, L, _dev(pairs, torch.int32), P, block_bytes,
                                  int(ref.shape[0]), _stream_ptr(stream)), "pa_copy_blocks")
+
+
+def pa_swap_blocks(src_pools, dst_pools, pairs, stream=None) -> None:
+    """Copies block ``pairs[p][0]`` of ``src_pools[l]`` onto block ``pairs[p][1]`` of
+    ``dst_pools[l]`` for every pool pair; pools are CUDA tensors or pinned host
+    tensors ``[blocks, ...]`` of the same block size; ``pairs`` is an int32
+    ``[P, 2]`` tensor on the device or in pinned host memory."""
+    import torch
+    L = len(src_pools)
+    if len(dst_pools) != L:
+        raise ValueError("one destination per source pool")
+
+    def ptr(t):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("contiguous CUDA or pinned host tensor expected")
+        return t.data_ptr()
+    sp = (ctypes.c_void_p * max(L, 1))(*[ptr(t) for t in src_pools])
+    dp = (ctypes.c_void_p * max(L, 1))(*[ptr(t) for t in dst_pools])
+    ref_s, ref_d = src_pools[0], dst_pools[0]
+    block_bytes = ref_s[0].numel() * ref_s.element_size()
+    if ref_d[0].numel() * ref_d.element_size() != block_bytes:
+        raise ValueError("source and destination blocks differ in size")
+    if pairs.dtype != torch.int32:
+        raise TypeError("int32 pairs expected")
+    _check(load().pa_swap_blocks(sp, dp, L, ptr(pairs), int(pairs.shape[0]), block_bytes,
+                                 int(ref_s.shape[0]), int(ref_d.shape[0]), _stream_ptr(stream)),
+           "pa_swap_blocks")
 
 
 def pa_decode_workspace_size(B: int, H: int, d: int) -> int:
@@ -337,6 +375,39 @@ class Allocator:
         _check(self._lib.pa_append_token(self._h, seq_id, int(token), ctypes.byref(slot),
                                          ctypes.byref(src), ctypes.byref(dst)), "pa_append_token")
         return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def set_swap_pool(self, num_host_blocks: int) -> None:
+        _check(self._lib.pa_alloc_set_swap_pool(self._h, num_host_blocks),
+               "pa_alloc_set_swap_pool")
+        self.host_blocks = num_host_blocks
+
+    def _swap(self, fn, name, seq_id):
+        cap = max(self.num_blocks, getattr(self, "host_blocks", 0), 1)
+        out = np.empty((cap, 2), np.int32)
+        n = ctypes.c_int32()
+        _check(fn(self._h, seq_id, _np_ptr(out), cap, ctypes.byref(n)), name)
+        return out[: n.value]
+
+    def swap_out(self, seq_id: int) -> np.ndarray:
+        """``pa_swap_out``: the copies ``[n, 2]`` {device block, host block}."""
+        return self._swap(self._lib.pa_swap_out, "pa_swap_out", seq_id)
+
+    def swap_in(self, seq_id: int) -> np.ndarray:
+        """``pa_swap_in``: the copies ``[n, 2]`` {host block, device block}."""
+        return self._swap(self._lib.pa_swap_in, "pa_swap_in", seq_id)
+
+    def swap_stats(self) -> dict:
+        s = SwapStats()
+        _check(self._lib.pa_swap_stats_get(self._h, ctypes.byref(s)), "pa_swap_stats_get")
+        return {f: getattr(s, f) for f, _ in SwapStats._fields_}
+
+    def host_free_list(self):
+        cap = max(getattr(self, "host_blocks", 0), 1)
+        out = np.empty(cap, np.int32)
+        n = ctypes.c_int32()
+        _check(self._lib.pa_host_free_list(self._h, _np_ptr(out), cap, ctypes.byref(n)),
+               "pa_host_free_list")
+        return out[: n.value].tolist()
 
     def prefix_stats(self) -> dict:
         s = PrefixStats()

@@ -22,9 +22,18 @@
 // whole prefix and a hit needs a token-exact, block-aligned prefix.  A prompt reuses cached blocks up to its first miss; a
 // freed block keeps its entry while it waits on the free list (a hit takes it
 // back off the list) and loses it when the free list hands it out again.
+//
+// Swap ("LLM推理优化：vLLM PagedAttention深度解析与工程实践", section 3.2: too few
+// free blocks calls for swap or preemption; "vLLM推理加速深度解析：从PagedAttention
+// 原理到生产部署实战", section 4: with swap space the KV cache moves to CPU
+// memory): a swapped-out sequence's blocks, in table order, take host blocks
+// from the front of a host free list and drop their device counts; swap-in
+// takes fresh device blocks from the front of the device free list and returns
+// the host blocks to the back of the host list.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <deque>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
@@ -42,6 +51,8 @@ struct Sequence {
     bool tracked = false;
     std::vector<int32_t> pending;  // token ids of the partial last block
     uint64_t chain = 0;            // entry id of the last full block's content
+    bool swapped = false;          // blocks live in the host pool (`host`)
+    std::vector<int32_t> host;
 };
 
 struct Key {
@@ -86,6 +97,9 @@ struct pa_allocator {
     std::vector<const Key*> block_key;  // key of the entry a block holds, or null
     uint64_t next_entry = 1;
     pa_prefix_stats pstats{};
+    std::deque<int32_t> host_free;  // swap space
+    int32_t host_blocks = 0;
+    int32_t swapped_seqs = 0;
 
     int64_t capacity(const Sequence& s) const { return (int64_t)s.table.size() * block_size; }
 
@@ -218,6 +232,7 @@ PA_API pa_status pa_alloc(pa_allocator* a, int64_t seq_id, int32_t num_tokens) {
     if (!a || num_tokens < 0) return PA_ERR_INVALID;
     auto it = a->seqs.find(seq_id);
     const bool fresh = (it == a->seqs.end());
+    if (!fresh && it->second.swapped) return PA_ERR_INVALID;
     Sequence empty;
     const Sequence& cur = fresh ? empty : it->second;
     const int64_t held = a->capacity(cur);
@@ -239,7 +254,7 @@ PA_API pa_status pa_append_slot(pa_allocator* a, int64_t seq_id, int64_t* slot_o
     if (!a || !slot_out) return PA_ERR_INVALID;
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
-    if (it->second.length == INT32_MAX) return PA_ERR_INVALID;
+    if (it->second.length == INT32_MAX || it->second.swapped) return PA_ERR_INVALID;
     if (a->append_need(it->second, [&](int32_t b) { return a->ref[b]; }) > a->nfree)
         return PA_ERR_OOM;
     pa_allocator::untrack(it->second);  // token id unknown
@@ -265,7 +280,7 @@ pa_status append_batch(pa_allocator* a, const int64_t* seq_ids, const int32_t* t
         if (!seen.insert(seq_ids[i]).second) return PA_ERR_INVALID;
         auto it = a->seqs.find(seq_ids[i]);
         if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
-        if (it->second.length == INT32_MAX) return PA_ERR_INVALID;
+        if (it->second.length == INT32_MAX || it->second.swapped) return PA_ERR_INVALID;
         batch[(size_t)i] = &it->second;
     }
     // Count the blocks the batch takes, following the counts it lowers as
@@ -364,7 +379,7 @@ PA_API pa_status pa_append_token(pa_allocator* a, int64_t seq_id, int32_t token,
     if (!a || !slot_out) return PA_ERR_INVALID;
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
-    if (it->second.length == INT32_MAX) return PA_ERR_INVALID;
+    if (it->second.length == INT32_MAX || it->second.swapped) return PA_ERR_INVALID;
     if (a->append_need(it->second, [&](int32_t b) { return a->ref[b]; }) > a->nfree)
         return PA_ERR_OOM;
     int32_t src, dst;
@@ -389,7 +404,7 @@ PA_API pa_status pa_fork(pa_allocator* a, int64_t parent, int64_t child) {
     if (!a) return PA_ERR_INVALID;
     auto p = a->seqs.find(parent);
     if (p == a->seqs.end()) return PA_ERR_NOT_FOUND;
-    if (a->seqs.count(child)) return PA_ERR_INVALID;
+    if (a->seqs.count(child) || p->second.swapped) return PA_ERR_INVALID;
     Sequence copy = p->second;
     for (int32_t b : copy.table) a->ref[b] += 1;
     a->seqs.emplace(child, std::move(copy));
@@ -400,6 +415,8 @@ PA_API pa_status pa_free(pa_allocator* a, int64_t seq_id) {
     if (!a) return PA_ERR_INVALID;
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    for (int32_t h : it->second.host) a->host_free.push_back(h);
+    if (it->second.swapped) a->swapped_seqs -= 1;
     for (int32_t b : it->second.table)
         if (--a->ref[b] == 0) a->free_push_back(b);
     a->seqs.erase(it);
@@ -414,7 +431,8 @@ PA_API pa_status pa_export(const pa_allocator* a, const int64_t* seq_ids, int32_
     for (int32_t i = 0; i < B; ++i) {
         auto it = a->seqs.find(seq_ids[i]);
         if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
-        if ((int64_t)it->second.table.size() > max_blocks) return PA_ERR_INVALID;
+        if ((int64_t)it->second.table.size() > max_blocks || it->second.swapped)
+            return PA_ERR_INVALID;
     }
     for (int32_t i = 0; i < B; ++i) {
         const Sequence& s = a->seqs.find(seq_ids[i])->second;
@@ -433,7 +451,7 @@ PA_API pa_status pa_seq_slots(const pa_allocator* a, int64_t seq_id, int32_t sta
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
     const Sequence& s = it->second;
-    if ((int64_t)start + count > a->capacity(s)) return PA_ERR_INVALID;
+    if ((int64_t)start + count > a->capacity(s) || s.swapped) return PA_ERR_INVALID;
     for (int32_t t = 0; t < count; ++t) {
         const int32_t pos = start + t;
         slots[t] = (int64_t)s.table[pos / a->block_size] * a->block_size + pos % a->block_size;
@@ -463,6 +481,80 @@ PA_API pa_status pa_free_list(const pa_allocator* a, int32_t* out, int32_t cap, 
     if (cap < *n) return PA_ERR_INVALID;
     int32_t i = 0;
     for (int32_t b = a->fhead; b >= 0; b = a->fnext[b]) out[i++] = b;
+    return PA_OK;
+}
+
+PA_API pa_status pa_alloc_set_swap_pool(pa_allocator* a, int32_t num_host_blocks) {
+    if (!a || a->host_blocks || num_host_blocks < 0) return PA_ERR_INVALID;
+    a->host_blocks = num_host_blocks;
+    a->host_free.clear();
+    for (int32_t h = 0; h < num_host_blocks; ++h) a->host_free.push_back(h);
+    return PA_OK;
+}
+
+PA_API pa_status pa_swap_out(pa_allocator* a, int64_t seq_id, int32_t* pairs, int32_t cap,
+                             int32_t* n) {
+    if (!a || !n || cap < 0) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    Sequence& s = it->second;
+    const int32_t nb = (int32_t)s.table.size();
+    if (s.swapped || cap < nb || (nb > 0 && !pairs)) return PA_ERR_INVALID;
+    if (nb > (int32_t)a->host_free.size()) return PA_ERR_OOM;
+    for (int32_t j = 0; j < nb; ++j) {
+        const int32_t h = a->host_free.front();
+        a->host_free.pop_front();
+        pairs[2 * j] = s.table[(size_t)j];
+        pairs[2 * j + 1] = h;
+        s.host.push_back(h);
+    }
+    for (int32_t b : s.table)
+        if (--a->ref[b] == 0) a->free_push_back(b);
+    s.table.clear();
+    s.swapped = true;
+    a->swapped_seqs += 1;
+    *n = nb;
+    return PA_OK;
+}
+
+PA_API pa_status pa_swap_in(pa_allocator* a, int64_t seq_id, int32_t* pairs, int32_t cap,
+                            int32_t* n) {
+    if (!a || !n || cap < 0) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+    Sequence& s = it->second;
+    const int32_t nb = (int32_t)s.host.size();
+    if (!s.swapped || cap < nb || (nb > 0 && !pairs)) return PA_ERR_INVALID;
+    if (nb > a->nfree) return PA_ERR_OOM;
+    for (int32_t j = 0; j < nb; ++j) {
+        const int32_t b = a->take_front();
+        pairs[2 * j] = s.host[(size_t)j];
+        pairs[2 * j + 1] = b;
+        s.table.push_back(b);
+    }
+    for (int32_t h : s.host) a->host_free.push_back(h);
+    s.host.clear();
+    s.swapped = false;
+    a->swapped_seqs -= 1;
+    *n = nb;
+    return PA_OK;
+}
+
+PA_API pa_status pa_swap_stats_get(const pa_allocator* a, pa_swap_stats* out) {
+    if (!a || !out) return PA_ERR_INVALID;
+    out->host_blocks = a->host_blocks;
+    out->host_free = (int32_t)a->host_free.size();
+    out->swapped_seqs = a->swapped_seqs;
+    return PA_OK;
+}
+
+PA_API pa_status pa_host_free_list(const pa_allocator* a, int32_t* out, int32_t cap,
+                                   int32_t* n) {
+    if (!a || !n || cap < 0) return PA_ERR_INVALID;
+    *n = (int32_t)a->host_free.size();
+    if (cap < *n) return PA_ERR_INVALID;
+    int32_t i = 0;
+    for (int32_t h : a->host_free) out[i++] = h;
     return PA_OK;
 }
 

@@ -135,6 +135,41 @@ copy_blocks_kernel(const __grid_constant__ LayerPtrs layers, const int32_t* __re
     }
 }
 
+// Block copies between two pools (device <-> pinned host for swapping): for
+// every pool pair and every (src, dst) pair, block dst of the destination pool
+// becomes a copy of block src of the source pool.  blockIdx.x = pair,
+// blockIdx.y = pool pair; each thread moves four 16-byte vectors per step
+// (loads first, then stores), streaming hints on both sides.
+constexpr int kMaxSwapPools = 64;
+
+struct SwapPools {
+    const uint4* src[kMaxSwapPools];
+    uint4* dst[kMaxSwapPools];
+};
+
+__global__ void __launch_bounds__(kThreads)
+swap_blocks_kernel(const __grid_constant__ SwapPools pools, const int32_t* __restrict__ pairs,
+                   int64_t vecs_per_block, int32_t src_blocks, int32_t dst_blocks,
+                   unsigned int* __restrict__ err) {
+    const int32_t s = pairs[2 * blockIdx.x];
+    const int32_t d = pairs[2 * blockIdx.x + 1];
+    if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) pa::raise_error(err, PA_DEVERR_PAIR);
+        return;
+    }
+    const uint4* from = pools.src[blockIdx.y] + (int64_t)s * vecs_per_block;
+    uint4* to = pools.dst[blockIdx.y] + (int64_t)d * vecs_per_block;
+    int64_t i = threadIdx.x;
+    for (; i + 3 * kThreads < vecs_per_block; i += 4 * kThreads) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(from + i + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) __stcs(to + i + u * kThreads, v[u]);
+    }
+    for (; i < vecs_per_block; i += kThreads) __stcs(to + i, __ldcs(from + i));
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -199,6 +234,36 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
             Hkv, block_size, static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache),
             k_scale, v_scale, slots, err);
     return pa::cuda_status(cudaGetLastError());
+}
+
+PA_API pa_status pa_swap_blocks(const void* const* src_pools, void* const* dst_pools,
+                                int32_t num_pools, const int32_t* pairs, int32_t num_pairs,
+                                int64_t block_bytes, int32_t src_blocks, int32_t dst_blocks,
+                                void* stream) {
+    if (num_pools < 0 || num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 != 0 ||
+        src_blocks < 0 || dst_blocks < 0)
+        return PA_ERR_INVALID;
+    if (num_pools == 0 || num_pairs == 0) return PA_OK;
+    if (!src_pools || !dst_pools || !pairs) return PA_ERR_INVALID;
+    if (num_pairs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+    unsigned int* err = pa::device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    for (int32_t l0 = 0; l0 < num_pools; l0 += kMaxSwapPools) {
+        const int32_t nl = num_pools - l0 < kMaxSwapPools ? num_pools - l0 : kMaxSwapPools;
+        SwapPools sp{};
+        for (int32_t l = 0; l < nl; ++l) {
+            const void* s = src_pools[l0 + l];
+            void* d = dst_pools[l0 + l];
+            if (!s || !d || !aligned16(s) || !aligned16(d)) return PA_ERR_INVALID;
+            sp.src[l] = static_cast<const uint4*>(s);
+            sp.dst[l] = static_cast<uint4*>(d);
+        }
+        swap_blocks_kernel<<<dim3((unsigned)num_pairs, (unsigned)nl), kThreads, 0,
+                             static_cast<cudaStream_t>(stream)>>>(sp, pairs, block_bytes / 16,
+                                                                   src_blocks, dst_blocks, err);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
 }
 
 PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
