@@ -26,6 +26,8 @@ Sources, cited by page title and section:
 Contents:
 
 * :func:`decode` -- the fp64 attention over a block table (C, ``pa_oracle.c``).
+* :func:`multi_query` -- several causal query tokens per sequence over the
+  same table (chunked prefill / speculative verification, [P3] section 5).
 * :func:`reshape_and_cache` -- the KV append: a plain per-token scatter.
 * :func:`copy_blocks` -- the copy-on-write block copy: plain slice copies.
 * :class:`BlockManagerModel` -- the allocator, restated from [P1] section 3.2
@@ -93,6 +95,9 @@ def _load():
         lib.pa_oracle_to_double.argtypes = [P, i64, i32, P]
         lib.pa_oracle_e4m3_to_double.restype = ctypes.c_int
         lib.pa_oracle_e4m3_to_double.argtypes = [P, i64, P]
+        lib.pa_oracle_multi_query.restype = ctypes.c_int
+        lib.pa_oracle_multi_query.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                              i64, f64, i32, P, i32]
         lib.pa_oracle_decode_fp8.restype = ctypes.c_int
         lib.pa_oracle_decode_fp8.argtypes = [P, i32, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                              i64, f64, P]
@@ -109,6 +114,33 @@ def _u16(a) -> np.ndarray:
 
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, scale: float,
+                dtype: int, num_threads: int = 1) -> np.ndarray:
+    """fp64 attention of several query tokens per sequence over the paged cache
+    (chunked prefill / speculative verification, [P3] section 5).  Sequence
+    i's queries are rows ``q_start[i] .. q_start[i+1]-1`` of ``q [T, H, d]``
+    (uint16) and are its LAST ``q_start[i+1] - q_start[i]`` cached tokens;
+    query r attends causally to tokens ``0 .. context_lens[i] - qlen + r``
+    (a reading: the pages give no formula).  Returns ``out[T, H, d]`` float64.
+    """
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    tbl = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    T, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    B = lens.shape[0]
+    if qs.shape[0] != B + 1 or qs[-1] != T:
+        raise ValueError("q_start must have B + 1 entries ending at T")
+    out = np.zeros((T, H, d), dtype=np.float64)
+    rc = _load().pa_oracle_multi_query(_ptr(q), _ptr(qs), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(tbl), tbl.shape[1], _ptr(lens), B, H, Hkv, d, bs, N,
+                                       float(scale), int(dtype), _ptr(out), int(num_threads))
+    if rc:
+        raise ValueError("pa_oracle_multi_query failed (%d)" % rc)
+    return out
 
 
 def to_double(bits, dtype: int) -> np.ndarray:

@@ -80,18 +80,15 @@ typedef struct {
     int status;
 } orc_job;
 
-/* One (sequence, query head) output row. */
-static int orc_row(const orc_job* J, int32_t i, int32_t h, double* s /* [n] scratch */) {
-    const int32_t G = J->H / J->Hkv;
-    const int32_t g = h / G;
-    const int32_t n = J->lens[i];
+/* One query row (q at element offset qoff) of sequence i against its first n
+ * cached tokens of KV head g; the result goes to o[0..d). */
+static int orc_attend(const orc_job* J, int32_t i, int32_t g, int64_t qoff, int32_t n, double* o,
+                      double* s /* [n] scratch */) {
     const int32_t d = J->d;
-    double* o = J->out + ((int64_t)i * J->H + h) * d;
     for (int32_t k = 0; k < d; ++k) o[k] = 0.0;
     if (n == 0) return ORC_OK;
 
     /* logits */
-    const int64_t qoff = ((int64_t)i * J->H + h) * d;
     for (int32_t j = 0; j < n; ++j) {
         int32_t lb = j / J->bs;
         if (lb >= J->max_blocks) return ORC_ERR_TABLE;
@@ -120,6 +117,13 @@ static int orc_row(const orc_job* J, int32_t i, int32_t h, double* s /* [n] scra
         for (int32_t k = 0; k < d; ++k) o[k] += w * orc_elem(J->v, row + k, J->dtype);
     }
     return ORC_OK;
+}
+
+/* One (sequence, query head) output row of the decode. */
+static int orc_row(const orc_job* J, int32_t i, int32_t h, double* s /* [n] scratch */) {
+    const int32_t G = J->H / J->Hkv;
+    const int64_t off = ((int64_t)i * J->H + h) * J->d;
+    return orc_attend(J, i, h / G, off, J->lens[i], J->out + off, s);
 }
 
 static void* orc_worker(void* arg) {
@@ -321,4 +325,109 @@ int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_co
     }
     free(s);
     return ORC_OK;
+}
+
+/*
+ * Multi-token query over the paged cache (chunked prefill / speculative
+ * verification; "vLLM 深度拆解：当大模型推理学会「分页注意力」", section 5: a long
+ * prompt's prefill split into chunks, and a draft's N tokens verified by one
+ * forward pass).  Reading: sequence i's queries are its LAST qlen_i cached
+ * tokens, rows q_start[i] .. q_start[i+1]-1 of q; query r (0-based) attends to
+ * the cached tokens 0 .. n_i - qlen_i + r (causal), n_i = context_lens[i].
+ * Each output row is the decode's attention over that prefix.
+ *
+ * q       [T, H, d], T = q_start[B]      out  [T, H, d] double
+ * Rows are split over threads (each row computed by one thread).
+ */
+typedef struct {
+    orc_job base;
+    const int32_t* q_start;
+    int32_t t_begin, t_end;
+} orc_mq_job;
+
+static void* orc_mq_worker(void* arg) {
+    orc_mq_job* M = (orc_mq_job*)arg;
+    const orc_job* J = &M->base;
+    int32_t nmax = 1;
+    for (int32_t i = 0; i < J->B; ++i)
+        if (J->lens[i] > nmax) nmax = J->lens[i];
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    if (!s) {
+        M->base.status = ORC_ERR_ARG;
+        return NULL;
+    }
+    M->base.status = ORC_OK;
+    const int32_t G = J->H / J->Hkv;
+    int32_t i = 0;
+    for (int32_t t = M->t_begin; t < M->t_end && M->base.status == ORC_OK; ++t) {
+        while (M->q_start[i + 1] <= t) ++i;
+        const int32_t qlen = M->q_start[i + 1] - M->q_start[i];
+        const int32_t r = t - M->q_start[i];
+        const int32_t n = J->lens[i] - qlen + r + 1;
+        for (int32_t h = 0; h < J->H && M->base.status == ORC_OK; ++h) {
+            const int64_t off = ((int64_t)t * J->H + h) * J->d;
+            M->base.status = orc_attend(J, i, h / G, off, n, J->out + off, s);
+        }
+    }
+    free(s);
+    return NULL;
+}
+
+int pa_oracle_multi_query(const uint16_t* q, const int32_t* q_start, const uint16_t* k_cache,
+                          const uint16_t* v_cache, const int32_t* block_tables,
+                          int32_t max_blocks, const int32_t* context_lens, int32_t B, int32_t H,
+                          int32_t Hkv, int32_t d, int32_t block_size, int64_t num_blocks,
+                          double scale, int32_t dtype, double* out, int32_t num_threads) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || d <= 0 || block_size <= 0 ||
+        max_blocks < 0 || num_blocks < 0 || (dtype != 0 && dtype != 1) || !q_start)
+        return ORC_ERR_ARG;
+    if (q_start[0] != 0) return ORC_ERR_ARG;
+    for (int32_t i = 0; i < B; ++i) {
+        const int32_t qlen = q_start[i + 1] - q_start[i];
+        if (qlen < 0 || qlen > context_lens[i]) return ORC_ERR_ARG;
+    }
+    const int32_t T = q_start[B];
+    if (T == 0) return ORC_OK;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > T) num_threads = T;
+    orc_mq_job* jobs = (orc_mq_job*)calloc((size_t)num_threads, sizeof(orc_mq_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)num_threads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return ORC_ERR_ARG;
+    }
+    for (int t = 0; t < num_threads; ++t) {
+        orc_mq_job* M = &jobs[t];
+        M->base.q = q;
+        M->base.k = k_cache;
+        M->base.v = v_cache;
+        M->base.tbl = block_tables;
+        M->base.lens = context_lens;
+        M->base.max_blocks = max_blocks;
+        M->base.B = B;
+        M->base.H = H;
+        M->base.Hkv = Hkv;
+        M->base.d = d;
+        M->base.bs = block_size;
+        M->base.dtype = dtype;
+        M->base.num_blocks = num_blocks;
+        M->base.scale = scale;
+        M->base.out = out;
+        M->q_start = q_start;
+        M->t_begin = (int32_t)((int64_t)T * t / num_threads);
+        M->t_end = (int32_t)((int64_t)T * (t + 1) / num_threads);
+    }
+    if (num_threads == 1) {
+        orc_mq_worker(&jobs[0]);
+    } else {
+        for (int t = 0; t < num_threads; ++t) pthread_create(&th[t], NULL, orc_mq_worker, &jobs[t]);
+        for (int t = 0; t < num_threads; ++t) pthread_join(th[t], NULL);
+    }
+    int status = ORC_OK;
+    for (int t = 0; t < num_threads; ++t)
+        if (jobs[t].base.status != ORC_OK) status = jobs[t].base.status;
+    free(jobs);
+    free(th);
+    return status;
 }
