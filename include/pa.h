@@ -359,6 +359,31 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
                            int32_t num_blocks, float scale, pa_dtype dtype, void* out,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* Several query tokens per sequence over the paged cache: chunked prefill and
+ * speculative verification ([P3] section 5: a long prompt's prefill is cut
+ * into chunks that run between decode steps; a draft model's N tokens are
+ * verified by one forward pass).  Sequence i's queries are its LAST
+ * qlen_i = q_start[i+1] - q_start[i] cached tokens (their K/V already written
+ * by pa_reshape_and_cache); with n = context_lens[i], query r (0-based) of
+ * sequence i and query head h attend causally to tokens 0 .. n - qlen_i + r:
+ *   out[q_start[i] + r][h] = sum_j softmax_j(scale * q[q_start[i] + r][h] . K_j) V_j
+ * with K_j, V_j as in pa_decode (KV head h / G), fp32 accumulation, rounded
+ * once to the output dtype.  qlen_i = 1 is the decode of one token; qlen_i = n
+ * is the prefill of a whole prompt.  No workspace: no context is split.
+ *   q            (device) [T][H][d], T = q_start[B]; out (device) [T][H][d]
+ *   q_start      (device) [B + 1] int32, q_start[0] = 0, non-decreasing
+ *   max_q_len    (host) an upper bound of every qlen_i
+ *   other arguments as in pa_decode
+ * qlen_i > n (or < 0) skips sequence i and sets PA_DEVERR_CONTEXT; a context
+ * longer than its table row is cut to it and sets PA_DEVERR_TABLE_WIDTH; a
+ * table entry outside the pool reads zeros and sets PA_DEVERR_BLOCK_ID. */
+PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks, const int32_t* context_lens,
+                                int32_t max_q_len, int32_t B, int32_t H, int32_t Hkv, int32_t d,
+                                int32_t block_size, int32_t num_blocks, float scale,
+                                pa_dtype dtype, void* out, void* stream);
+
 /* pa_decode over an FP8 cache written by pa_reshape_and_cache_fp8 ([P4]
  * section 4.3).  Computes what pa_decode computes with
  *   K_j = k_scale[b][h / G][j % bs] * E4M3(k_cache[b][j % bs][h / G][:]),

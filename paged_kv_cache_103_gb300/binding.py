@@ -79,6 +79,8 @@ SIGNATURES = {
     "pa_decode_workspace_init": (_ST, [_P, _SZ, _P]),
     "pa_decode": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                         _F32, _ST, _P, _P, _SZ, _P]),
+    "pa_multi_query": (_ST, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                             _I32, ctypes.c_float, _ST, _P, _P]),
     "pa_decode_fp8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -246,6 +248,23 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
                             bs, N, float(scale), _dtype_code(q), _dev(out), _dev(workspace),
                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "pa_decode")
+
+
+def pa_multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, max_q_len: int,
+                   scale: float, out, stream=None) -> None:
+    """``q/out [T, H, d]`` (the last ``q_start[i+1]-q_start[i]`` tokens of sequence i,
+    concatenated), ``q_start [B+1]`` int32, caches ``[N, bs, Hkv, d]``,
+    ``block_tables [B, max_blocks]`` and ``context_lens [B]`` int32."""
+    import torch
+    T, H, d = q.shape
+    N, bs, Hkv, _ = k_cache.shape
+    B = int(context_lens.shape[0])
+    _check(load().pa_multi_query(_dev(q), _dev(q_start, torch.int32), _dev(k_cache),
+                                 _dev(v_cache), _dev(block_tables, torch.int32),
+                                 int(block_tables.shape[1]), _dev(context_lens, torch.int32),
+                                 int(max_q_len), B, H, Hkv, d, bs, N, float(scale),
+                                 _dtype_code(q), _dev(out), _stream_ptr(stream)),
+           "pa_multi_query")
 
 
 def pa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,

@@ -197,6 +197,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// For bf16: the rounding residuals of a pack2<true>(lo, hi) register, packed
+// again (P = hi part + this part carries about 16 significant bits).
+__device__ __forceinline__ uint32_t bf16x2_residual(uint32_t packed, float lo, float hi) {
+    return pack2<true>(lo - __uint_as_float(packed << 16), hi - __uint_as_float(packed & 0xFFFF0000u));
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

@@ -849,7 +849,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         }
                 }
                 // P^T as MMA B fragments: exp2, pack to 16 bits, transpose 8x8 tiles.
+                // A bf16 P keeps 8 bits; its rounding residual (pbl, a second
+                // B operand) restores about 16, so a short context whose V terms
+                // cancel stays within the tolerance (f16 and FP8 use f16 P).
+                constexpr bool kPbf16 = kBF16 && !kFp8;
                 uint32_t pb[kKeyTiles][NT][2];
+                uint32_t pbl[kKeyTiles][NT][2];
 #pragma unroll
                 for (int mt = 0; mt < kKeyTiles; ++mt)
 #pragma unroll
@@ -868,9 +873,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             e4[2] *= vmul[mt][1];
                             e4[3] *= vmul[mt][1];
                         }
-                        constexpr bool kPbf16 = kBF16 && !kFp8;
-                        pb[mt][nt][0] = pa::movmatrix_trans(pa::pack2<kPbf16>(e4[0], e4[1]));
-                        pb[mt][nt][1] = pa::movmatrix_trans(pa::pack2<kPbf16>(e4[2], e4[3]));
+                        const uint32_t h01 = pa::pack2<kPbf16>(e4[0], e4[1]);
+                        const uint32_t h23 = pa::pack2<kPbf16>(e4[2], e4[3]);
+                        pb[mt][nt][0] = pa::movmatrix_trans(h01);
+                        pb[mt][nt][1] = pa::movmatrix_trans(h23);
+                        if constexpr (kPbf16) {
+                            pbl[mt][nt][0] =
+                                pa::movmatrix_trans(pa::bf16x2_residual(h01, e4[0], e4[1]));
+                            pbl[mt][nt][1] =
+                                pa::movmatrix_trans(pa::bf16x2_residual(h23, e4[2], e4[3]));
+                        }
                     }
 
                 // O^T += V^T P^T: head_dim in 16-row m-tiles, keys in 16-key steps.
@@ -929,8 +941,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                                            rows_shift),
                                           a[0], a[1], a[2], a[3]);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
+                        for (int nt = 0; nt < NT; ++nt) {
                             pa::mma_16816<kBF16>(o[mt][nt], a, pb[ks2][nt][0], pb[ks2][nt][1]);
+                            if constexpr (kPbf16)
+                                pa::mma_16816<kBF16>(o[mt][nt], a, pbl[ks2][nt][0],
+                                                     pbl[ks2][nt][1]);
+                        }
                     }
                 }
             }

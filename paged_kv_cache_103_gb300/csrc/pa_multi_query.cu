@@ -1,0 +1,589 @@
+// Several query tokens per sequence over the paged cache (pa_multi_query):
+// chunked prefill and speculative verification ("vLLM 深度拆解：当大模型推理学会
+// 「分页注意力」", section 5: a long prompt's prefill is cut into chunks that run
+// between decode steps, and a draft model's N tokens are verified by one
+// forward pass of the main model).  Sequence i's queries are its last qlen_i
+// cached tokens (rows q_start[i] .. q_start[i+1]-1 of q); query r attends to
+// cached tokens 0 .. n_i - qlen_i + r (causal), as the decode does to all n_i.
+//
+//  * Work items are (sequence, KV head, tile of 64 rows), a row being one
+//    (query token, query head of the KV head's group) pair in token-major
+//    order, so one K/V chunk serves the whole GQA group.  Persistent CTAs (two
+//    per SM) take items heaviest-first (the last tiles of each sequence see
+//    the most keys).
+//  * A producer warp streams 64-token K and V chunks of the item's context
+//    (only up to the tile's last causal key) through a shared-memory ring with
+//    the decode's 3-D TMA boxes; the table is read 32 entries at a time, the
+//    next window and the next item's first window one step ahead.
+//  * Four consumer warps own 16 rows each and run FlashAttention-style over
+//    the chunks: S = Q K^T and O += P V as m16n8k16 tensor-core MMAs (P stays
+//    in registers as the A operand), online softmax in base 2 with the per-row
+//    causal limit, normalisation once at the end.  V rows past the context are
+//    zeroed in shared memory before use (unwritten slots may hold NaN).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kRows = 64;           // query rows per work item (4 warps x 16)
+constexpr int kKv = 64;             // keys per pipeline stage
+constexpr int kWarps = 4;           // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kCtasPerSm = 2;
+constexpr int kMaxStages = 8;
+constexpr int kMaxBatch = 4096;
+constexpr uint32_t kSmemBudget = 113 * 1024;
+constexpr uint64_t kWaitLimitNs = 1ull << 30;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Params {
+    const uint16_t* q;
+    const int32_t* q_start;
+    uint16_t* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    unsigned int* err;
+    int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages;
+    float scale_log2;
+};
+
+struct Layout {
+    uint32_t stage_bytes, bars, prefix, total;
+};
+
+__host__ __device__ inline Layout make_layout(int D, int B, int stages) {
+    Layout L;
+    L.stage_bytes = 2u * kKv * D * 2;                      // K then V, 16-bit
+    L.bars = stages * L.stage_bytes;                       // full[], empty[]
+    L.prefix = L.bars + 2 * kMaxStages * 8;                // [B + 1] int32 item prefix
+    L.total = 1024 + L.prefix + (uint32_t)(B + 1) * 4 + 32 * 4;
+    return L;
+}
+
+__device__ __forceinline__ int32_t clamp_len(int32_t n, int32_t cap) {
+    return n < 0 ? 0 : (n > cap ? cap : n);
+}
+
+// Byte offset of (token t, 64-column half h, 16-byte column c) in a tensor's
+// chunk: [box][half][rows][128 B], TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t c,
+                                                uint32_t halves, uint32_t rows_shift) {
+    const uint32_t b = t >> rows_shift, r = t & ((1u << rows_shift) - 1u);
+    return ((((b * halves + h) << rows_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
+}
+
+struct Item {
+    int32_t i, g, tile;
+    int32_t n, qlen, q0;       // context, queries, first query row of the sequence
+    int32_t row0, rows;        // rows [row0, row0 + rows) of the (qlen x G) rows
+    int32_t chunks;            // K/V chunks the tile needs
+};
+
+// Item w of the flattened list: sequence i holds Hkv * tiles_i items.
+__device__ __forceinline__ Item find_item(const int32_t* prefix, const Params& p, int32_t w,
+                                          int32_t max_len) {
+    int32_t lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (prefix[mid] <= w) lo = mid; else hi = mid;
+    }
+    Item it;
+    it.i = lo;
+    const int32_t tiles = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+    const int32_t local = w - prefix[lo];
+    it.g = local / tiles;
+    it.tile = local - it.g * tiles;
+    it.n = clamp_len(__ldg(p.context_lens + lo), max_len);
+    it.q0 = __ldg(p.q_start + lo);
+    it.qlen = __ldg(p.q_start + lo + 1) - it.q0;
+    it.row0 = it.tile * kRows;
+    it.rows = min(kRows, it.qlen * p.G - it.row0);
+    const int32_t r_max = (it.row0 + it.rows - 1) / p.G;
+    const int32_t kv_end = it.n - it.qlen + r_max + 1;     // keys 0 .. kv_end-1
+    it.chunks = (kv_end + kKv - 1) / kKv;
+    return it;
+}
+
+// 2 CTAs x 160 threads per SM leave 204 registers per thread; the cap keeps
+// the D = 128 accumulators (O 64, Q 32, S 32, P 16) out of local memory.
+template <int D, bool kBF16>
+__global__ void __maxnreg__(200)
+multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const Params p) {
+    constexpr uint32_t kHalves = D / 64;
+    const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
+    const Layout L = make_layout(D, B, S);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + kMaxStages;
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
+    int32_t* scan = prefix + (B + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t max_len = p.max_blocks * bs;
+    const uint32_t rows_shift = (uint32_t)(31 - __clz(bs < 32 ? bs : 32));
+
+    // ---- item prefix: prefix[i] = Hkv * sum_{i' < i} ceil(qlen_i' * G / 64)
+    {
+        const int per = (B + kThreads - 1) / kThreads;
+        const int beg = min(tid * per, B), end = min(beg + per, B);
+        auto tiles_of = [&](int i) {
+            const int32_t n = __ldg(p.context_lens + i);
+            const int32_t qlen = __ldg(p.q_start + i + 1) - __ldg(p.q_start + i);
+            if (qlen < 0 || qlen > clamp_len(n, max_len)) {
+                if (blockIdx.x == 0 && qlen != 0) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
+                return 0;
+            }
+            if (blockIdx.x == 0 && n > max_len) pa::raise_error(p.err, PA_DEVERR_TABLE_WIDTH);
+            return (qlen * G + kRows - 1) / kRows;
+        };
+        int32_t local = 0;
+        for (int i = beg; i < end; ++i) local += tiles_of(i);
+        int32_t x = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) scan[warp] = x;
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) {
+                pa::mbar_init(&full[s], 1);
+                pa::mbar_init(&empty[s], kWarps);
+            }
+            pa::fence_barrier_init();
+        }
+        __syncthreads();
+        int32_t run = x - local;
+        for (int w = 0; w < warp; ++w) run += scan[w];
+        for (int i = beg; i < end; ++i) {
+            prefix[i] = run * Hkv;
+            run += tiles_of(i);
+        }
+        if (tid == 0) {
+            int32_t total = 0;
+            for (int w = 0; w < kThreads / 32; ++w) total += scan[w];
+            prefix[B] = total * Hkv;
+        }
+        __syncthreads();
+    }
+    const int32_t W = prefix[B];
+    // This CTA's items, heaviest first: w = W - 1 - (blockIdx.x + k * gridDim.x).
+    auto item_at = [&](int32_t k) { return W - 1 - ((int32_t)blockIdx.x + k * (int32_t)gridDim.x); };
+
+    if (warp == kWarps) {
+        // =============================== producer ===============================
+        if (lane == 0) {
+            pa::prefetch_tensormap(&kmap);
+            pa::prefetch_tensormap(&vmap);
+        }
+        const uint64_t policy = pa::l2_policy_evict_first();
+        const int bs_shift = 31 - __clz(bs);
+        const int bpc = kKv >> rows_shift;             // boxes per chunk and tensor (2..8)
+        const int32_t oob_row = p.num_blocks * bs;
+        const uint32_t tx_bytes = L.stage_bytes;
+        auto load_window = [&](int32_t i, int32_t base) {
+            const int32_t j = base + lane;
+            return j < p.max_blocks ? __ldg(p.block_tables + (int64_t)i * p.max_blocks + j) : -1;
+        };
+        int stage = 0;
+        uint32_t use = 0;
+        int32_t kglob = 0;       // chunks issued so far
+        bool dead = false;
+        int32_t w = item_at(0);
+        int32_t went = -1, wnext = -1, nwent = -1, nwnext = -1;
+        if (w >= 0) {
+            const Item it = find_item(prefix, p, w, max_len);
+            went = load_window(it.i, 0);
+            wnext = load_window(it.i, 32);
+        }
+        for (int32_t k = 0; w >= 0 && !dead; ++k) {
+            const Item it = find_item(prefix, p, w, max_len);
+            const int32_t wn = item_at(k + 1);
+            if (wn >= 0) {                               // the next item's first windows
+                const Item nx = find_item(prefix, p, wn, max_len);
+                nwent = load_window(nx.i, 0);
+                nwnext = load_window(nx.i, 32);
+            }
+            const int32_t nb = (it.n + bs - 1) >> bs_shift;
+            int32_t wbase = 0;
+            for (int32_t c = 0; c < it.chunks; ++c, ++kglob) {
+                const int32_t j0 = (c * kKv) >> bs_shift;  // windows start at multiples of bpc
+                if (j0 + bpc > wbase + 32) {
+                    wbase += 32;
+                    went = wnext;
+                    wnext = load_window(it.i, wbase + 32);
+                }
+                if (kglob >= S &&
+                    !__all_sync(0xffffffffu, pa::mbar_wait(&empty[stage], use ^ 1u, kWaitLimitNs))) {
+                    dead = true;
+                    if (lane == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+                    break;
+                }
+                int32_t blk[8];
+#pragma unroll
+                for (int b = 0; b < 8; ++b)
+                    blk[b] = __shfl_sync(0xffffffffu, went, (j0 - wbase + b) & 31);
+                if (lane == 0) {
+                    pa::mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                    unsigned char* kdst = smem + stage * L.stage_bytes;
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        if (b >= bpc) break;
+                        bool ok = j0 + b < nb;
+                        if (ok && (blk[b] < 0 || blk[b] >= p.num_blocks)) {
+                            ok = false;
+                            pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                        }
+                        const uint32_t off = ((uint32_t)b * kHalves << rows_shift) * 128;
+                        const int32_t row = ok ? blk[b] * bs : oob_row;
+                        const int32_t z = it.g * (int32_t)kHalves;
+                        pa::tma_load_3d(kdst + off, &kmap, &full[stage], 0, row, z, policy);
+                        pa::tma_load_3d(kdst + L.stage_bytes / 2 + off, &vmap, &full[stage], 0,
+                                        row, z, policy);
+                    }
+                }
+                __syncwarp();
+                if (++stage == S) {
+                    stage = 0;
+                    use ^= 1u;
+                }
+            }
+            w = wn;
+            went = nwent;
+            wnext = nwnext;
+        }
+        // every issued load has landed before the CTA may exit
+        for (int s = 0; s < S && s < kglob; ++s) {
+            const int32_t last_use = (kglob - 1 - s) / S;
+            pa::mbar_wait(&full[s], (uint32_t)(last_use & 1), kWaitLimitNs);
+        }
+        return;
+    }
+
+    // ================================ consumers ================================
+    const int qr = lane >> 2;        // fragment row (and +8)
+    const int qc = 2 * (lane & 3);   // fragment column pair
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t smem_base = pa::smem_addr(smem);
+    int stage = 0;
+    uint32_t use = 0;
+    bool dead = false;
+
+    for (int32_t k = 0;; ++k) {
+        const int32_t w = item_at(k);
+        if (w < 0) break;
+        const Item it = find_item(prefix, p, w, max_len);
+        // this lane's two rows: (token r, head hg) and its causal limit
+        int32_t lim[2];
+        const uint16_t* qrow[2];
+        bool valid[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int32_t row = it.row0 + warp * 16 + qr + 8 * h2;
+            valid[h2] = row - it.row0 < it.rows;
+            const int32_t r = row / G, hg = row - (row / G) * G;
+            lim[h2] = valid[h2] ? it.n - it.qlen + r : -1;
+            qrow[h2] = p.q + ((int64_t)(it.q0 + r) * p.H + it.g * G + hg) * D + qc;
+        }
+        // Q as A fragments
+        uint32_t qa[D / 16][4];
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                qa[ks][h2] = valid[h2] ? __ldg(reinterpret_cast<const unsigned int*>(qrow[h2] + 16 * ks)) : 0u;
+                qa[ks][2 + h2] =
+                    valid[h2] ? __ldg(reinterpret_cast<const unsigned int*>(qrow[h2] + 16 * ks + 8)) : 0u;
+            }
+        }
+        float o[D / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        const int32_t warp_lim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
+
+        for (int32_t c = 0; c < it.chunks; ++c) {
+            const bool ready =
+                dead || pa::mbar_wait(&full[stage], use, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ready)) {
+                dead = true;
+                if (lane == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+            }
+            const int32_t key0 = c * kKv;
+            if (!dead && key0 <= warp_lim) {
+                const uint32_t kt = smem_base + stage * L.stage_bytes;
+                const uint32_t vt = kt + L.stage_bytes / 2;
+                const int32_t valid_keys = min(it.n - key0, kKv);
+                if (valid_keys < kKv) {
+                    // zero V rows past the context (every warp, before its own use)
+                    unsigned char* vbytes = smem + stage * L.stage_bytes + L.stage_bytes / 2;
+                    const int per_half = (kKv - valid_keys) * 8;
+                    for (int e = lane; e < per_half * (int)kHalves; e += 32) {
+                        const int hh = e / per_half, rem = e - hh * per_half;
+                        const uint32_t tok = (uint32_t)(valid_keys + (rem >> 3));
+                        *reinterpret_cast<uint4*>(
+                            vbytes + tile_offset(tok, hh, rem & 7, kHalves, rows_shift)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    pa::fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                // S = Q K^T: 16 rows x 64 keys (8 n-tiles)
+                float s[8][4];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t d = 16 * ks + (mi & 1) * 8;
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        const uint32_t key = 16 * np + (mi >> 1) * 8 + rr;
+                        uint32_t b[4];
+                        pa::ldsm_x4(kt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves, rows_shift),
+                                    b[0], b[1], b[2], b[3]);
+                        pa::mma_16816<kBF16>(s[2 * np], qa[ks], b[0], b[1]);
+                        pa::mma_16816<kBF16>(s[2 * np + 1], qa[ks], b[2], b[3]);
+                    }
+                }
+                // causal mask, online softmax (rows qr and qr + 8 of this warp)
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int32_t key = key0 + 8 * nt + qc + (e & 1);
+                        const float x = key <= lim[e >> 1] ? s[nt][e] * p.scale_log2 : -INFINITY;
+                        s[nt][e] = x;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                    }
+                float alpha[2], msafe[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float v = mx[h2];
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+                    const float m_new = fmaxf(m_run[h2], v);
+                    msafe[h2] = m_new == -INFINITY ? 0.f : m_new;
+                    alpha[h2] = pa::fast_exp2(m_run[h2] - msafe[h2]);
+                    m_run[h2] = m_new;
+                    l_run[h2] *= alpha[h2];
+                }
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    o[nt][0] *= alpha[0];
+                    o[nt][1] *= alpha[0];
+                    o[nt][2] *= alpha[1];
+                    o[nt][3] *= alpha[1];
+                }
+                // P as A fragments (k-step = 16 keys = n-tiles 2 ks2, 2 ks2 + 1).
+                // bf16 keeps 8 bits of P: a second, residual part (pl) restores
+                // about 16, so a row of a few keys whose V terms cancel stays
+                // within the tolerance; f16 P (11 bits) needs none.
+                uint32_t pa_[4][4], pl[4][4];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    float e4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        e4[e] = pa::fast_exp2(s[nt][e] - msafe[e >> 1]);
+                        l_run[e >> 1] += e4[e];
+                    }
+                    const uint32_t h01 = pa::pack2<kBF16>(e4[0], e4[1]);
+                    const uint32_t h23 = pa::pack2<kBF16>(e4[2], e4[3]);
+                    pa_[nt >> 1][(nt & 1) * 2] = h01;
+                    pa_[nt >> 1][(nt & 1) * 2 + 1] = h23;
+                    if constexpr (kBF16) {
+                        pl[nt >> 1][(nt & 1) * 2] = pa::bf16x2_residual(h01, e4[0], e4[1]);
+                        pl[nt >> 1][(nt & 1) * 2 + 1] = pa::bf16x2_residual(h23, e4[2], e4[3]);
+                    }
+                }
+                // O += P V: 16 rows x D (D/8 n-tiles), 64 keys (4 k-steps)
+#pragma unroll
+                for (int ks2 = 0; ks2 < 4; ++ks2) {
+                    const uint32_t key = 16 * ks2 + (mi & 1) * 8 + rr;
+                    const uint32_t a[4] = {pa_[ks2][0], pa_[ks2][1], pa_[ks2][2], pa_[ks2][3]};
+                    const uint32_t al[4] = {pl[ks2][0], pl[ks2][1], pl[ks2][2], pl[ks2][3]};
+#pragma unroll
+                    for (int np2 = 0; np2 < D / 16; ++np2) {
+                        const uint32_t d = 16 * np2 + (mi >> 1) * 8;
+                        uint32_t b[4];
+                        pa::ldsm_x4_trans(vt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves,
+                                                           rows_shift),
+                                          b[0], b[1], b[2], b[3]);
+                        pa::mma_16816<kBF16>(o[2 * np2], a, b[0], b[1]);
+                        pa::mma_16816<kBF16>(o[2 * np2 + 1], a, b[2], b[3]);
+                        if constexpr (kBF16) {
+                            pa::mma_16816<kBF16>(o[2 * np2], al, b[0], b[1]);
+                            pa::mma_16816<kBF16>(o[2 * np2 + 1], al, b[2], b[3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&empty[stage]);
+            if (++stage == S) {
+                stage = 0;
+                use ^= 1u;
+            }
+        }
+        if (dead) continue;
+        // normalise and store
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float v = l_run[h2];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            l_run[h2] = v > 0.f ? 1.f / v : 0.f;
+        }
+        uint16_t* orow[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+            orow[h2] = p.out + (qrow[h2] - p.q);           // same [T][H][D] offset as q
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+                if (valid[h2])
+                    *reinterpret_cast<uint32_t*>(orow[h2] + 8 * nt) =
+                        pa::pack2<kBF16>(o[nt][2 * h2] * l_run[h2], o[nt][2 * h2 + 1] * l_run[h2]);
+    }
+}
+
+// ---- host side -----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// The decode's 3-D cache view: {64 elements, token rows of the pool, 64-column
+// half over all KV heads}; box {64, min(block_size, 32), d / 64}.
+bool encode_cache_map(CUtensorMap* map, const void* base, int32_t rows, int32_t Hkv, int32_t d,
+                      int32_t block_size, pa_dtype dtype) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)Hkv * d / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)Hkv * d * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(block_size < 32 ? block_size : 32),
+                               (cuuint32_t)(d / 64)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return encode(map,
+                  dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int choose_stages(int D, int B) {
+    const Layout L0 = make_layout(D, B, 0);
+    if (L0.total >= kSmemBudget) return 0;
+    int s = (int)((kSmemBudget - L0.total) / L0.stage_bytes);
+    return s > kMaxStages ? kMaxStages : s;
+}
+
+template <int D, bool kBF16>
+pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const Params& prm, size_t smem,
+                 int grid, cudaStream_t stream) {
+    auto kern = multi_query_kernel<D, kBF16>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBudget);
+    });
+    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(km, vm, prm);
+    return pa::cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks, const int32_t* context_lens,
+                                int32_t max_q_len, int32_t B, int32_t H, int32_t Hkv, int32_t d,
+                                int32_t block_size, int32_t num_blocks, float scale,
+                                pa_dtype dtype, void* out, void* stream) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || max_q_len < 0 ||
+        !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (H % Hkv != 0) return PA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int G = H / Hkv;
+    // item indices are int32: every sequence's tiles times Hkv
+    if ((int64_t)B * Hkv * (((int64_t)max_q_len * G + kRows - 1) / kRows) >= ((int64_t)1 << 30))
+        return PA_ERR_UNSUPPORTED;
+    if (B == 0 || max_q_len == 0) return PA_OK;
+    if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+        return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3u)
+        return PA_ERR_INVALID;
+    const int stages = choose_stages(d, B);
+    if (stages < 2) return PA_ERR_UNSUPPORTED;
+    unsigned int* err = pa::device_error_word();
+    const int sms = pa::device_sm_count();
+    if (!err || !sms) return PA_ERR_CUDA;
+
+    CUtensorMap km, vm;
+    const int32_t rows = num_blocks * block_size;
+    if (!encode_cache_map(&km, k_cache, rows, Hkv, d, block_size, dtype) ||
+        !encode_cache_map(&vm, v_cache, rows, Hkv, d, block_size, dtype))
+        return PA_ERR_CUDA;
+
+    Params prm;
+    prm.q = static_cast<const uint16_t*>(q);
+    prm.q_start = q_start;
+    prm.out = static_cast<uint16_t*>(out);
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.err = err;
+    prm.max_blocks = max_blocks;
+    prm.B = B;
+    prm.H = H;
+    prm.Hkv = Hkv;
+    prm.G = G;
+    prm.bs = block_size;
+    prm.num_blocks = num_blocks;
+    prm.stages = stages;
+    prm.scale_log2 = scale * kLog2e;
+    const size_t smem = make_layout(d, B, stages).total;
+    const int grid = sms * kCtasPerSm;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 128)
+        return dtype == PA_BF16 ? launch<128, true>(km, vm, prm, smem, grid, st)
+                                : launch<128, false>(km, vm, prm, smem, grid, st);
+    return dtype == PA_BF16 ? launch<64, true>(km, vm, prm, smem, grid, st)
+                            : launch<64, false>(km, vm, prm, smem, grid, st);
+}
+
+}  // extern "C"

@@ -131,6 +131,9 @@ def _custom(B, H, Hkv, d, bs, lens, dtype=torch.bfloat16, seed=0, extra_blocks=3
     dict(B=2, H=14, Hkv=2, d=64, bs=16, lens=[5000, 17], dtype=torch.bfloat16),
     dict(B=1, H=4, Hkv=1, d=128, bs=16, lens=[100000]),                  # one pair on every CTA
     dict(B=300, H=8, Hkv=2, d=128, bs=16, lens=list(range(1, 301))),
+    # many short bf16 rows: a few keys whose V terms cancel need more than the
+    # 8 bits of a bf16 P
+    dict(B=512, H=28, Hkv=4, d=128, bs=8, lens=[1 + (7 * i) % 12 for i in range(512)]),
 ])
 def test_edge_shapes(case):
     dtype = case.pop("dtype", torch.bfloat16)

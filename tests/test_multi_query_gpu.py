@@ -1,0 +1,133 @@
+"""GPU parity of pa_multi_query (several causal query tokens per sequence over
+the paged cache: chunked prefill, speculative verification) against the fp64
+oracle, |gpu - ref| <= 2e-3 + 1e-2 |ref| per element.  Unused slots of every
+last block hold NaN, so keys past a context must contribute nothing."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_103_gb300 import binding
+from paged_kv_cache_103_gb300 import workloads as wl
+
+from _harness import THREADS, assert_close, nan_tails
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_103_gb300 import build
+    build.build()
+    binding.load()
+
+
+def _setup(lens, qlens, H, Hkv, d, bs, dtype, seed):
+    N = int(math.ceil(1.25 * sum(math.ceil(n / bs) for n in lens))) + 2
+    m = oracle.BlockManagerModel(N, bs, np.random.default_rng(seed).permutation(N))
+    for i, n in enumerate(lens):
+        m.allocate(i, int(n))
+    kc = wl.normal_tensor((N, bs, Hkv, d), dtype, seed * 3 + 1)
+    vc = wl.normal_tensor((N, bs, Hkv, d), dtype, seed * 3 + 2)
+    nan_tails(m, kc, vc)
+    tbl, ln = m.export(range(len(lens)))
+    q_start = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q = wl.normal_tensor((int(q_start[-1]), H, d), dtype, seed * 3 + 3)
+    return kc, vc, tbl, ln, q_start, q
+
+
+def _gpu(kc, vc, tbl, ln, q_start, q, scale, max_q_len=None):
+    out = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    binding.pa_multi_query(q.cuda(), torch.from_numpy(q_start).cuda(), kc.cuda(), vc.cuda(),
+                           torch.from_numpy(tbl).cuda(), torch.from_numpy(ln).cuda(),
+                           int(max_q_len if max_q_len is not None else np.diff(q_start).max(initial=0)),
+                           scale, out)
+    return out
+
+
+def _ref(kc, vc, tbl, ln, q_start, q, scale):
+    code = oracle.DTYPE_F16 if q.dtype == torch.float16 else oracle.DTYPE_BF16
+    return oracle.multi_query(wl.bits(q), q_start, wl.bits(kc), wl.bits(vc), tbl, ln, scale, code,
+                              num_threads=THREADS)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (28, 4), (32, 4), (32, 2)])
+@pytest.mark.parametrize("d,bs,dtype", [(64, 16, torch.float16), (128, 8, torch.bfloat16),
+                                        (128, 32, torch.float16)])
+def test_mixed_query_lengths(H, Hkv, d, bs, dtype):
+    lens = [1, 37, 200, 130, 64, 71, 5]
+    qlens = [1, 6, 200, 65, 1, 0, 5]          # decode, speculative, whole prompt, chunk, none
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, H, Hkv, d, bs, dtype, H + d + bs)
+    scale = 1 / math.sqrt(d)
+    out = _gpu(kc, vc, tbl, ln, qs, q, scale)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, scale), "multi-query G=%d" % (H // Hkv))
+
+
+def test_speculative_verification_full_size():
+    """128 sequences of the Qwen long-tail shape verifying 6 tokens each (a
+    draft of 5 plus the last accepted token)."""
+    w = wl.qwen_longtail(16)
+    lens = np.asarray(w.context_lens, np.int64) + 6
+    qlens = [6] * w.B
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, w.H, w.Hkv, w.d, w.block_size, torch.bfloat16, 21)
+    out = _gpu(kc, vc, tbl, ln, qs, q, w.scale)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, w.scale), "speculative 128 x 6")
+
+
+def test_chunked_prefill_chunk_of_512():
+    """Two sequences each prefilling a 512-token chunk on top of 3584 cached
+    tokens (GQA 32 / 8, bf16)."""
+    lens = [4096, 4096]
+    qlens = [512, 512]
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, 32, 8, 128, 16, torch.bfloat16, 22)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128)), "chunk 512")
+
+
+def test_chunked_prefill_chunk_of_2048_sampled_rows():
+    """A 2048-token chunk on top of 6144 cached tokens, checked on sampled
+    rows: row r equals the oracle's single-query attention over its own
+    causal prefix (n - qlen + r + 1 tokens)."""
+    n, qlen, H, Hkv, d = 8192, 2048, 32, 8, 128
+    kc, vc, tbl, ln, qs, q = _setup([n], [qlen], H, Hkv, d, 16, torch.bfloat16, 23)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d)).cpu()
+    assert binding.pa_check_device_errors() == 0
+    for r in [0, 1, 63, 64, 777, 1500, 2046, 2047]:
+        ref = oracle.multi_query(wl.bits(q[r:r + 1]), [0, 1], wl.bits(kc), wl.bits(vc), tbl,
+                                 [n - qlen + r + 1], 1 / math.sqrt(d), oracle.DTYPE_BF16,
+                                 num_threads=THREADS)
+        assert_close(out[r:r + 1], ref, "chunk 2048 row %d" % r)
+
+
+def test_single_query_matches_decode_reference():
+    lens = [300, 1, 1000, 64]
+    kc, vc, tbl, ln, qs, q = _setup(lens, [1, 1, 1, 1], 8, 2, 128, 16, torch.float16, 24)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 0.1)
+    ref = oracle.decode(wl.bits(q), wl.bits(kc), wl.bits(vc), tbl, ln, 0.1, oracle.DTYPE_F16,
+                        num_threads=THREADS)
+    assert_close(out.cpu(), ref, "single query")
+
+
+def test_repeat_is_deterministic():
+    kc, vc, tbl, ln, qs, q = _setup([900, 333], [129, 17], 28, 4, 128, 16, torch.bfloat16, 25)
+    a = _gpu(kc, vc, tbl, ln, qs, q, 0.09)
+    b = _gpu(kc, vc, tbl, ln, qs, q, 0.09)
+    assert torch.equal(a, b)
+
+
+def test_more_queries_than_context_is_flagged_and_skipped():
+    kc, vc, tbl, ln, qs, q = _setup([10, 20], [3, 5], 4, 2, 64, 16, torch.float16, 26)
+    ln_bad = ln.copy()
+    ln_bad[0] = 2                                # 3 queries, 2 cached tokens
+    out = _gpu(kc, vc, tbl, ln_bad, qs, q, 0.125)
+    assert binding.pa_check_device_errors() & binding.DEVERR["CONTEXT"]
+    assert torch.isnan(out[:3].float()).all()     # sequence 0 untouched
+    ref = _ref(kc, vc, tbl, ln, qs, q, 0.125)
+    assert_close(out[3:].cpu(), ref[3:], "the valid sequence")
