@@ -699,6 +699,116 @@ def run_swap(args):
                    "bytes_per_direction": int(moved)}}))
 
 
+def load_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_multi_query(args):
+    """pa_multi_query on two shapes: a chunked prefill (4 sequences, a
+    2048-token chunk each on top of 6144 cached tokens, 7B GQA 32 / 8 heads,
+    bf16) timed against the tensor roofline, and speculative verification (the
+    Qwen long-tail batch of 128 sequences, 6 query tokens each) timed against
+    the HBM roofline.  CUDA events over repeated launches on one stream."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+    from paged_kv_cache_103_gb300 import build as pa_build
+
+    pa_build.build()
+    binding.load()
+    dev = torch.device("cuda")
+
+    def make(lens, qlens, H, Hkv, d, bs, seed):
+        N = int(math.ceil(1.25 * sum(math.ceil(n / bs) for n in lens))) + 2
+        alloc = binding.Allocator(N, bs, np.random.default_rng(seed).permutation(N).astype(np.int32))
+        for i, n in enumerate(lens):
+            alloc.alloc(i, int(n))
+        mb = max(math.ceil(n / bs) for n in lens)
+        tbl, ln = alloc.export(list(range(len(lens))), mb)
+        qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+        g = torch.Generator(device=dev).manual_seed(seed)
+        kc = torch.randn(N, bs, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn(N, bs, Hkv, d, generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn(int(qs[-1]), H, d, generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        ws = torch.empty(binding.pa_multi_query_workspace_size(len(lens), H, Hkv, d,
+                                                                int(max(qlens))),
+                         dtype=torch.uint8, device=dev)
+        binding.pa_decode_workspace_init(ws)
+        return dict(kc=kc, vc=vc, q=q, out=out, ws=ws, tbl=torch.from_numpy(tbl).to(dev),
+                    ln=torch.from_numpy(ln).to(dev), qs=torch.from_numpy(qs).to(dev),
+                    lens=np.asarray(lens), qlens=np.asarray(qlens), H=H, Hkv=Hkv, d=d,
+                    maxq=int(max(qlens)))
+
+    def time_it(c, reps, flush=None):
+        def run():
+            binding.pa_multi_query(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"], c["maxq"],
+                                   1 / math.sqrt(c["d"]), c["out"], c["ws"])
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            if flush is not None:
+                flush.zero_()
+                torch.count_nonzero(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if binding.pa_check_device_errors():
+            raise RuntimeError("device error flags set")
+        return sorted(ts)[len(ts) // 2]
+
+    reps = max(5, min(args.steps, 50))
+    # chunked prefill
+    pf = make([8192] * 4, [2048] * 4, 32, 8, 128, 16, 31)
+    t_pf = time_it(pf, reps)
+    keys = sum(sum(n - ql + r + 1 for r in range(ql)) for n, ql in zip(pf["lens"], pf["qlens"]))
+    flops = 4.0 * pf["H"] * pf["d"] * keys
+    tflops = flops / (t_pf * 1e-3) / 1e12
+    peak_t, peak_kind = load_tensor_peak()
+    # speculative verification
+    w = wl_mod().qwen_longtail(16)
+    lens = (np.asarray(w.context_lens, np.int64) + 6).tolist()
+    sv = make(lens, [6] * w.B, w.H, w.Hkv, w.d, 16, 32)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    t_sv = time_it(sv, reps, flush)
+    kv = kv_bytes(lens, w.Hkv, w.d)
+    gbs = kv / (t_sv * 1e-3) / 1e9
+    peak_h, _ = load_peak()
+    print(json.dumps({
+        "metric": "multi-query paged attention: TFLOP/s (chunked prefill), KV GB/s "
+                  "(speculative verification)",
+        "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": reps, "warmup": 3,
+        "ms_per_step": round(t_pf, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (N(0,1) Q/K/V, random block placement)",
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak_t, 4),
+                     "peak_source": "%s bf16_tflops (cuBLAS burst)" % peak_kind,
+                     "flops_per_launch": flops,
+                     "note": "mma.sync m16n8k16 path; bf16 PV carries a residual operand "
+                             "(1.5x the MMAs of the plain count)"},
+        "e2e": None,
+        "speculative_verification": {
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t_sv * 1e3, 2),
+            "pct_of_hbm_peak": round(100 * gbs / peak_h, 1), "tokens": 6 * w.B,
+            "config": "qwen long-tail batch, 128 sequences x 6 query tokens, 28 / 4 heads, "
+                      "block 16, L2 flushed between launches"},
+        "gpu_launches": 2 * (reps + 3),
+        "config": {"workload": "chunked prefill: 4 sequences x 2048-token chunk on 6144 cached "
+                               "tokens, 32 / 8 heads of 128, bf16, block 16",
+                   "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,8 +824,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-format", choices=["native", "fp8"], default="native",
                     help="cache in the workload's 16-bit dtype, or E4M3 codes + fp32 scales")
-    ap.add_argument("--measure", choices=["decode", "swap"], default="decode",
-                    help="swap: device<->host block swap bandwidth instead of the decode step")
+    ap.add_argument("--measure", choices=["decode", "swap", "multi_query"], default="decode",
+                    help="swap: device<->host block swap bandwidth; multi_query: chunked prefill "
+                         "and speculative verification, instead of the decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -723,6 +834,8 @@ def main():
         run_reference(args)
     elif args.measure == "swap":
         run_swap(args)
+    elif args.measure == "multi_query":
+        run_multi_query(args)
     else:
         run_gpu(args)
 

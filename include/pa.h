@@ -369,20 +369,30 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
  *   out[q_start[i] + r][h] = sum_j softmax_j(scale * q[q_start[i] + r][h] . K_j) V_j
  * with K_j, V_j as in pa_decode (KV head h / G), fp32 accumulation, rounded
  * once to the output dtype.  qlen_i = 1 is the decode of one token; qlen_i = n
- * is the prefill of a whole prompt.  No workspace: no context is split.
+ * is the prefill of a whole prompt.  The work (64-row query tiles x 64-key
+ * chunks) is split evenly over the CTAs, so a tile whose context is long is
+ * shared by several CTAs whose partial results the last one merges; the
+ * workspace holds their arrival tickets and partials.
  *   q            (device) [T][H][d], T = q_start[B]; out (device) [T][H][d]
  *   q_start      (device) [B + 1] int32, q_start[0] = 0, non-decreasing
- *   max_q_len    (host) an upper bound of every qlen_i
+ *   max_q_len    (host) an upper bound of every qlen_i (sizes the workspace)
+ *   workspace    (device) >= pa_multi_query_workspace_size(B, H, Hkv, d,
+ *                max_q_len) bytes, zeroed once (pa_decode_workspace_init);
+ *                every call leaves the tickets at zero
  *   other arguments as in pa_decode
- * qlen_i > n (or < 0) skips sequence i and sets PA_DEVERR_CONTEXT; a context
+ * qlen_i > n (or < 0), or a batch with more query rows than max_q_len allows,
+ * skips the sequence (or the call) and sets PA_DEVERR_CONTEXT; a context
  * longer than its table row is cut to it and sets PA_DEVERR_TABLE_WIDTH; a
  * table entry outside the pool reads zeros and sets PA_DEVERR_BLOCK_ID. */
+PA_API size_t pa_multi_query_workspace_size(int32_t B, int32_t H, int32_t Hkv, int32_t d,
+                                            int32_t max_q_len);
 PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables,
                                 int32_t max_blocks, const int32_t* context_lens,
                                 int32_t max_q_len, int32_t B, int32_t H, int32_t Hkv, int32_t d,
                                 int32_t block_size, int32_t num_blocks, float scale,
-                                pa_dtype dtype, void* out, void* stream);
+                                pa_dtype dtype, void* out, void* workspace, size_t ws_bytes,
+                                void* stream);
 
 /* pa_decode over an FP8 cache written by pa_reshape_and_cache_fp8 ([P4]
  * section 4.3).  Computes what pa_decode computes with

@@ -79,8 +79,9 @@ SIGNATURES = {
     "pa_decode_workspace_init": (_ST, [_P, _SZ, _P]),
     "pa_decode": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                         _F32, _ST, _P, _P, _SZ, _P]),
+    "pa_multi_query_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pa_multi_query": (_ST, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
-                             _I32, ctypes.c_float, _ST, _P, _P]),
+                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_fp8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -250,11 +251,16 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
            "pa_decode")
 
 
+def pa_multi_query_workspace_size(B: int, H: int, Hkv: int, d: int, max_q_len: int) -> int:
+    return int(load().pa_multi_query_workspace_size(B, H, Hkv, d, max_q_len))
+
+
 def pa_multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, max_q_len: int,
-                   scale: float, out, stream=None) -> None:
+                   scale: float, out, workspace, stream=None) -> None:
     """``q/out [T, H, d]`` (the last ``q_start[i+1]-q_start[i]`` tokens of sequence i,
     concatenated), ``q_start [B+1]`` int32, caches ``[N, bs, Hkv, d]``,
-    ``block_tables [B, max_blocks]`` and ``context_lens [B]`` int32."""
+    ``block_tables [B, max_blocks]`` and ``context_lens [B]`` int32, ``workspace`` a
+    zero-initialised byte tensor of ``pa_multi_query_workspace_size`` bytes."""
     import torch
     T, H, d = q.shape
     N, bs, Hkv, _ = k_cache.shape
@@ -263,7 +269,9 @@ def pa_multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, max
                                  _dev(v_cache), _dev(block_tables, torch.int32),
                                  int(block_tables.shape[1]), _dev(context_lens, torch.int32),
                                  int(max_q_len), B, H, Hkv, d, bs, N, float(scale),
-                                 _dtype_code(q), _dev(out), _stream_ptr(stream)),
+                                 _dtype_code(q), _dev(out), _dev(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)),
            "pa_multi_query")
 
 

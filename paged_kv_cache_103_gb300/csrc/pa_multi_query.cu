@@ -33,13 +33,15 @@
 
 namespace {
 
-constexpr int kRows = 64;           // query rows per work item (4 warps x 16)
-constexpr int kKv = 64;             // keys per pipeline stage
+constexpr int kRows = 64;           // query rows per item (4 warps x 16)
+constexpr int kKv = 64;             // keys per pipeline stage (a "chunk")
 constexpr int kWarps = 4;           // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 8;
 constexpr int kMaxBatch = 4096;
+constexpr int kMaxCtas = 512;
+constexpr int kMinChunksPerCta = 4;
 constexpr uint32_t kSmemBudget = 113 * 1024;
 constexpr uint64_t kWaitLimitNs = 1ull << 30;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -50,8 +52,10 @@ struct Params {
     uint16_t* out;
     const int32_t* block_tables;
     const int32_t* context_lens;
+    int32_t* counters;   // [items_cap][kWarps] arrival tickets of split items
+    float* partials;     // [2 * kMaxCtas][kRows * (D + 2)] per-CTA partial rows
     unsigned int* err;
-    int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages;
+    int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages, items_cap;
     float scale_log2;
 };
 
@@ -59,12 +63,13 @@ struct Layout {
     uint32_t stage_bytes, bars, prefix, total;
 };
 
+// Stages, barriers, then prefix[B + 1] (chunks), iprefix[B + 1] (items), scan[64].
 __host__ __device__ inline Layout make_layout(int D, int B, int stages) {
     Layout L;
     L.stage_bytes = 2u * kKv * D * 2;                      // K then V, 16-bit
     L.bars = stages * L.stage_bytes;                       // full[], empty[]
-    L.prefix = L.bars + 2 * kMaxStages * 8;                // [B + 1] int32 item prefix
-    L.total = 1024 + L.prefix + (uint32_t)(B + 1) * 4 + 32 * 4;
+    L.prefix = L.bars + 2 * kMaxStages * 8;
+    L.total = 1024 + L.prefix + (uint32_t)(B + 1) * 8 + 64 * 4;
     return L;
 }
 
@@ -80,45 +85,85 @@ __device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t
     return ((((b * halves + h) << rows_shift) + r) << 7) + ((c ^ (t & 7u)) << 4);
 }
 
-struct Item {
-    int32_t i, g, tile;
-    int32_t n, qlen, q0;       // context, queries, first query row of the sequence
-    int32_t row0, rows;        // rows [row0, row0 + rows) of the (qlen x G) rows
-    int32_t chunks;            // K/V chunks the tile needs
+struct SeqInfo {
+    int32_t n, qlen, q0, tiles;   // context, queries, first query row, 64-row tiles
 };
 
-// Item w of the flattened list: sequence i holds Hkv * tiles_i items.
-__device__ __forceinline__ Item find_item(const int32_t* prefix, const Params& p, int32_t w,
-                                          int32_t max_len) {
-    int32_t lo = 0, hi = p.B;
-    while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (prefix[mid] <= w) lo = mid; else hi = mid;
-    }
-    Item it;
-    it.i = lo;
-    const int32_t tiles = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
-    const int32_t local = w - prefix[lo];
-    it.g = local / tiles;
-    it.tile = local - it.g * tiles;
-    it.n = clamp_len(__ldg(p.context_lens + lo), max_len);
-    it.q0 = __ldg(p.q_start + lo);
-    it.qlen = __ldg(p.q_start + lo + 1) - it.q0;
-    it.row0 = it.tile * kRows;
-    it.rows = min(kRows, it.qlen * p.G - it.row0);
-    const int32_t r_max = (it.row0 + it.rows - 1) / p.G;
-    const int32_t kv_end = it.n - it.qlen + r_max + 1;     // keys 0 .. kv_end-1
-    it.chunks = (kv_end + kKv - 1) / kKv;
-    return it;
+__device__ __forceinline__ SeqInfo seq_info(const Params& p, int32_t i, int32_t max_len) {
+    SeqInfo s;
+    s.n = clamp_len(__ldg(p.context_lens + i), max_len);
+    s.q0 = __ldg(p.q_start + i);
+    s.qlen = __ldg(p.q_start + i + 1) - s.q0;
+    s.tiles = (s.qlen < 0 || s.qlen > s.n) ? 0 : (s.qlen * p.G + kRows - 1) / kRows;
+    return s;
 }
 
-// 2 CTAs x 160 threads per SM leave 204 registers per thread; the cap keeps
-// the D = 128 accumulators (O 64, Q 32, S 32, P 16) out of local memory.
+// Chunks tile t reads: keys 0 .. n - qlen + r_max, r_max its last query token.
+__device__ __forceinline__ int32_t tile_chunks(const SeqInfo& s, int32_t t, int32_t G) {
+    const int32_t rows_end = min((t + 1) * kRows, s.qlen * G);
+    const int32_t r_max = (rows_end - 1) / G;
+    return (s.n - s.qlen + r_max + 1 + kKv - 1) / kKv;
+}
+
+// The flattened work list is every (sequence i, KV head g, tile t, chunk c)
+// in that order; a segment is the part of one item (i, g, t) inside [pos, hi).
+struct Seg {
+    int32_t i, g, t;
+    SeqInfo s;
+    int32_t c0, len, nc;   // first chunk, chunks in the segment, chunks of the item
+    int32_t a;             // flattened index of the item's first chunk
+    int32_t item;          // item id (counter index)
+};
+
+__device__ __forceinline__ Seg find_seg(const int32_t* prefix, const int32_t* iprefix,
+                                        const Params& p, int32_t pos, int32_t hi,
+                                        int32_t max_len) {
+    int32_t lo_i = 0, hi_i = p.B;
+    while (hi_i - lo_i > 1) {
+        const int32_t mid = (lo_i + hi_i) >> 1;
+        if (prefix[mid] <= pos) lo_i = mid; else hi_i = mid;
+    }
+    Seg sg;
+    sg.i = lo_i;
+    sg.s = seq_info(p, lo_i, max_len);
+    const int32_t per_g = (prefix[lo_i + 1] - prefix[lo_i]) / p.Hkv;
+    const int32_t local = pos - prefix[lo_i];
+    sg.g = local / per_g;
+    const int32_t lg = local - sg.g * per_g;
+    int32_t t = 0, acc = 0, ct = tile_chunks(sg.s, 0, p.G);
+    while (acc + ct <= lg) {
+        acc += ct;
+        ++t;
+        ct = tile_chunks(sg.s, t, p.G);
+    }
+    sg.t = t;
+    sg.nc = ct;
+    sg.c0 = lg - acc;
+    sg.a = pos - sg.c0;
+    sg.len = min(hi - pos, ct - sg.c0);
+    sg.item = iprefix[lo_i] + sg.g * sg.s.tiles + t;
+    return sg;
+}
+
+__device__ __forceinline__ int32_t cta_begin(int64_t c, int64_t W, int64_t C) {
+    return (int32_t)(c * W / C);
+}
+
+// Slot of the partial CTA c leaves for the item starting at a: its first slot
+// if the item is where its share begins, else its second.
+__device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t W, int64_t C, int32_t a) {
+    return cta_begin(c, W, C) >= a ? 2 * c : 2 * c + 1;
+}
+
+// Two CTAs of five warps per SM put three warps on two of the four SM
+// sub-partitions, whose register files hold 16K registers each: 168 per
+// thread at most.
 template <int D, bool kBF16>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(168)
 multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const Params p) {
     constexpr uint32_t kHalves = D / 64;
+    constexpr int kSlotFloats = kRows * (D + 2);
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
     const Layout L = make_layout(D, B, S);
     extern __shared__ unsigned char smem_raw[];
@@ -127,35 +172,50 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kMaxStages;
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
-    int32_t* scan = prefix + (B + 1);
+    int32_t* iprefix = prefix + (B + 1);
+    int32_t* scan = iprefix + (B + 1);   // [32] chunks, [32] items
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t max_len = p.max_blocks * bs;
     const uint32_t rows_shift = (uint32_t)(31 - __clz(bs < 32 ? bs : 32));
 
-    // ---- item prefix: prefix[i] = Hkv * sum_{i' < i} ceil(qlen_i' * G / 64)
+    // ---- prefixes: prefix[i] = Hkv * chunks of sequence i's tiles before i,
+    //      iprefix[i] = Hkv * tiles before i
     {
         const int per = (B + kThreads - 1) / kThreads;
         const int beg = min(tid * per, B), end = min(beg + per, B);
-        auto tiles_of = [&](int i) {
-            const int32_t n = __ldg(p.context_lens + i);
-            const int32_t qlen = __ldg(p.q_start + i + 1) - __ldg(p.q_start + i);
-            if (qlen < 0 || qlen > clamp_len(n, max_len)) {
-                if (blockIdx.x == 0 && qlen != 0) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
-                return 0;
+        auto count = [&](int i, int32_t& chunks, int32_t& tiles) {
+            const SeqInfo s = seq_info(p, i, max_len);
+            if (blockIdx.x == 0) {
+                const int32_t raw = __ldg(p.context_lens + i);
+                if (s.qlen != 0 && s.tiles == 0) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
+                if (raw > max_len) pa::raise_error(p.err, PA_DEVERR_TABLE_WIDTH);
             }
-            if (blockIdx.x == 0 && n > max_len) pa::raise_error(p.err, PA_DEVERR_TABLE_WIDTH);
-            return (qlen * G + kRows - 1) / kRows;
+            tiles = s.tiles;
+            chunks = 0;
+            for (int32_t t = 0; t < s.tiles; ++t) chunks += tile_chunks(s, t, G);
         };
-        int32_t local = 0;
-        for (int i = beg; i < end; ++i) local += tiles_of(i);
-        int32_t x = local;
+        int32_t lc = 0, lt = 0;
+        for (int i = beg; i < end; ++i) {
+            int32_t c, t;
+            count(i, c, t);
+            lc += c;
+            lt += t;
+        }
+        int32_t xc = lc, xt = lt;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
+            const int32_t yc = __shfl_up_sync(0xffffffffu, xc, off);
+            const int32_t yt = __shfl_up_sync(0xffffffffu, xt, off);
+            if (lane >= off) {
+                xc += yc;
+                xt += yt;
+            }
         }
-        if (lane == 31) scan[warp] = x;
+        if (lane == 31) {
+            scan[warp] = xc;
+            scan[32 + warp] = xt;
+        }
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
                 pa::mbar_init(&full[s], 1);
@@ -164,22 +224,40 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
             pa::fence_barrier_init();
         }
         __syncthreads();
-        int32_t run = x - local;
-        for (int w = 0; w < warp; ++w) run += scan[w];
+        int32_t rc = xc - lc, rt = xt - lt;
+        for (int w = 0; w < warp; ++w) {
+            rc += scan[w];
+            rt += scan[32 + w];
+        }
         for (int i = beg; i < end; ++i) {
-            prefix[i] = run * Hkv;
-            run += tiles_of(i);
+            prefix[i] = rc * Hkv;
+            iprefix[i] = rt * Hkv;
+            int32_t c, t;
+            count(i, c, t);
+            rc += c;
+            rt += t;
         }
         if (tid == 0) {
-            int32_t total = 0;
-            for (int w = 0; w < kThreads / 32; ++w) total += scan[w];
-            prefix[B] = total * Hkv;
+            int32_t tc = 0, tt = 0;
+            for (int w = 0; w < kThreads / 32; ++w) {
+                tc += scan[w];
+                tt += scan[32 + w];
+            }
+            prefix[B] = tc * Hkv;
+            iprefix[B] = tt * Hkv;
+            if (blockIdx.x == 0 && iprefix[B] > p.items_cap) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
         }
         __syncthreads();
     }
-    const int32_t W = prefix[B];
-    // This CTA's items, heaviest first: w = W - 1 - (blockIdx.x + k * gridDim.x).
-    auto item_at = [&](int32_t k) { return W - 1 - ((int32_t)blockIdx.x + k * (int32_t)gridDim.x); };
+    if (iprefix[B] > p.items_cap) return;   // more queries than max_q_len promised
+    const int64_t W = prefix[B];
+    // every CTA gets at least kMinChunksPerCta chunks of a balanced contiguous share
+    int64_t C = W / kMinChunksPerCta;
+    if (C > (int64_t)gridDim.x) C = gridDim.x;
+    if (C < 1) C = 1;
+    if ((int64_t)blockIdx.x >= C) return;
+    const int32_t lo = cta_begin(blockIdx.x, W, C);
+    const int32_t hi = cta_begin(blockIdx.x + 1, W, C);
 
     if (warp == kWarps) {
         // =============================== producer ===============================
@@ -189,9 +267,8 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         const uint64_t policy = pa::l2_policy_evict_first();
         const int bs_shift = 31 - __clz(bs);
-        const int bpc = kKv >> rows_shift;             // boxes per chunk and tensor (2..8)
+        const int bpc = kKv >> rows_shift;             // blocks (boxes per tensor) per chunk
         const int32_t oob_row = p.num_blocks * bs;
-        const uint32_t tx_bytes = L.stage_bytes;
         auto load_window = [&](int32_t i, int32_t base) {
             const int32_t j = base + lane;
             return j < p.max_blocks ? __ldg(p.block_tables + (int64_t)i * p.max_blocks + j) : -1;
@@ -200,29 +277,30 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
         uint32_t use = 0;
         int32_t kglob = 0;       // chunks issued so far
         bool dead = false;
-        int32_t w = item_at(0);
+        Seg cur{}, nxt{};
         int32_t went = -1, wnext = -1, nwent = -1, nwnext = -1;
-        if (w >= 0) {
-            const Item it = find_item(prefix, p, w, max_len);
-            went = load_window(it.i, 0);
-            wnext = load_window(it.i, 32);
+        if (lo < hi) {
+            cur = find_seg(prefix, iprefix, p, lo, hi, max_len);
+            const int32_t b0 = (cur.c0 * kKv) >> bs_shift;
+            went = load_window(cur.i, b0);
+            wnext = load_window(cur.i, b0 + 32);
         }
-        for (int32_t k = 0; w >= 0 && !dead; ++k) {
-            const Item it = find_item(prefix, p, w, max_len);
-            const int32_t wn = item_at(k + 1);
-            if (wn >= 0) {                               // the next item's first windows
-                const Item nx = find_item(prefix, p, wn, max_len);
-                nwent = load_window(nx.i, 0);
-                nwnext = load_window(nx.i, 32);
+        for (int32_t pos = lo; pos < hi && !dead;) {
+            const int32_t npos = pos + cur.len;
+            if (npos < hi) {                                 // the next segment's windows
+                nxt = find_seg(prefix, iprefix, p, npos, hi, max_len);
+                const int32_t b0 = (nxt.c0 * kKv) >> bs_shift;
+                nwent = load_window(nxt.i, b0);
+                nwnext = load_window(nxt.i, b0 + 32);
             }
-            const int32_t nb = (it.n + bs - 1) >> bs_shift;
-            int32_t wbase = 0;
-            for (int32_t c = 0; c < it.chunks; ++c, ++kglob) {
-                const int32_t j0 = (c * kKv) >> bs_shift;  // windows start at multiples of bpc
+            const int32_t nb = (cur.s.n + bs - 1) >> bs_shift;
+            int32_t wbase = (cur.c0 * kKv) >> bs_shift;      // windows start at multiples of bpc
+            for (int32_t c = cur.c0; c < cur.c0 + cur.len; ++c, ++kglob) {
+                const int32_t j0 = (c * kKv) >> bs_shift;
                 if (j0 + bpc > wbase + 32) {
                     wbase += 32;
                     went = wnext;
-                    wnext = load_window(it.i, wbase + 32);
+                    wnext = load_window(cur.i, wbase + 32);
                 }
                 if (kglob >= S &&
                     !__all_sync(0xffffffffu, pa::mbar_wait(&empty[stage], use ^ 1u, kWaitLimitNs))) {
@@ -235,7 +313,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int b = 0; b < 8; ++b)
                     blk[b] = __shfl_sync(0xffffffffu, went, (j0 - wbase + b) & 31);
                 if (lane == 0) {
-                    pa::mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                    pa::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
                     unsigned char* kdst = smem + stage * L.stage_bytes;
 #pragma unroll
                     for (int b = 0; b < 8; ++b) {
@@ -247,7 +325,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                         }
                         const uint32_t off = ((uint32_t)b * kHalves << rows_shift) * 128;
                         const int32_t row = ok ? blk[b] * bs : oob_row;
-                        const int32_t z = it.g * (int32_t)kHalves;
+                        const int32_t z = cur.g * (int32_t)kHalves;
                         pa::tma_load_3d(kdst + off, &kmap, &full[stage], 0, row, z, policy);
                         pa::tma_load_3d(kdst + L.stage_bytes / 2 + off, &vmap, &full[stage], 0,
                                         row, z, policy);
@@ -259,9 +337,10 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                     use ^= 1u;
                 }
             }
-            w = wn;
+            cur = nxt;
             went = nwent;
             wnext = nwnext;
+            pos = npos;
         }
         // every issued load has landed before the CTA may exit
         for (int s = 0; s < S && s < kglob; ++s) {
@@ -280,42 +359,41 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
     uint32_t use = 0;
     bool dead = false;
 
-    for (int32_t k = 0;; ++k) {
-        const int32_t w = item_at(k);
-        if (w < 0) break;
-        const Item it = find_item(prefix, p, w, max_len);
+    for (int32_t pos = lo; pos < hi;) {
+        const Seg sg = find_seg(prefix, iprefix, p, pos, hi, max_len);
+        pos += sg.len;
+        const int32_t row0 = sg.t * kRows;
+        const int32_t nrows = min(kRows, sg.s.qlen * G - row0);
         // this lane's two rows: (token r, head hg) and its causal limit
         int32_t lim[2];
-        const uint16_t* qrow[2];
+        int64_t qoff[2];
         bool valid[2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-            const int32_t row = it.row0 + warp * 16 + qr + 8 * h2;
-            valid[h2] = row - it.row0 < it.rows;
-            const int32_t r = row / G, hg = row - (row / G) * G;
-            lim[h2] = valid[h2] ? it.n - it.qlen + r : -1;
-            qrow[h2] = p.q + ((int64_t)(it.q0 + r) * p.H + it.g * G + hg) * D + qc;
+            const int32_t row = warp * 16 + qr + 8 * h2;
+            valid[h2] = row < nrows;
+            const int32_t ra = row0 + row;
+            const int32_t r = ra / G, hg = ra - (ra / G) * G;
+            lim[h2] = valid[h2] ? sg.s.n - sg.s.qlen + r : -1;
+            qoff[h2] = ((int64_t)(sg.s.q0 + r) * p.H + sg.g * G + hg) * D + qc;
         }
-        // Q as A fragments
-        uint32_t qa[D / 16][4];
+        uint32_t qa[D / 16][4];   // Q as A fragments
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+        for (int ks = 0; ks < D / 16; ++ks)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                qa[ks][h2] = valid[h2] ? __ldg(reinterpret_cast<const unsigned int*>(qrow[h2] + 16 * ks)) : 0u;
-                qa[ks][2 + h2] =
-                    valid[h2] ? __ldg(reinterpret_cast<const unsigned int*>(qrow[h2] + 16 * ks + 8)) : 0u;
+                const unsigned int* qp = reinterpret_cast<const unsigned int*>(p.q + qoff[h2] + 16 * ks);
+                qa[ks][h2] = valid[h2] ? __ldg(qp) : 0u;
+                qa[ks][2 + h2] = valid[h2] ? __ldg(qp + 4) : 0u;
             }
-        }
         float o[D / 8][4];
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         const int32_t warp_lim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
 
-        for (int32_t c = 0; c < it.chunks; ++c) {
-            const bool ready =
-                dead || pa::mbar_wait(&full[stage], use, kWaitLimitNs);
+        for (int32_t c = sg.c0; c < sg.c0 + sg.len; ++c) {
+            const bool ready = dead || pa::mbar_wait(&full[stage], use, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ready)) {
                 dead = true;
                 if (lane == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
@@ -324,7 +402,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
             if (!dead && key0 <= warp_lim) {
                 const uint32_t kt = smem_base + stage * L.stage_bytes;
                 const uint32_t vt = kt + L.stage_bytes / 2;
-                const int32_t valid_keys = min(it.n - key0, kKv);
+                const int32_t valid_keys = min(sg.s.n - key0, kKv);
                 if (valid_keys < kKv) {
                     // zero V rows past the context (every warp, before its own use)
                     unsigned char* vbytes = smem + stage * L.stage_bytes + L.stage_bytes / 2;
@@ -339,93 +417,101 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                     pa::fence_proxy_async_smem();
                     __syncwarp();
                 }
-                // S = Q K^T: 16 rows x 64 keys (8 n-tiles)
-                float s[8][4];
+                // The chunk in two halves of 32 keys (fewer live registers: two
+                // CTAs per SM); a half past every row's causal limit is skipped.
+#pragma unroll 1
+                for (int kh = 0; kh < 2; ++kh) {
+                    const int32_t hkey0 = key0 + 32 * kh;
+                    if (hkey0 > warp_lim) break;
+                    // S = Q K^T: 16 rows x 32 keys (4 n-tiles)
+                    float s[4][4];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+                    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t d = 16 * ks + (mi & 1) * 8;
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t d = 16 * ks + (mi & 1) * 8;
 #pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        const uint32_t key = 16 * np + (mi >> 1) * 8 + rr;
-                        uint32_t b[4];
-                        pa::ldsm_x4(kt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves, rows_shift),
-                                    b[0], b[1], b[2], b[3]);
-                        pa::mma_16816<kBF16>(s[2 * np], qa[ks], b[0], b[1]);
-                        pa::mma_16816<kBF16>(s[2 * np + 1], qa[ks], b[2], b[3]);
+                        for (int np = 0; np < 2; ++np) {
+                            const uint32_t key = 32 * kh + 16 * np + (mi >> 1) * 8 + rr;
+                            uint32_t b[4];
+                            pa::ldsm_x4(kt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves,
+                                                         rows_shift),
+                                        b[0], b[1], b[2], b[3]);
+                            pa::mma_16816<kBF16>(s[2 * np], qa[ks], b[0], b[1]);
+                            pa::mma_16816<kBF16>(s[2 * np + 1], qa[ks], b[2], b[3]);
+                        }
                     }
-                }
-                // causal mask, online softmax (rows qr and qr + 8 of this warp)
-                float mx[2] = {-INFINITY, -INFINITY};
+                    // causal mask, online softmax (rows qr and qr + 8 of this warp)
+                    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+                    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int32_t key = key0 + 8 * nt + qc + (e & 1);
-                        const float x = key <= lim[e >> 1] ? s[nt][e] * p.scale_log2 : -INFINITY;
-                        s[nt][e] = x;
-                        mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                        for (int e = 0; e < 4; ++e) {
+                            const int32_t key = hkey0 + 8 * nt + qc + (e & 1);
+                            const float x = key <= lim[e >> 1] ? s[nt][e] * p.scale_log2 : -INFINITY;
+                            s[nt][e] = x;
+                            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                        }
+                    float alpha[2], msafe[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float v = mx[h2];
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+                        const float m_new = fmaxf(m_run[h2], v);
+                        msafe[h2] = m_new == -INFINITY ? 0.f : m_new;
+                        alpha[h2] = pa::fast_exp2(m_run[h2] - msafe[h2]);
+                        m_run[h2] = m_new;
+                        l_run[h2] *= alpha[h2];
                     }
-                float alpha[2], msafe[2];
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float v = mx[h2];
-                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-                    const float m_new = fmaxf(m_run[h2], v);
-                    msafe[h2] = m_new == -INFINITY ? 0.f : m_new;
-                    alpha[h2] = pa::fast_exp2(m_run[h2] - msafe[h2]);
-                    m_run[h2] = m_new;
-                    l_run[h2] *= alpha[h2];
-                }
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    o[nt][0] *= alpha[0];
-                    o[nt][1] *= alpha[0];
-                    o[nt][2] *= alpha[1];
-                    o[nt][3] *= alpha[1];
-                }
-                // P as A fragments (k-step = 16 keys = n-tiles 2 ks2, 2 ks2 + 1).
-                // bf16 keeps 8 bits of P: a second, residual part (pl) restores
-                // about 16, so a row of a few keys whose V terms cancel stays
-                // within the tolerance; f16 P (11 bits) needs none.
-                uint32_t pa_[4][4], pl[4][4];
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    float e4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        e4[e] = pa::fast_exp2(s[nt][e] - msafe[e >> 1]);
-                        l_run[e >> 1] += e4[e];
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        o[nt][0] *= alpha[0];
+                        o[nt][1] *= alpha[0];
+                        o[nt][2] *= alpha[1];
+                        o[nt][3] *= alpha[1];
                     }
-                    const uint32_t h01 = pa::pack2<kBF16>(e4[0], e4[1]);
-                    const uint32_t h23 = pa::pack2<kBF16>(e4[2], e4[3]);
-                    pa_[nt >> 1][(nt & 1) * 2] = h01;
-                    pa_[nt >> 1][(nt & 1) * 2 + 1] = h23;
-                    if constexpr (kBF16) {
-                        pl[nt >> 1][(nt & 1) * 2] = pa::bf16x2_residual(h01, e4[0], e4[1]);
-                        pl[nt >> 1][(nt & 1) * 2 + 1] = pa::bf16x2_residual(h23, e4[2], e4[3]);
-                    }
-                }
-                // O += P V: 16 rows x D (D/8 n-tiles), 64 keys (4 k-steps)
+                    // P as A fragments (k-step = 16 keys = n-tiles 2 ks2, 2 ks2 + 1).
+                    // bf16 keeps 8 bits of P: a second, residual part (pl)
+                    // restores about 16, so a row of a few keys whose V terms
+                    // cancel stays within the tolerance; f16 P (11 bits) needs none.
+                    uint32_t pa_[2][4], pl[2][4];
 #pragma unroll
-                for (int ks2 = 0; ks2 < 4; ++ks2) {
-                    const uint32_t key = 16 * ks2 + (mi & 1) * 8 + rr;
-                    const uint32_t a[4] = {pa_[ks2][0], pa_[ks2][1], pa_[ks2][2], pa_[ks2][3]};
-                    const uint32_t al[4] = {pl[ks2][0], pl[ks2][1], pl[ks2][2], pl[ks2][3]};
+                    for (int nt = 0; nt < 4; ++nt) {
+                        float e4[4];
 #pragma unroll
-                    for (int np2 = 0; np2 < D / 16; ++np2) {
-                        const uint32_t d = 16 * np2 + (mi >> 1) * 8;
-                        uint32_t b[4];
-                        pa::ldsm_x4_trans(vt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves,
-                                                           rows_shift),
-                                          b[0], b[1], b[2], b[3]);
-                        pa::mma_16816<kBF16>(o[2 * np2], a, b[0], b[1]);
-                        pa::mma_16816<kBF16>(o[2 * np2 + 1], a, b[2], b[3]);
+                        for (int e = 0; e < 4; ++e) {
+                            e4[e] = pa::fast_exp2(s[nt][e] - msafe[e >> 1]);
+                            l_run[e >> 1] += e4[e];
+                        }
+                        const uint32_t h01 = pa::pack2<kBF16>(e4[0], e4[1]);
+                        const uint32_t h23 = pa::pack2<kBF16>(e4[2], e4[3]);
+                        pa_[nt >> 1][(nt & 1) * 2] = h01;
+                        pa_[nt >> 1][(nt & 1) * 2 + 1] = h23;
                         if constexpr (kBF16) {
-                            pa::mma_16816<kBF16>(o[2 * np2], al, b[0], b[1]);
-                            pa::mma_16816<kBF16>(o[2 * np2 + 1], al, b[2], b[3]);
+                            pl[nt >> 1][(nt & 1) * 2] = pa::bf16x2_residual(h01, e4[0], e4[1]);
+                            pl[nt >> 1][(nt & 1) * 2 + 1] = pa::bf16x2_residual(h23, e4[2], e4[3]);
+                        }
+                    }
+                    // O += P V: 16 rows x D (D/8 n-tiles), 32 keys (2 k-steps)
+#pragma unroll
+                    for (int ks2 = 0; ks2 < 2; ++ks2) {
+                        const uint32_t key = 32 * kh + 16 * ks2 + (mi & 1) * 8 + rr;
+                        const uint32_t a[4] = {pa_[ks2][0], pa_[ks2][1], pa_[ks2][2], pa_[ks2][3]};
+                        const uint32_t al[4] = {pl[ks2][0], pl[ks2][1], pl[ks2][2], pl[ks2][3]};
+#pragma unroll
+                        for (int np2 = 0; np2 < D / 16; ++np2) {
+                            const uint32_t d = 16 * np2 + (mi >> 1) * 8;
+                            uint32_t b[4];
+                            pa::ldsm_x4_trans(vt + tile_offset(key, d >> 6, (d & 63) >> 3, kHalves,
+                                                               rows_shift),
+                                              b[0], b[1], b[2], b[3]);
+                            pa::mma_16816<kBF16>(o[2 * np2], a, b[0], b[1]);
+                            pa::mma_16816<kBF16>(o[2 * np2 + 1], a, b[2], b[3]);
+                            if constexpr (kBF16) {
+                                pa::mma_16816<kBF16>(o[2 * np2], al, b[0], b[1]);
+                                pa::mma_16816<kBF16>(o[2 * np2 + 1], al, b[2], b[3]);
+                            }
                         }
                     }
                 }
@@ -438,25 +524,89 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
             }
         }
         if (dead) continue;
-        // normalise and store
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
             float v = l_run[h2];
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
-            l_run[h2] = v > 0.f ? 1.f / v : 0.f;
+            l_run[h2] = v;
         }
-        uint16_t* orow[2];
+        auto store_row_pair = [&](int h2, int nt, float x, float y) {
+            *reinterpret_cast<uint32_t*>(p.out + qoff[h2] + 8 * nt) = pa::pack2<kBF16>(x, y);
+        };
+        if (sg.c0 == 0 && sg.len == sg.nc) {
+            // the whole item is in this CTA's share: normalise and store
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-            orow[h2] = p.out + (qrow[h2] - p.q);           // same [T][H][D] offset as q
+            for (int h2 = 0; h2 < 2; ++h2) {
+                if (!valid[h2]) continue;
+                const float inv = l_run[h2] > 0.f ? 1.f / l_run[h2] : 0.f;
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
+                for (int nt = 0; nt < D / 8; ++nt)
+                    store_row_pair(h2, nt, o[nt][2 * h2] * inv, o[nt][2 * h2 + 1] * inv);
+            }
+            continue;
+        }
+        // A split item: this warp's 16 rows go to the CTA's partial slot; the
+        // last CTA to finish them (per-warp ticket) merges all partials.
+        const int64_t c_first = ((int64_t)(sg.a + 1) * C - 1) / W;
+        const int64_t c_last = ((int64_t)(sg.a + sg.nc) * C - 1) / W;
+        float* ps = p.partials + partial_slot(blockIdx.x, W, C, sg.a) * kSlotFloats;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-                if (valid[h2])
-                    *reinterpret_cast<uint32_t*>(orow[h2] + 8 * nt) =
-                        pa::pack2<kBF16>(o[nt][2 * h2] * l_run[h2], o[nt][2 * h2 + 1] * l_run[h2]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int row = warp * 16 + qr + 8 * h2;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<float2*>(&ps[row * D + 8 * nt + qc]) =
+                    make_float2(o[nt][2 * h2], o[nt][2 * h2 + 1]);
+            if ((lane & 3) == 0) {
+                ps[kRows * D + row] = m_run[h2];
+                ps[kRows * D + kRows + row] = l_run[h2];
+            }
+        }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence();
+            int32_t* ctr = p.counters + (int64_t)sg.item * kWarps + warp;
+            last = atomicAdd(ctr, 1) == (int)(c_last - c_first);
+            if (last) {
+                atomicExch(ctr, 0);
+                __threadfence();
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        const int ncov = (int)(c_last - c_first + 1);
+        const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == sg.a ? 0 : 1);
+        for (int e = lane; e < 16 * (D / 4); e += 32) {
+            const int row = warp * 16 + e / (D / 4), d4 = (e % (D / 4)) * 4;
+            if (row >= nrows) continue;
+            float M = -INFINITY;
+            for (int cc = 0; cc < ncov; ++cc) {
+                const float* q = p.partials + (cc ? 2 * (c_first + cc) : slot0) * kSlotFloats;
+                M = fmaxf(M, __ldcg(q + kRows * D + row));
+            }
+            const float msafe = M == -INFINITY ? 0.f : M;
+            float Ls = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cc = 0; cc < ncov; ++cc) {
+                const float* q = p.partials + (cc ? 2 * (c_first + cc) : slot0) * kSlotFloats;
+                const float f = pa::fast_exp2(__ldcg(q + kRows * D + row) - msafe);
+                Ls += f * __ldcg(q + kRows * D + kRows + row);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(q + row * D + d4));
+                acc.x += f * v.x;
+                acc.y += f * v.y;
+                acc.z += f * v.z;
+                acc.w += f * v.w;
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            const int32_t ra = row0 + row;
+            const int32_t r = ra / G, hg = ra - (ra / G) * G;
+            uint2 packed;
+            packed.x = pa::pack2<kBF16>(acc.x * inv, acc.y * inv);
+            packed.y = pa::pack2<kBF16>(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)(sg.s.q0 + r) * p.H + sg.g * G + hg) * D +
+                                      d4) = packed;
+        }
     }
 }
 
@@ -503,6 +653,20 @@ int choose_stages(int D, int B) {
     return s > kMaxStages ? kMaxStages : s;
 }
 
+// Upper bound of the work items: every sequence's 64-row tiles times Hkv.
+int64_t items_cap(int32_t B, int32_t H, int32_t Hkv, int32_t max_q_len) {
+    const int64_t G = H / Hkv;
+    return (int64_t)B * Hkv * (((int64_t)max_q_len * G + kRows - 1) / kRows);
+}
+
+size_t counters_bytes(int64_t items) {
+    return (((size_t)items * kWarps * sizeof(int32_t)) + 255) & ~size_t(255);
+}
+
+size_t partials_bytes(int32_t d) {
+    return (size_t)2 * kMaxCtas * kRows * (d + 2) * sizeof(float);
+}
+
 template <int D, bool kBF16>
 pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const Params& prm, size_t smem,
                  int grid, cudaStream_t stream) {
@@ -512,6 +676,9 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const Params& prm
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBudget);
+        if (attr_err == cudaSuccess)   // the largest shared-memory carve-out: two CTAs per SM
+            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                            100);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
     kern<<<grid, kThreads, smem, stream>>>(km, vm, prm);
@@ -522,12 +689,20 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const Params& prm
 
 extern "C" {
 
+PA_API size_t pa_multi_query_workspace_size(int32_t B, int32_t H, int32_t Hkv, int32_t d,
+                                            int32_t max_q_len) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || max_q_len < 0 || (d != 64 && d != 128))
+        return 0;
+    return counters_bytes(items_cap(B, H, Hkv, max_q_len)) + partials_bytes(d);
+}
+
 PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables,
                                 int32_t max_blocks, const int32_t* context_lens,
                                 int32_t max_q_len, int32_t B, int32_t H, int32_t Hkv, int32_t d,
                                 int32_t block_size, int32_t num_blocks, float scale,
-                                pa_dtype dtype, void* out, void* stream) {
+                                pa_dtype dtype, void* out, void* workspace, size_t ws_bytes,
+                                void* stream) {
     if (B < 0 || H <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || max_q_len < 0 ||
         !std::isfinite(scale))
         return PA_ERR_INVALID;
@@ -538,15 +713,19 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
     if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
     if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
     const int G = H / Hkv;
-    // item indices are int32: every sequence's tiles times Hkv
-    if ((int64_t)B * Hkv * (((int64_t)max_q_len * G + kRows - 1) / kRows) >= ((int64_t)1 << 30))
-        return PA_ERR_UNSUPPORTED;
+    // flattened chunk indices are int32: every tile's chunks times Hkv
+    const int64_t cap = items_cap(B, H, Hkv, max_q_len);
+    const int64_t max_chunks = ((int64_t)max_blocks * block_size + kKv - 1) / kKv;
+    if (cap * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
     if (B == 0 || max_q_len == 0) return PA_OK;
-    if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out ||
+        !workspace)
         return PA_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+    if (ws_bytes < pa_multi_query_workspace_size(B, H, Hkv, d, max_q_len)) return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(workspace)) & 15u)
         return PA_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3u)
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7u)
         return PA_ERR_INVALID;
     const int stages = choose_stages(d, B);
     if (stages < 2) return PA_ERR_UNSUPPORTED;
@@ -566,6 +745,9 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
     prm.out = static_cast<uint16_t*>(out);
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
+    prm.counters = static_cast<int32_t*>(workspace);
+    prm.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                            counters_bytes(cap));
     prm.err = err;
     prm.max_blocks = max_blocks;
     prm.B = B;
@@ -575,9 +757,11 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
     prm.bs = block_size;
     prm.num_blocks = num_blocks;
     prm.stages = stages;
+    prm.items_cap = (int32_t)cap;
     prm.scale_log2 = scale * kLog2e;
     const size_t smem = make_layout(d, B, stages).total;
-    const int grid = sms * kCtasPerSm;
+    int grid = sms * kCtasPerSm;
+    if (grid > kMaxCtas) grid = kMaxCtas;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 128)
         return dtype == PA_BF16 ? launch<128, true>(km, vm, prm, smem, grid, st)

@@ -40,12 +40,22 @@ def _setup(lens, qlens, H, Hkv, d, bs, dtype, seed):
     return kc, vc, tbl, ln, q_start, q
 
 
-def _gpu(kc, vc, tbl, ln, q_start, q, scale, max_q_len=None):
+def _workspace(B, H, Hkv, d, mq):
+    ws = torch.empty(binding.pa_multi_query_workspace_size(B, H, Hkv, d, mq), dtype=torch.uint8,
+                     device="cuda")
+    binding.pa_decode_workspace_init(ws)
+    return ws
+
+
+def _gpu(kc, vc, tbl, ln, q_start, q, scale, max_q_len=None, ws=None):
     out = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    mq = int(max_q_len if max_q_len is not None else np.diff(q_start).max(initial=0))
+    H, d = q.shape[1], q.shape[2]
+    if ws is None:
+        ws = _workspace(len(ln), H, kc.shape[2], d, mq)
     binding.pa_multi_query(q.cuda(), torch.from_numpy(q_start).cuda(), kc.cuda(), vc.cuda(),
-                           torch.from_numpy(tbl).cuda(), torch.from_numpy(ln).cuda(),
-                           int(max_q_len if max_q_len is not None else np.diff(q_start).max(initial=0)),
-                           scale, out)
+                           torch.from_numpy(tbl).cuda(), torch.from_numpy(ln).cuda(), mq, scale,
+                           out, ws)
     return out
 
 
@@ -115,11 +125,18 @@ def test_single_query_matches_decode_reference():
     assert_close(out.cpu(), ref, "single query")
 
 
-def test_repeat_is_deterministic():
-    kc, vc, tbl, ln, qs, q = _setup([900, 333], [129, 17], 28, 4, 128, 16, torch.bfloat16, 25)
-    a = _gpu(kc, vc, tbl, ln, qs, q, 0.09)
-    b = _gpu(kc, vc, tbl, ln, qs, q, 0.09)
-    assert torch.equal(a, b)
+def test_repeat_reuses_workspace_and_is_deterministic():
+    """Long contexts with few tiles make the items split between CTAs; a
+    reused workspace must come back with every ticket at zero."""
+    kc, vc, tbl, ln, qs, q = _setup([20000, 333, 9000], [6, 17, 6], 28, 4, 128, 16,
+                                    torch.bfloat16, 25)
+    ws = _workspace(3, 28, 4, 128, 17)
+    a = _gpu(kc, vc, tbl, ln, qs, q, 0.09, ws=ws)
+    for _ in range(3):
+        b = _gpu(kc, vc, tbl, ln, qs, q, 0.09, ws=ws)
+        assert torch.equal(a, b)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(a.cpu(), _ref(kc, vc, tbl, ln, qs, q, 0.09), "split items")
 
 
 def test_more_queries_than_context_is_flagged_and_skipped():
