@@ -785,9 +785,34 @@ def run_multi_query(args):
     kv = kv_bytes(lens, w.Hkv, w.d)
     gbs = kv / (t_sv * 1e-3) / 1e9
     peak_h, _ = load_peak()
+    # the oracle on the host cores: 256 query rows of the first prefill sequence (each over its
+    # full causal context), same tables and cache contents
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = os.cpu_count() or 1
+        rows = 256
+        qs0 = np.array([0, rows], np.int32)
+        qh = pf["q"][:rows].cpu()
+        n0 = int(pf["lens"][0])
+        q_off = n0 - int(pf["qlens"][0])            # these are the chunk's first rows
+        kh_, vh_ = pf["kc"].cpu(), pf["vc"].cpu()
+        tbl0 = pf["tbl"][:1].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.multi_query(wl_mod().bits(qh), qs0, wl_mod().bits(kh_), wl_mod().bits(vh_), tbl0,
+                           np.array([q_off + rows], np.int32), 1 / math.sqrt(pf["d"]),
+                           oracle.DTYPE_BF16, num_threads=threads)
+        dt = time.perf_counter() - t0
+        cflops = 4.0 * pf["H"] * pf["d"] * sum(q_off + r + 1 for r in range(rows))
+        cpu = {"value": round(cflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle", "seconds": round(dt, 2),
+               "sample": "%d query rows of one 2048-token prefill chunk (each over its %d+ "
+                         "causal keys), fp64 C oracle" % (rows, q_off + 1)}
     print(json.dumps({
         "metric": "multi-query paged attention: TFLOP/s (chunked prefill), KV GB/s "
                   "(speculative verification)",
+        "cpu_baseline": cpu,
         "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": reps, "warmup": 3,
         "ms_per_step": round(t_pf, 4), "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic (N(0,1) Q/K/V, random block placement)",
