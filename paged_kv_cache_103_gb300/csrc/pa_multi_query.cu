@@ -8,18 +8,24 @@
 //
 //  * Work items are (sequence, KV head, tile of 64 rows), a row being one
 //    (query token, query head of the KV head's group) pair in token-major
-//    order, so one K/V chunk serves the whole GQA group.  Persistent CTAs (two
-//    per SM) take items heaviest-first (the last tiles of each sequence see
-//    the most keys).
-//  * A producer warp streams 64-token K and V chunks of the item's context
-//    (only up to the tile's last causal key) through a shared-memory ring with
-//    the decode's 3-D TMA boxes; the table is read 32 entries at a time, the
-//    next window and the next item's first window one step ahead.
+//    order, so one K/V chunk serves the whole GQA group.  An item reads the
+//    64-key chunks of its context up to its last row's causal limit.  The
+//    list of (item, chunk) pairs is cut into equal contiguous shares over the
+//    persistent CTAs (two per SM); an item inside one share finishes in one
+//    pass, an item split between shares leaves per-row partials (m, l, O) and
+//    the last CTA to finish it -- an atomic ticket per item and warp, never a
+//    wait -- merges them.
+//  * A producer warp streams the K and V chunks of its share through a
+//    shared-memory ring with the decode's 3-D TMA boxes; the table is read 32
+//    entries at a time, the next window and the next segment's first window
+//    one step ahead.
 //  * Four consumer warps own 16 rows each and run FlashAttention-style over
-//    the chunks: S = Q K^T and O += P V as m16n8k16 tensor-core MMAs (P stays
-//    in registers as the A operand), online softmax in base 2 with the per-row
-//    causal limit, normalisation once at the end.  V rows past the context are
-//    zeroed in shared memory before use (unwritten slots may hold NaN).
+//    the chunks in 32-key halves: S = Q K^T and O += P V as m16n8k16
+//    tensor-core MMAs (P stays in registers as the A operand; a bf16 P carries
+//    its rounding residual as a second operand), online softmax in base 2 with
+//    the per-row causal limit, normalisation once at the end.  V rows past the
+//    context are zeroed in shared memory before use (unwritten slots may hold
+//    NaN).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
