@@ -444,11 +444,15 @@ def run_gpu(args):
 
 def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode, fp8,
             seqs):
-    """Real decode steps through the C ABI with host buffers: each step appends
-    one token per sequence in the host allocator, exports the tables into
-    pinned memory, copies them and the step's q / new K / new V to the device,
-    runs the append and the decode, and reads the output back.  (Copy-on-write
-    pairs cannot arise here: no sequence shares a partial block.)"""
+    """Real decode steps through the C ABI with host buffers.  Each step: the
+    host allocator appends one token per sequence (pa_append_batch) and
+    exports the tables (pa_export) into pinned memory; then one CUDA graph
+    replay copies the step's q / new K / new V / tables / lengths / slots to
+    the device, runs the append and the decode and copies the output back;
+    the host waits for it.  The graph was captured once through the same C-ABI
+    calls, as a serving loop would (the decode's max_context_len is the bound
+    after all steps).  Copy-on-write pairs cannot arise here: no sequence
+    shares a partial block."""
     import numpy as np
     import torch
 
@@ -471,47 +475,47 @@ def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, de
     d_tbl = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
     d_lens = torch.empty(B, dtype=torch.int32, device=dev)
     d_slots = torch.empty(B, dtype=torch.int64, device=dev)
-    d_pairs = torch.empty((B, 2), dtype=torch.int32, device=dev)
     d_out = torch.empty_like(q)
     ids = list(seqs)
     n_tbl, n_lens, n_slots, n_pairs = (h_tbl.numpy(), h_lens.numpy(), h_slots.numpy(),
                                       h_pairs.numpy())
-    h2d = d2h = 0
+    ins = ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tbl, h_tbl), (d_lens, h_lens),
+           (d_slots, h_slots))
+    h2d = sum(src.numel() * src.element_size() for _, src in ins)
+    d2h = d_out.numel() * d_out.element_size()
+    max_len_bound = int(w.context_lens.max()) + 1 + steps
+    # capture (nothing runs); the tables are exported once so that every buffer holds valid data
+    alloc.export(ids, max_blocks, n_tbl, n_lens)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
+        append(d_kn, d_vn, d_slots)
+        decode(d_q, d_tbl, d_lens, max_len_bound, d_out)
+        h_out.copy_(d_out, non_blocking=True)
     kv_total = 0
-    launches = 0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
         _, pairs = alloc.append_batch(ids, n_slots, n_pairs)
+        if len(pairs):
+            raise RuntimeError("unexpected copy-on-write pairs in the e2e leg")
         alloc.export(ids, max_blocks, n_tbl, n_lens)
-        with torch.cuda.stream(stream):
-            for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tbl, h_tbl),
-                             (d_lens, h_lens), (d_slots, h_slots)):
-                dst.copy_(src, non_blocking=True)
-                h2d += src.numel() * src.element_size()
-            if len(pairs):
-                if fp8:
-                    raise RuntimeError("unexpected copy-on-write pairs in the e2e leg")
-                d_pairs[: len(pairs)].copy_(h_pairs[: len(pairs)], non_blocking=True)
-                h2d += len(pairs) * 8
-                binding.pa_copy_blocks([kc], [vc], d_pairs[: len(pairs)], stream)
-                launches += 1
-            append(d_kn, d_vn, d_slots)
-            decode(d_q, d_tbl, d_lens, int(n_lens.max()), d_out)
-            launches += 2
-            h_out.copy_(d_out, non_blocking=True)
-            d2h += d_out.numel() * d_out.element_size()
+        with torch.cuda.stream(stream):      # replay() launches on the current stream
+            graph.replay()
         stream.synchronize()
         kv_total += kv_bytes(n_lens, Hkv, d, fp8=fp8)
+    torch.cuda.synchronize()
     t1 = time.perf_counter()
     if binding.pa_check_device_errors(stream):
         raise RuntimeError("device error flags set in the e2e leg")
     return {"value": round(kv_total / (t1 - t0) / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
-            "gpu_launches": launches,
-            "includes": "host append_batch + export, pinned H2D of q/k_new/v_new/tables/lens/"
-                        "slots, reshape_and_cache, decode, D2H of out, stream sync per step"}
+            "gpu_launches": 2 * steps,
+            "includes": "host pa_append_batch + pa_export into pinned memory, then one CUDA-graph "
+                        "replay of: pinned H2D of q/k_new/v_new/tables/lens/slots, "
+                        "reshape_and_cache, decode, D2H of out; stream sync per step"}
 
 
 def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):
