@@ -139,6 +139,19 @@ def test_repeat_reuses_workspace_and_is_deterministic():
     assert_close(a.cpu(), _ref(kc, vc, tbl, ln, qs, q, 0.09), "split items")
 
 
+@pytest.mark.parametrize("H,Hkv,d,dtype", [(8, 1, 64, torch.float16), (32, 2, 128, torch.float16),
+                                           (16, 16, 64, torch.bfloat16)])
+def test_split_items_every_instantiation(H, Hkv, d, dtype):
+    """Few tiles over long contexts: each tile is shared by several CTAs and
+    merged from partials, for head dims 64 / 128, f16 / bf16, G = 1 .. 16."""
+    lens = [30000, 12000, 7]
+    qlens = [3, 9, 7]
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, H, Hkv, d, 32, dtype, 27 + H)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d)), "split items")
+
+
 def test_more_queries_than_context_is_flagged_and_skipped():
     kc, vc, tbl, ln, qs, q = _setup([10, 20], [3, 5], 4, 2, 64, 16, torch.float16, 26)
     ln_bad = ln.copy()
