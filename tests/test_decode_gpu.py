@@ -209,3 +209,30 @@ def test_single_long_pair_split_over_every_cta_d64():
     assert binding.pa_check_device_errors() == 0
     assert_close(out.cpu(), oracle_decode(w, host["q"], host["k_cache"], host["v_cache"], tbl,
                                           lens), "long-d64")
+
+
+@pytest.mark.parametrize("H,Hkv,d,dtype", [(32, 2, 128, torch.bfloat16), (8, 8, 64, torch.float16)])
+def test_max_batch(H, Hkv, d, dtype):
+    """The largest batch one call takes: 4096 short sequences, empty ones
+    among them, G = 16 and G = 1."""
+    B = 4096
+    lens = np.random.default_rng(H + d).integers(0, 48, size=B)
+    w, host, tbl, lens = _custom(B, H, Hkv, d, 16, lens, dtype=dtype, seed=H + d)
+    run = GpuRun(w, host)
+    out = run.decode(tbl, lens)
+    assert binding.pa_check_device_errors() == 0
+    ref = oracle_decode(w, host["q"], host["k_cache"], host["v_cache"], tbl, lens)
+    assert_close(out.cpu(), ref, "B=4096 G=%d" % (H // Hkv))
+    assert torch.count_nonzero(out[np.where(lens == 0)[0]]).item() == 0
+
+
+def test_batch_above_the_limit_is_refused():
+    w, host, tbl, lens = _custom(4097, 4, 4, 64, 16, np.ones(4097, np.int32), seed=3)
+    run = GpuRun(w, host)
+    run.out.fill_(7.0)
+    with pytest.raises(binding.PaError) as e:
+        run.decode(tbl, lens)
+    assert binding.STATUS_NAMES[e.value.status] == "PA_ERR_UNSUPPORTED"
+    torch.cuda.synchronize()
+    assert bool((run.out == 7.0).all())                    # nothing was launched
+    assert binding.pa_check_device_errors() == 0

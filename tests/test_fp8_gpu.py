@@ -286,3 +286,14 @@ def test_decode_fp8_rejects_head_dim_64():
     ws = torch.zeros(binding.pa_decode_workspace_size(1, 2, 64), dtype=torch.uint8, device="cuda")
     with pytest.raises(binding.PaError):
         binding.pa_decode_fp8(q, kc, kc, ks, ks, tbl, n, 1, 0.125, torch.empty_like(q), ws)
+
+
+def test_decode_fp8_max_batch():
+    """4096 short sequences (the largest batch one call takes), G = 8."""
+    lens = np.random.default_rng(12).integers(0, 40, size=4096)
+    q, c, run, tbl, n = _quantised_through_append(4096, 16, 2, 16, torch.bfloat16, lens, 12)
+    scale = 1.0 / math.sqrt(128)
+    out = run.decode(tbl, n, scale)
+    assert binding.pa_check_device_errors() == 0
+    _same_cache(run, c)
+    assert_close(out.cpu(), _oracle_decode(q, c, tbl, n, scale), "fp8 B=4096")

@@ -161,3 +161,25 @@ def test_more_queries_than_context_is_flagged_and_skipped():
     assert torch.isnan(out[:3].float()).all()     # sequence 0 untouched
     ref = _ref(kc, vc, tbl, ln, qs, q, 0.125)
     assert_close(out[3:].cpu(), ref[3:], "the valid sequence")
+
+
+def test_max_batch():
+    """4096 sequences (the largest batch one call takes), each verifying 0 to
+    3 tokens over a short context."""
+    B = 4096
+    rng = np.random.default_rng(31)
+    lens = rng.integers(1, 60, size=B)
+    qlens = np.minimum(lens, rng.integers(0, 4, size=B))
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, 8, 2, 128, 16, torch.bfloat16, 31)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128)), "B=4096")
+
+
+def test_batch_above_the_limit_is_refused():
+    lens = [2] * 4097
+    kc, vc, tbl, ln, qs, q = _setup(lens, [1] * 4097, 4, 2, 64, 16, torch.float16, 32)
+    with pytest.raises(binding.PaError) as e:
+        _gpu(kc, vc, tbl, ln, qs, q, 0.125)
+    assert binding.STATUS_NAMES[e.value.status] == "PA_ERR_UNSUPPORTED"
+    assert binding.pa_check_device_errors() == 0
