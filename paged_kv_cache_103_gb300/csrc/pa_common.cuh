@@ -24,6 +24,16 @@ __device__ __forceinline__ void raise_error(unsigned int* word, unsigned int bit
     atomicOr(word, bits);
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

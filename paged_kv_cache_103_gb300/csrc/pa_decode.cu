@@ -172,20 +172,6 @@ __device__ __forceinline__ bool wait_flag(const int* flag, int value, uint64_t l
     }
 }
 
-// Folds the softmax state (m2, l2) into (m, l): row maxima in base 2, sums
-// relative to them.  An empty state has m = -inf.
-__device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
-    if (m2 == -INFINITY) return;
-    if (m == -INFINITY) {
-        m = m2;
-        l = l2;
-        return;
-    }
-    const float mn = fmaxf(m, m2);
-    l = l * pa::fast_exp2(m - mn) + l2 * pa::fast_exp2(m2 - mn);
-    m = mn;
-}
-
 __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -551,96 +537,70 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             ps[kMaxG + t] = rinfo[kMaxG + t];
         }
         // Publish: the group barrier orders every thread's stores before thread
-        // 0's fence, whose release covers them (cumulativity); the ticket names
-        // the pair's last CTA.
+        // 0's release (cumulativity); the acquire-release ticket names the
+        // pair's last CTA and, for that CTA, acquires every other CTA's partial.
         sync();
         if (t == 0) {
-            __threadfence();
             int32_t* ctr = p.counters + (int64_t)sg.i * Hkv + sg.g;
-            const int prev = atomicAdd(ctr, 1);
+            const int prev = pa::atomic_add_acq_rel_gpu(ctr, 1);
             const int last = prev == (int)(c_last - c_first);
-            if (last) {
-                atomicExch(ctr, 0);
-                __threadfence();
-            }
+            if (last) atomicExch(ctr, 0);   // ready for the next launch
             *flag = last;
         }
         sync();
         if (!*flag) return;
-        // Last CTA of the pair: merge the n_cov partials.  Each thread folds the
-        // (m, l) of a strided subset of partials for every row, then warps, then
-        // (for four warps) the warps through shared memory.
+        // Last CTA of the pair: each thread folds, for its 4 output values, the
+        // ncov partials (m_c, l_c, O_c) eight at a time (all eight loads in
+        // flight at once): M = max m_c, out = sum 2^(m_c - M) O_c / sum
+        // 2^(m_c - M) l_c.
         const int ncov = (int)(c_last - c_first + 1);
         // CTA c > c_first starts inside the pair (its first slot); c_first
         // uses its first slot only if its share starts there.
         const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == sg.a ? 0 : 1);
-        float mr[kMaxG], lr[kMaxG];
-#pragma unroll
-        for (int r = 0; r < kMaxG; ++r) {
-            mr[r] = -INFINITY;
-            lr[r] = 0.f;
-        }
-        for (int c = t; c < ncov; c += nthr) {
-            const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-#pragma unroll
-            for (int r = 0; r < kMaxG; ++r)
-                if (r < G) lse_combine(mr[r], lr[r], __ldcg(q + r), __ldcg(q + kMaxG + r));
-        }
-#pragma unroll
-        for (int r = 0; r < kMaxG; ++r) {
-            if (r >= G) break;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, mr[r], off);
-                const float l2 = __shfl_xor_sync(0xffffffffu, lr[r], off);
-                lse_combine(mr[r], lr[r], m2, l2);
-            }
-            if (nthr > 32) {
-                if (lane == 0) {  // sm / sl are free again: reuse them per warp
-                    sm[warp * kMaxG + r] = mr[r];
-                    sl[warp * kMaxG + r] = lr[r];
-                }
-            } else if (lane == r) {
-                rinfo[r] = mr[r];
-                rinfo[kMaxG + r] = 1.f / lr[r];
-            }
-        }
-        if (nthr > 32) {
-            sync();
-            if (t < G) {
-                float M = -INFINITY, Lsum = 0.f;
-                for (int w = 0; w < nthr / 32; ++w)
-                    lse_combine(M, Lsum, sm[w * kMaxG + t], sl[w * kMaxG + t]);
-                rinfo[t] = M;
-                rinfo[kMaxG + t] = 1.f / Lsum;
-            }
-        }
-        sync();
-        // Per-partial factors 2^(m_c - M) / L, staged in `so` (its W * G * D
-        // floats are free now) when they fit, else recomputed.
-        const bool staged = ncov <= kConsumerWarps * D;
-        for (int e = t; staged && e < ncov * G; e += nthr) {
-            const int c = e / G, r = e - c * G;
-            const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-            so[e] = pa::fast_exp2(__ldcg(q + r) - rinfo[r]) * rinfo[kMaxG + r];
-        }
-        sync();
         for (int e = t; e < G * D / 4; e += nthr) {
             const int r = e / (D / 4), d4 = (e - r * (D / 4)) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int c = 0; c < ncov; ++c) {
-                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-                const float f = staged ? so[c * G + r]
-                                       : pa::fast_exp2(__ldcg(q + r) - rinfo[r]) * rinfo[kMaxG + r];
-                const float4 ov =
-                    __ldcg(reinterpret_cast<const float4*>(q + 2 * kMaxG + r * D + d4));
-                v.x += f * ov.x;
-                v.y += f * ov.y;
-                v.z += f * ov.z;
-                v.w += f * ov.w;
+            float M = -INFINITY, Ls = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < ncov; c0 += 8) {
+                float pm[8], pl[8];
+                float4 po[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j;
+                    if (c < ncov) {
+                        const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+                        pm[j] = __ldcg(q + r);
+                        pl[j] = __ldcg(q + kMaxG + r);
+                        po[j] = __ldcg(reinterpret_cast<const float4*>(q + 2 * kMaxG + r * D + d4));
+                    } else {
+                        pm[j] = -INFINITY;
+                        pl[j] = 0.f;
+                        po[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float Mb = M;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) Mb = fmaxf(Mb, pm[j]);
+                if (Mb == -INFINITY) continue;
+                const float a = pa::fast_exp2(M - Mb);   // 0 while M = -inf
+                Ls *= a;
+                acc.x *= a;
+                acc.y *= a;
+                acc.z *= a;
+                acc.w *= a;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float f = pa::fast_exp2(pm[j] - Mb);
+                    Ls += f * pl[j];
+                    acc.x += f * po[j].x;
+                    acc.y += f * po[j].y;
+                    acc.z += f * po[j].z;
+                    acc.w += f * po[j].w;
+                }
+                M = Mb;
             }
-            store4(r, d4, v);
+            const float inv = 1.f / Ls;
+            store4(r, d4, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
         }
     };
 

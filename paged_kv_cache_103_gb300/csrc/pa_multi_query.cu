@@ -569,40 +569,65 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                 ps[kRows * D + kRows + row] = l_run[h2];
             }
         }
+        // Publish: __syncwarp orders the lanes' stores before lane 0's release
+        // (cumulativity); the acquire-release ticket names the last CTA and,
+        // for it, acquires the other CTAs' partials.
         __syncwarp();
         int last = 0;
         if (lane == 0) {
-            __threadfence();
             int32_t* ctr = p.counters + (int64_t)sg.item * kWarps + warp;
-            last = atomicAdd(ctr, 1) == (int)(c_last - c_first);
-            if (last) {
-                atomicExch(ctr, 0);
-                __threadfence();
-            }
+            last = pa::atomic_add_acq_rel_gpu(ctr, 1) == (int)(c_last - c_first);
+            if (last) atomicExch(ctr, 0);   // ready for the next launch
         }
         if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        __syncwarp();
         const int ncov = (int)(c_last - c_first + 1);
         const int64_t slot0 = 2 * c_first + (cta_begin(c_first, W, C) == sg.a ? 0 : 1);
+        // Each lane folds, for its 4 output values, the ncov partials
+        // (m_c, l_c, O_c) eight at a time with all eight loads in flight.
         for (int e = lane; e < 16 * (D / 4); e += 32) {
             const int row = warp * 16 + e / (D / 4), d4 = (e % (D / 4)) * 4;
             if (row >= nrows) continue;
-            float M = -INFINITY;
-            for (int cc = 0; cc < ncov; ++cc) {
-                const float* q = p.partials + (cc ? 2 * (c_first + cc) : slot0) * kSlotFloats;
-                M = fmaxf(M, __ldcg(q + kRows * D + row));
-            }
-            const float msafe = M == -INFINITY ? 0.f : M;
-            float Ls = 0.f;
+            float M = -INFINITY, Ls = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc = 0; cc < ncov; ++cc) {
-                const float* q = p.partials + (cc ? 2 * (c_first + cc) : slot0) * kSlotFloats;
-                const float f = pa::fast_exp2(__ldcg(q + kRows * D + row) - msafe);
-                Ls += f * __ldcg(q + kRows * D + kRows + row);
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(q + row * D + d4));
-                acc.x += f * v.x;
-                acc.y += f * v.y;
-                acc.z += f * v.z;
-                acc.w += f * v.w;
+            for (int c0 = 0; c0 < ncov; c0 += 8) {
+                float pm[8], pl[8];
+                float4 po[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int cc = c0 + j;
+                    if (cc < ncov) {
+                        const float* q =
+                            p.partials + (cc ? 2 * (c_first + cc) : slot0) * kSlotFloats;
+                        pm[j] = __ldcg(q + kRows * D + row);
+                        pl[j] = __ldcg(q + kRows * D + kRows + row);
+                        po[j] = __ldcg(reinterpret_cast<const float4*>(q + row * D + d4));
+                    } else {
+                        pm[j] = -INFINITY;
+                        pl[j] = 0.f;
+                        po[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float Mb = M;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) Mb = fmaxf(Mb, pm[j]);
+                if (Mb == -INFINITY) continue;   // rows with no key so far
+                const float a = pa::fast_exp2(M - Mb);   // 0 while M = -inf
+                Ls *= a;
+                acc.x *= a;
+                acc.y *= a;
+                acc.z *= a;
+                acc.w *= a;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float f = pa::fast_exp2(pm[j] - Mb);
+                    Ls += f * pl[j];
+                    acc.x += f * po[j].x;
+                    acc.y += f * po[j].y;
+                    acc.z += f * po[j].z;
+                    acc.w += f * po[j].w;
+                }
+                M = Mb;
             }
             const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
             const int32_t ra = row0 + row;
