@@ -506,16 +506,27 @@ def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, de
         decode(d_q, d_tbl, d_lens, max_len_bound, d_out)
         h_out.copy_(d_out, non_blocking=True)
     kv_total = 0
+    # host-side time per phase, summed over the steps (perf_counter)
+    phase = {"append_batch": 0.0, "export": 0.0, "replay": 0.0, "wait": 0.0}
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
+        ta = time.perf_counter()
         _, pairs = alloc.append_batch(ids, n_slots, n_pairs)
         if len(pairs):
             raise RuntimeError("unexpected copy-on-write pairs in the e2e leg")
+        tb = time.perf_counter()
         alloc.export(ids, max_blocks, n_tbl, n_lens)
+        tc = time.perf_counter()
         with torch.cuda.stream(stream):      # replay() launches on the current stream
             graph.replay()
+        td = time.perf_counter()
         stream.synchronize()
+        te = time.perf_counter()
+        phase["append_batch"] += tb - ta
+        phase["export"] += tc - tb
+        phase["replay"] += td - tc
+        phase["wait"] += te - td
         kv_total += kv_bytes(n_lens, Hkv, d, fp8=fp8)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
@@ -524,6 +535,7 @@ def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, de
     return {"value": round(kv_total / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
+            "host_us_per_step": {k: round(v * 1e6 / steps, 1) for k, v in phase.items()},
             "gpu_launches": 2 * steps,
             "includes": "host pa_append_batch + pa_export into pinned memory, then one CUDA-graph "
                         "replay of: pinned H2D of q/k_new/v_new/tables/lens/slots, "
