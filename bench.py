@@ -404,8 +404,8 @@ def run_gpu(args):
     peak, peak_kind = load_peak()
 
     # ---- e2e leg through the C ABI: host allocator step, pinned H2D, kernels, D2H
-    e2e = run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode,
-                  fp8, seqs)
+    e2e = run_e2e(args, w, host, alloc, kc, vc, ks if fp8 else None, vs if fp8 else None,
+                  stream, max_blocks, fp8, seqs)
 
     l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9) if not flush_l2
                else "L2 flushed between steps (512 MiB write + read outside the timed kernels; %.3f GB "
@@ -454,92 +454,52 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, host, alloc, q, kc, vc, stream, dev, max_blocks, append, decode, fp8,
-            seqs):
-    """Real decode steps through the C ABI with host buffers.  Each step: the
-    host allocator appends one token per sequence (pa_append_batch) and
-    exports the tables (pa_export) into pinned memory; then one CUDA graph
-    replay copies the step's q / new K / new V / tables / lengths / slots to
-    the device, runs the append and the decode and copies the output back;
-    the host waits for it.  The graph was captured once through the same C-ABI
-    calls, as a serving loop would (the decode's max_context_len is the bound
-    after all steps).  Copy-on-write pairs cannot arise here: no sequence
-    shares a partial block."""
+def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs):
+    """Real decode steps through the C ABI with host buffers, one call per
+    step: pa_step_run appends one token per sequence with the host allocator
+    (pa_append_batch), exports the tables (pa_export) into the executor's
+    pinned staging buffer, then replays the executor's CUDA graph -- one
+    host->device copy of q / new K / new V / slots / tables / lengths, the
+    append, the decode, one device->host copy of the output -- and waits for
+    it.  The inputs are written into the pinned staging once (the same
+    synthetic rows every step); each step still copies them to the device.
+    Copy-on-write cannot arise here: no sequence shares a partial block."""
     import numpy as np
     import torch
 
     from paged_kv_cache_103_gb300 import binding
 
     steps = min(args.steps, args.e2e_extra)
-    B, H, Hkv, d = w.B, w.H, w.Hkv, w.d
-    pin = dict(pin_memory=True)
-    h_q = host["q"].clone().pin_memory()
-    h_kn = host["k_new"].clone().pin_memory()
-    h_vn = host["v_new"].clone().pin_memory()
-    h_tbl = torch.empty((B, max_blocks), dtype=torch.int32, **pin)
-    h_lens = torch.empty(B, dtype=torch.int32, **pin)
-    h_slots = torch.empty(B, dtype=torch.int64, **pin)
-    h_pairs = torch.empty((B, 2), dtype=torch.int32, **pin)
-    h_out = torch.empty_like(h_q, **pin)
-    d_q = torch.empty_like(q)
-    d_kn = torch.empty((B, Hkv, d), dtype=q.dtype, device=dev)
-    d_vn = torch.empty_like(d_kn)
-    d_tbl = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
-    d_lens = torch.empty(B, dtype=torch.int32, device=dev)
-    d_slots = torch.empty(B, dtype=torch.int64, device=dev)
-    d_out = torch.empty_like(q)
-    ids = list(seqs)
-    n_tbl, n_lens, n_slots, n_pairs = (h_tbl.numpy(), h_lens.numpy(), h_slots.numpy(),
-                                      h_pairs.numpy())
-    ins = ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tbl, h_tbl), (d_lens, h_lens),
-           (d_slots, h_slots))
-    h2d = sum(src.numel() * src.element_size() for _, src in ins)
-    d2h = d_out.numel() * d_out.element_size()
-    max_len_bound = int(w.context_lens.max()) + 1 + steps
-    # capture (nothing runs); the tables are exported once so that every buffer holds valid data
-    alloc.export(ids, max_blocks, n_tbl, n_lens)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for dst, src in ins:
-            dst.copy_(src, non_blocking=True)
-        append(d_kn, d_vn, d_slots)
-        decode(d_q, d_tbl, d_lens, max_len_bound, d_out)
-        h_out.copy_(d_out, non_blocking=True)
+    B, H, Hkv, d, bs = w.B, w.H, w.Hkv, w.d, w.block_size
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    step = binding.Step(alloc, B, H, Hkv, d, max_blocks, max_blocks * bs, kc, vc, w.scale,
+                        k_scale=ks if fp8 else None, v_scale=vs if fp8 else None, dtype=dt)
+    step.q.copy_(host["q"])
+    step.k_new.copy_(host["k_new"])
+    step.v_new.copy_(host["v_new"])
+    ids = np.asarray(seqs, dtype=np.int64)
+    h2d = step.layout["in_bytes"]
+    d2h = step.out.numel() * step.out.element_size()
     kv_total = 0
-    # host-side time per phase, summed over the steps (perf_counter)
-    phase = {"append_batch": 0.0, "export": 0.0, "replay": 0.0, "wait": 0.0}
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        ta = time.perf_counter()
-        _, pairs = alloc.append_batch(ids, n_slots, n_pairs)
-        if len(pairs):
-            raise RuntimeError("unexpected copy-on-write pairs in the e2e leg")
-        tb = time.perf_counter()
-        alloc.export(ids, max_blocks, n_tbl, n_lens)
-        tc = time.perf_counter()
-        with torch.cuda.stream(stream):      # replay() launches on the current stream
-            graph.replay()
-        td = time.perf_counter()
-        stream.synchronize()
-        te = time.perf_counter()
-        phase["append_batch"] += tb - ta
-        phase["export"] += tc - tb
-        phase["replay"] += td - tc
-        phase["wait"] += te - td
-        kv_total += kv_bytes(n_lens, Hkv, d, fp8=fp8)
-    torch.cuda.synchronize()
+        step.run(ids, stream)
+        kv_total += kv_bytes(step.context_lens.numpy(), Hkv, d, fp8=fp8)
     t1 = time.perf_counter()
     if binding.pa_check_device_errors(stream):
         raise RuntimeError("device error flags set in the e2e leg")
+    if not torch.isfinite(step.out.float()).all():
+        raise RuntimeError("non-finite output in the e2e leg")
+    step.close()
     return {"value": round(kv_total / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
-            "host_us_per_step": {k: round(v * 1e6 / steps, 1) for k, v in phase.items()},
             "gpu_launches": 2 * steps,
-            "includes": "host pa_append_batch + pa_export into pinned memory, then one CUDA-graph "
-                        "replay of: pinned H2D of q/k_new/v_new/tables/lens/slots, "
-                        "reshape_and_cache, decode, D2H of out; stream sync per step"}
+            "includes": "one pa_step_run per step (C ABI): host pa_append_batch + pa_export into "
+                        "pinned staging, then the library's CUDA graph: one pinned H2D of "
+                        "q/k_new/v_new/slots/tables/lens, reshape_and_cache%s, decode%s, one D2H "
+                        "of out; waits for the step" % (("_fp8", "_fp8") if fp8 else ("", ""))}
 
 
 def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):

@@ -437,6 +437,72 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
                                    int32_t block_size, int32_t num_blocks, float scale,
                                    pa_dtype dtype, void* out, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Decode step executor: one call per step for one layer's whole hot path --
+ * the block manager's bookkeeping on the host ([P1] section 3.2: a slot for
+ * each new token, block tables for the kernel; [P3] section 3.3: a shared
+ * last block is copied before it is written), one host->device copy of the
+ * step's inputs and tables, pa_copy_blocks when copy-on-write arises,
+ * pa_reshape_and_cache, pa_decode and one device->host copy of the output
+ * (pa_reshape_and_cache_fp8 and pa_decode_fp8 over an FP8 cache).
+ * The copies and the two kernels are captured once, at creation, into a CUDA
+ * graph owned by the executor and replayed every step.  The caller owns the
+ * staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
+ * torch tensor) and a device buffer, both pa_step_layout.total bytes and
+ * 256-byte aligned, laid out as pa_step_layout gives.  The caller writes a
+ * step's q [B][H][d] and new k / v [B][Hkv][d] (dtype) into the host buffer at
+ * offsets q, k_new, v_new; the executor writes slot_mapping, block_tables,
+ * context_lens and cow_pairs there itself and leaves the output [B][H][d] at
+ * offset out.  The paper has no counterpart to the executor object; it exists
+ * so that a serving loop pays one launch per step.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_step pa_step;
+
+typedef struct pa_step_desc {
+    int32_t B;                /* sequences per step, 1 .. 4096 */
+    int32_t H, Hkv, d;        /* query heads, KV heads, head dim (64 or 128) */
+    int32_t block_size;       /* 8, 16 or 32 */
+    int32_t num_blocks;       /* blocks of the cache pool */
+    int32_t max_blocks;       /* table width exported every step */
+    int32_t max_context_len;  /* bound of every context length, <= max_blocks * block_size */
+    pa_dtype dtype;           /* of q, k_new, v_new, the output and a 16-bit cache */
+    float scale;              /* attention scale, 1/sqrt(d) for the pages' formula */
+    int32_t fp8;              /* 1: E4M3 cache with per-(token, KV head) scales (d = 128) */
+} pa_step_desc;
+
+typedef struct pa_step_layout {  /* byte offsets into both staging buffers */
+    size_t q, k_new, v_new, slot_mapping, block_tables, context_lens;
+    size_t in_bytes;             /* [0, in_bytes) is copied host->device each step */
+    size_t cow_pairs, out;       /* copy-on-write pairs [B][2] int32; output [B][H][d] */
+    size_t total;
+} pa_step_layout;
+
+/* Layout of the staging buffers for desc; PA_ERR_INVALID for a bad desc. */
+PA_API pa_status pa_step_layout_get(const pa_step_desc* desc, pa_step_layout* out);
+
+/* Creates an executor for one layer's caches k_cache / v_cache (device,
+ * [num_blocks][block_size][Hkv][d], dtype or, with fp8, uint8 codes plus
+ * k_scale / v_scale [num_blocks][Hkv][block_size] fp32; the scales are NULL
+ * otherwise) and the allocator alloc (all must outlive it).  workspace (device, >= pa_decode_workspace_size(B, H, d) bytes, zeroed
+ * once) is the decode's.  Captures the graph on a private stream; nothing
+ * runs.  PA_ERR_INVALID for bad arguments or misaligned staging. */
+PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale, void* host_stage,
+                                void* dev_stage, void* workspace, size_t ws_bytes,
+                                pa_step** out);
+
+/* One decode step for the B sequences seq_ids (host): appends one token to
+ * each (pa_append_batch), issues the copy-on-write copies that needs, exports
+ * the tables, launches the graph on `stream` and waits for it, so the output
+ * is in the host buffer on return.  A sequence whose length after the append
+ * would exceed max_context_len or max_blocks * block_size returns
+ * PA_ERR_BOUNDS before anything changes; allocator errors are those of
+ * pa_append_batch (all or nothing).  The staging buffers are reused: write
+ * the next step's inputs only after this call returned. */
+PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream);
+
+PA_API void pa_step_destroy(pa_step* s);
+
 /* Synchronises `stream`, returns the current device's error word in *flags
  * (host, nullable) and clears it.  Returns PA_ERR_BOUNDS or PA_ERR_TIMEOUT if
  * any bit was set, PA_ERR_CUDA if the stream reports an error, else PA_OK. */

@@ -39,6 +39,20 @@ class SwapStats(ctypes.Structure):
                 ("swapped_seqs", ctypes.c_int32)]
 
 
+class StepDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("max_context_len", ctypes.c_int32), ("dtype", ctypes.c_int),
+                ("scale", ctypes.c_float), ("fp8", ctypes.c_int32)]
+
+
+class StepLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("q", "k_new", "v_new", "slot_mapping",
+                                                "block_tables", "context_lens", "in_bytes",
+                                                "cow_pairs", "out", "total")]
+
+
 class PrefixStats(ctypes.Structure):
     _fields_ = [("lookups", ctypes.c_int64), ("hits", ctypes.c_int64),
                 ("registered", ctypes.c_int64), ("evicted", ctypes.c_int64),
@@ -86,6 +100,11 @@ SIGNATURES = {
                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                 _I32, _F32, _ST, _P, _P]),
+    "pa_step_layout_get": (_ST, [ctypes.POINTER(StepDesc), ctypes.POINTER(StepLayout)]),
+    "pa_step_create": (_ST, [ctypes.POINTER(StepDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                             ctypes.POINTER(_P)]),
+    "pa_step_run": (_ST, [_P, _P, _P]),
+    "pa_step_destroy": (None, [_P]),
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "pa_decode_grid_size": (_I32, []),
     "pa_selftest_wait_timeout": (_ST, [ctypes.c_uint32, _P]),
@@ -484,3 +503,85 @@ class Allocator:
         s = AllocStats()
         _check(self._lib.pa_alloc_stats_get(self._h, ctypes.byref(s)), "pa_alloc_stats_get")
         return {f: getattr(s, f) for f, _ in AllocStats._fields_}
+
+
+class Step:
+    """The decode step executor (``pa_step_*``) for one layer's caches.
+
+    Allocates its two staging buffers (pinned host, device) and the decode
+    workspace as torch tensors and exposes the host buffer's regions as
+    tensors: fill ``q``, ``k_new`` and ``v_new`` before each :meth:`run`; the
+    step's output is then in ``out``.  With ``k_scale``/``v_scale`` the caches
+    are FP8 codes (uint8) and ``dtype`` gives the 16-bit type of the inputs."""
+
+    def __init__(self, alloc: Allocator, B: int, H: int, Hkv: int, d: int, max_blocks: int,
+                 max_context_len: int, k_cache, v_cache, scale: float, k_scale=None,
+                 v_scale=None, dtype=None):
+        import torch
+        self._lib = load()
+        N, bs = int(k_cache.shape[0]), int(k_cache.shape[1])
+        if tuple(k_cache.shape) != (N, bs, Hkv, d) or v_cache.shape != k_cache.shape:
+            raise ValueError("caches must be [num_blocks, block_size, Hkv, d]")
+        fp8 = k_scale is not None
+        if fp8 and dtype not in (torch.float16, torch.bfloat16):
+            raise ValueError("an FP8 cache needs dtype, the 16-bit type of q and k/v_new")
+        dt = dtype if fp8 else k_cache.dtype
+        self.desc = StepDesc(B, H, Hkv, d, bs, N, max_blocks, max_context_len,
+                             PA_F16 if dt == torch.float16 else PA_BF16, scale, int(fp8))
+        lay = StepLayout()
+        _check(self._lib.pa_step_layout_get(ctypes.byref(self.desc), ctypes.byref(lay)),
+               "pa_step_layout_get")
+        self.layout = {f: getattr(lay, f) for f, _ in StepLayout._fields_}
+        dev = k_cache.device
+        # 256-byte alignment: over-allocate and take an aligned view
+        self._host_raw = torch.empty(lay.total + 256, dtype=torch.uint8, pin_memory=True)
+        self._dev_raw = torch.empty(lay.total + 256, dtype=torch.uint8, device=dev)
+        self.host = self._aligned(self._host_raw, lay.total)
+        self.dev = self._aligned(self._dev_raw, lay.total)
+        self.ws = torch.zeros(pa_decode_workspace_size(B, H, d), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
+        self._caches = (k_cache, v_cache, k_scale, v_scale)
+        self.alloc = alloc
+        self._h = ctypes.c_void_p()
+        _check(self._lib.pa_step_create(ctypes.byref(self.desc), alloc._h, _dev(k_cache),
+                                        _dev(v_cache),
+                                        _dev(k_scale, torch.float32) if fp8 else None,
+                                        _dev(v_scale, torch.float32) if fp8 else None,
+                                        self.host.data_ptr(), self.dev.data_ptr(),
+                                        self.ws.data_ptr(), self.ws.numel(),
+                                        ctypes.byref(self._h)), "pa_step_create")
+
+        def region(name, shape, dtype):
+            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+            off = self.layout[name]
+            return self.host[off: off + n].view(dtype).view(*shape)
+
+        self.q = region("q", (B, H, d), dt)
+        self.k_new = region("k_new", (B, Hkv, d), dt)
+        self.v_new = region("v_new", (B, Hkv, d), dt)
+        self.out = region("out", (B, H, d), dt)
+        self.slot_mapping = region("slot_mapping", (B,), torch.int64)
+        self.block_tables = region("block_tables", (B, max_blocks), torch.int32)
+        self.context_lens = region("context_lens", (B,), torch.int32)
+
+    @staticmethod
+    def _aligned(raw, n):
+        off = (-raw.data_ptr()) % 256
+        return raw[off: off + n]
+
+    def run(self, seq_ids, stream=None) -> None:
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        if ids.shape[0] != self.desc.B:
+            raise ValueError("the executor runs %d sequences per step" % self.desc.B)
+        _check(self._lib.pa_step_run(self._h, _np_ptr(ids), _stream_ptr(stream)), "pa_step_run")
+
+    def close(self):
+        if self._h:
+            self._lib.pa_step_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

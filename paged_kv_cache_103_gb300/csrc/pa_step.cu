@@ -1,0 +1,215 @@
+// Decode step executor: one C-ABI call per step runs the whole hot path of one
+// layer.  The host part is the block manager's per-step bookkeeping
+// ("LLM推理优化：vLLM PagedAttention深度解析与工程实践", section 3.2: a slot
+// per new token, block tables handed to the kernel; "vLLM 深度拆解：当大模型
+// 推理学会「分页注意力」", section 3.3: copy-on-write of a shared last block);
+// the device part is one host->device copy of the step's inputs and tables,
+// the append (pa_reshape_and_cache), the attention (pa_decode) and one
+// device->host copy of the output.  The device part is captured once into a CUDA graph and
+// replayed every step, so a step costs one graph launch instead of one launch
+// or copy call per operation.
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "pa.h"
+#include "pa_common.cuh"
+
+struct pa_step {
+    pa_step_desc desc;
+    pa_step_layout lay;
+    pa_allocator* alloc;
+    void* k_cache;
+    void* v_cache;
+    float* k_scale;       // FP8 caches only
+    float* v_scale;
+    unsigned char* host;  // pinned staging
+    unsigned char* dev;   // device staging
+    int64_t block_bytes;  // one block of one cache (codes for FP8)
+    cudaGraphExec_t exec;
+};
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool desc_ok(const pa_step_desc* d) {
+    return d && d->B > 0 && d->B <= 4096 && d->H > 0 && d->Hkv > 0 && d->H % d->Hkv == 0 &&
+           (d->d == 64 || d->d == 128) &&
+           (d->block_size == 8 || d->block_size == 16 || d->block_size == 32) &&
+           d->num_blocks > 0 && d->max_blocks > 0 && d->max_context_len > 0 &&
+           (int64_t)d->max_context_len <= (int64_t)d->max_blocks * d->block_size &&
+           (d->dtype == PA_F16 || d->dtype == PA_BF16) && (d->fp8 == 0 || d->fp8 == 1) &&
+           (d->fp8 == 0 || d->d == 128);
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API pa_status pa_step_layout_get(const pa_step_desc* d, pa_step_layout* out) {
+    if (!desc_ok(d) || !out) return PA_ERR_INVALID;
+    const size_t e = 2;
+    pa_step_layout L;
+    size_t at = 0;
+    L.q = at;
+    at = align256(at + (size_t)d->B * d->H * d->d * e);
+    L.k_new = at;
+    at = align256(at + (size_t)d->B * d->Hkv * d->d * e);
+    L.v_new = at;
+    at = align256(at + (size_t)d->B * d->Hkv * d->d * e);
+    L.slot_mapping = at;
+    at = align256(at + (size_t)d->B * sizeof(int64_t));
+    L.block_tables = at;
+    at = align256(at + (size_t)d->B * d->max_blocks * sizeof(int32_t));
+    L.context_lens = at;
+    at = align256(at + (size_t)d->B * sizeof(int32_t));
+    L.in_bytes = at;
+    L.cow_pairs = at;
+    at = align256(at + (size_t)d->B * 2 * sizeof(int32_t));
+    L.out = at;
+    at = align256(at + (size_t)d->B * d->H * d->d * e);
+    L.total = at;
+    *out = L;
+    return PA_OK;
+}
+
+PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale, void* host_stage,
+                                void* dev_stage, void* workspace, size_t ws_bytes,
+                                pa_step** out) {
+    if (!desc_ok(d) || !alloc || !k_cache || !v_cache || !host_stage || !dev_stage ||
+        !workspace || !out)
+        return PA_ERR_INVALID;
+    if (d->fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(host_stage) | reinterpret_cast<uintptr_t>(dev_stage)) & 255u)
+        return PA_ERR_INVALID;
+    if (ws_bytes < pa_decode_workspace_size(d->B, d->H, d->d)) return PA_ERR_INVALID;
+    *out = nullptr;
+    pa_step* s = new (std::nothrow) pa_step;
+    if (!s) return PA_ERR_OOM;
+    s->desc = *d;
+    pa_step_layout_get(d, &s->lay);
+    s->alloc = alloc;
+    s->k_cache = k_cache;
+    s->v_cache = v_cache;
+    s->k_scale = d->fp8 ? k_scale : nullptr;
+    s->v_scale = d->fp8 ? v_scale : nullptr;
+    s->host = static_cast<unsigned char*>(host_stage);
+    s->dev = static_cast<unsigned char*>(dev_stage);
+    s->block_bytes = (int64_t)d->block_size * d->Hkv * d->d * (d->fp8 ? 1 : 2);
+    s->exec = nullptr;
+
+    // One-time set-up of the device error word and SM count, outside the capture.
+    if (!pa::device_error_word() || !pa::device_sm_count()) {
+        delete s;
+        return PA_ERR_CUDA;
+    }
+    // The graph is captured on a private stream; it can be launched on any.
+    cudaStream_t cap = nullptr;
+    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
+        delete s;
+        return PA_ERR_CUDA;
+    }
+    const pa_step_layout& L = s->lay;
+    unsigned char* h = s->host;
+    unsigned char* g = s->dev;
+    pa_status st = PA_OK;
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+        st = PA_ERR_CUDA;
+    } else {
+        if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, cap) != cudaSuccess)
+            st = PA_ERR_CUDA;
+        const int64_t* slots = reinterpret_cast<const int64_t*>(g + L.slot_mapping);
+        const int32_t* tables = reinterpret_cast<const int32_t*>(g + L.block_tables);
+        const int32_t* lens = reinterpret_cast<const int32_t*>(g + L.context_lens);
+        if (st == PA_OK && d->fp8)
+            st = pa_reshape_and_cache_fp8(g + L.k_new, g + L.v_new, slots, d->B, k_cache, v_cache,
+                                          k_scale, v_scale, d->num_blocks, d->block_size, d->Hkv,
+                                          d->d, d->dtype, cap);
+        else if (st == PA_OK)
+            st = pa_reshape_and_cache(g + L.k_new, g + L.v_new, slots, d->B, k_cache, v_cache,
+                                      d->num_blocks, d->block_size, d->Hkv, d->d, d->dtype, cap);
+        if (st == PA_OK && d->fp8)
+            st = pa_decode_fp8(g + L.q, k_cache, v_cache, k_scale, v_scale, tables, d->max_blocks,
+                               lens, d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size,
+                               d->num_blocks, d->scale, d->dtype, g + L.out, workspace, ws_bytes,
+                               cap);
+        else if (st == PA_OK)
+            st = pa_decode(g + L.q, k_cache, v_cache, tables, d->max_blocks, lens,
+                           d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size,
+                           d->num_blocks, d->scale, d->dtype, g + L.out, workspace, ws_bytes, cap);
+        if (st == PA_OK &&
+            cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d->B * d->H * d->d * 2,
+                            cudaMemcpyDeviceToHost, cap) != cudaSuccess)
+            st = PA_ERR_CUDA;
+        // End the capture whatever happened, so the stream is usable again.
+        if (cudaStreamEndCapture(cap, &graph) != cudaSuccess && st == PA_OK) st = PA_ERR_CUDA;
+    }
+    if (st == PA_OK && cudaGraphInstantiate(&s->exec, graph, 0) != cudaSuccess) st = PA_ERR_CUDA;
+    if (graph) cudaGraphDestroy(graph);
+    cudaStreamDestroy(cap);
+    if (st != PA_OK) {
+        if (s->exec) cudaGraphExecDestroy(s->exec);
+        delete s;
+        return st;
+    }
+    *out = s;
+    return PA_OK;
+}
+
+PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream) {
+    if (!s || !seq_ids) return PA_ERR_INVALID;
+    const pa_step_desc& d = s->desc;
+    const pa_step_layout& L = s->lay;
+    // Every sequence must still fit the executor's bounds after the append;
+    // checked first so that a refusal changes nothing.
+    for (int32_t i = 0; i < d.B; ++i) {
+        int32_t len = 0, nb = 0;
+        const pa_status st = pa_seq_info(s->alloc, seq_ids[i], &len, &nb);
+        if (st != PA_OK) return st;
+        if (len + 1 > d.max_context_len ||
+            (len + d.block_size) / d.block_size > d.max_blocks)
+            return PA_ERR_BOUNDS;
+    }
+    int32_t ncow = 0;
+    int32_t* pairs = reinterpret_cast<int32_t*>(s->host + L.cow_pairs);
+    pa_status st = pa_append_batch(s->alloc, seq_ids, d.B,
+                                   reinterpret_cast<int64_t*>(s->host + L.slot_mapping), pairs,
+                                   &ncow);
+    if (st != PA_OK) return st;
+    st = pa_export(s->alloc, seq_ids, d.B, d.max_blocks,
+                   reinterpret_cast<int32_t*>(s->host + L.block_tables),
+                   reinterpret_cast<int32_t*>(s->host + L.context_lens));
+    if (st != PA_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (ncow > 0) {
+        // Copy-on-write before the step's append writes the new token.
+        int32_t* dpairs = reinterpret_cast<int32_t*>(s->dev + L.cow_pairs);
+        if (cudaMemcpyAsync(dpairs, pairs, (size_t)ncow * 2 * sizeof(int32_t),
+                            cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            return PA_ERR_CUDA;
+        void* kc = s->k_cache;
+        void* vc = s->v_cache;
+        st = pa_copy_blocks(&kc, &vc, 1, dpairs, ncow, s->block_bytes, d.num_blocks, cs);
+        if (st != PA_OK) return st;
+        if (d.fp8) {   // and the blocks' scales, [num_blocks][Hkv][block_size] fp32
+            void* ks = s->k_scale;
+            void* vs = s->v_scale;
+            st = pa_copy_blocks(&ks, &vs, 1, dpairs, ncow, (int64_t)d.Hkv * d.block_size * 4,
+                                d.num_blocks, cs);
+            if (st != PA_OK) return st;
+        }
+    }
+    if (cudaGraphLaunch(s->exec, cs) != cudaSuccess) return PA_ERR_CUDA;
+    return cudaStreamSynchronize(cs) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API void pa_step_destroy(pa_step* s) {
+    if (!s) return;
+    if (s->exec) cudaGraphExecDestroy(s->exec);
+    delete s;
+}
+
+}  // extern "C"

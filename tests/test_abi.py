@@ -90,3 +90,34 @@ def test_cache_op_host_checks(lib):
     assert lib.pa_reshape_and_cache(P, P, P, 1, P, P, 8, 16, 2, 64, 5, None) == 6   # dtype
     assert lib.pa_copy_blocks(None, None, 0, None, 0, 4096, 8, None) == 0
     assert lib.pa_copy_blocks(None, None, 1, None, 1, 4095, 8, None) == 1             # not x16
+
+
+def test_step_layout_and_argument_checks(lib):
+    """The executor's staging layout: every region 256-byte aligned, in the
+    documented order, large enough for its tensor; bad descriptions refused."""
+    d = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0)
+    L = binding.StepLayout()
+    assert lib.pa_step_layout_get(ctypes.byref(d), ctypes.byref(L)) == 0
+    order = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "out"]
+    sizes = {"q": 64 * 40 * 128 * 2, "k_new": 64 * 40 * 128 * 2, "v_new": 64 * 40 * 128 * 2,
+             "slot_mapping": 64 * 8, "block_tables": 64 * 128 * 4, "context_lens": 64 * 4,
+             "out": 64 * 40 * 128 * 2}
+    offs = [getattr(L, n) for n in order]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    for a, b in zip(order, order[1:]):
+        if a != "context_lens":
+            assert getattr(L, b) - getattr(L, a) >= sizes[a]
+    assert L.in_bytes == L.cow_pairs and L.in_bytes >= L.context_lens + sizes["context_lens"]
+    assert L.out - L.cow_pairs >= 64 * 2 * 4 and L.total >= L.out + sizes["out"]
+    for field, bad in [("max_context_len", 2049), ("d", 96), ("block_size", 64), ("B", 0),
+                       ("Hkv", 3), ("dtype", 7), ("fp8", 2)]:
+        e = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0)
+        setattr(e, field, bad)
+        assert lib.pa_step_layout_get(ctypes.byref(e), ctypes.byref(L)) == 1, field
+    # creation refuses missing buffers before touching the device
+    h = ctypes.c_void_p()
+    assert lib.pa_step_create(ctypes.byref(d), None, None, None, None, None, None, None, None,
+                              0, ctypes.byref(h)) == 1
+    e = binding.StepDesc(64, 40, 40, 64, 16, 5240, 128, 2048, 0, 0.088, 1)   # FP8 needs d 128
+    assert lib.pa_step_layout_get(ctypes.byref(e), ctypes.byref(L)) == 1
+    assert lib.pa_step_run(None, None, None) == 1
