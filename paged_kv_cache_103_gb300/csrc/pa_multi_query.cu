@@ -39,16 +39,25 @@
 
 namespace {
 
-constexpr int kRows = 64;           // query rows per item (4 warps x 16)
+constexpr int kMaxRows = 64;        // query rows per item at most (4 consumer warps x 16)
 constexpr int kKv = 64;             // keys per pipeline stage (a "chunk")
-constexpr int kWarps = 4;           // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kCtasPerSm = 2;
+constexpr int kMaxWarps = 4;        // consumer warps per CTA at most
 constexpr int kMaxStages = 8;
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxCtas = 512;
 constexpr int kMinChunksPerCta = 4;
-constexpr uint32_t kSmemBudget = 113 * 1024;
+
+// Launch shapes: NW consumer warps of 16 rows each plus one producer warp per
+// CTA.  Four run two CTAs per SM with 113 KB of shared memory each; three
+// (items of at most 48 rows, e.g. a few draft tokens of a GQA group, where a
+// fourth warp would idle) run three CTAs per SM with 75 KB each.
+template <int NW>
+struct Shape {
+    static constexpr int kRows = 16 * NW;
+    static constexpr int kThreads = (NW + 1) * 32;
+    static constexpr int kCtasPerSm = NW == 4 ? 2 : 3;
+    static constexpr uint32_t kSmemBudget = NW == 4 ? 113 * 1024 : 75 * 1024;
+};
 constexpr uint64_t kWaitLimitNs = 1ull << 30;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -62,6 +71,7 @@ struct Params {
     float* partials;     // [2 * kMaxCtas][kRows * (D + 2)] per-CTA partial rows
     unsigned int* err;
     int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages, items_cap;
+    int32_t rows;        // query rows per item: 16 per consumer warp
     float scale_log2;
 };
 
@@ -100,13 +110,15 @@ __device__ __forceinline__ SeqInfo seq_info(const Params& p, int32_t i, int32_t 
     s.n = clamp_len(__ldg(p.context_lens + i), max_len);
     s.q0 = __ldg(p.q_start + i);
     s.qlen = __ldg(p.q_start + i + 1) - s.q0;
-    s.tiles = (s.qlen < 0 || s.qlen > s.n) ? 0 : (s.qlen * p.G + kRows - 1) / kRows;
+    s.tiles = (s.qlen < 0 || s.qlen > s.n) ? 0 : (s.qlen * p.G + p.rows - 1) / p.rows;
     return s;
 }
 
-// Chunks tile t reads: keys 0 .. n - qlen + r_max, r_max its last query token.
-__device__ __forceinline__ int32_t tile_chunks(const SeqInfo& s, int32_t t, int32_t G) {
-    const int32_t rows_end = min((t + 1) * kRows, s.qlen * G);
+// Chunks tile t (of `rows` rows) reads: keys 0 .. n - qlen + r_max, r_max its
+// last query token.
+__device__ __forceinline__ int32_t tile_chunks(const SeqInfo& s, int32_t t, int32_t G,
+                                               int32_t rows) {
+    const int32_t rows_end = min((t + 1) * rows, s.qlen * G);
     const int32_t r_max = (rows_end - 1) / G;
     return (s.n - s.qlen + r_max + 1 + kKv - 1) / kKv;
 }
@@ -136,11 +148,11 @@ __device__ __forceinline__ Seg find_seg(const int32_t* prefix, const int32_t* ip
     const int32_t local = pos - prefix[lo_i];
     sg.g = local / per_g;
     const int32_t lg = local - sg.g * per_g;
-    int32_t t = 0, acc = 0, ct = tile_chunks(sg.s, 0, p.G);
+    int32_t t = 0, acc = 0, ct = tile_chunks(sg.s, 0, p.G, p.rows);
     while (acc + ct <= lg) {
         acc += ct;
         ++t;
-        ct = tile_chunks(sg.s, t, p.G);
+        ct = tile_chunks(sg.s, t, p.G, p.rows);
     }
     sg.t = t;
     sg.nc = ct;
@@ -163,11 +175,14 @@ __device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t W, int64_t C,
 
 // Two CTAs of five warps per SM put three warps on two of the four SM
 // sub-partitions, whose register files hold 16K registers each: 168 per
-// thread at most.
-template <int D, bool kBF16>
+// thread at most (three CTAs of four warps: three warps on every one).
+template <int D, bool kBF16, int NW>
 __global__ void __maxnreg__(168)
 multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const Params p) {
+    constexpr int kWarps = NW;
+    constexpr int kRows = Shape<NW>::kRows;
+    constexpr int kThreads = Shape<NW>::kThreads;
     constexpr uint32_t kHalves = D / 64;
     constexpr int kSlotFloats = kRows * (D + 2);
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
@@ -199,7 +214,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             tiles = s.tiles;
             chunks = 0;
-            for (int32_t t = 0; t < s.tiles; ++t) chunks += tile_chunks(s, t, G);
+            for (int32_t t = 0; t < s.tiles; ++t) chunks += tile_chunks(s, t, G, kRows);
         };
         int32_t lc = 0, lt = 0;
         for (int i = beg; i < end; ++i) {
@@ -677,42 +692,44 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int32_t rows, int32_t 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int choose_stages(int D, int B) {
+int choose_stages(int D, int B, uint32_t budget) {
     const Layout L0 = make_layout(D, B, 0);
-    if (L0.total >= kSmemBudget) return 0;
-    int s = (int)((kSmemBudget - L0.total) / L0.stage_bytes);
+    if (L0.total >= budget) return 0;
+    int s = (int)((budget - L0.total) / L0.stage_bytes);
     return s > kMaxStages ? kMaxStages : s;
 }
 
-// Upper bound of the work items: every sequence's 64-row tiles times Hkv.
+// Upper bound of the work items under either launch shape: every sequence's
+// tiles (of 48 rows, the smaller tile) times Hkv.
 int64_t items_cap(int32_t B, int32_t H, int32_t Hkv, int32_t max_q_len) {
     const int64_t G = H / Hkv;
-    return (int64_t)B * Hkv * (((int64_t)max_q_len * G + kRows - 1) / kRows);
+    const int64_t rows = Shape<3>::kRows;
+    return (int64_t)B * Hkv * (((int64_t)max_q_len * G + rows - 1) / rows);
 }
 
 size_t counters_bytes(int64_t items) {
-    return (((size_t)items * kWarps * sizeof(int32_t)) + 255) & ~size_t(255);
+    return (((size_t)items * kMaxWarps * sizeof(int32_t)) + 255) & ~size_t(255);
 }
 
 size_t partials_bytes(int32_t d) {
-    return (size_t)2 * kMaxCtas * kRows * (d + 2) * sizeof(float);
+    return (size_t)2 * kMaxCtas * kMaxRows * (d + 2) * sizeof(float);
 }
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, int NW>
 pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const Params& prm, size_t smem,
                  int grid, cudaStream_t stream) {
-    auto kern = multi_query_kernel<D, kBF16>;
+    auto kern = multi_query_kernel<D, kBF16, NW>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBudget);
-        if (attr_err == cudaSuccess)   // the largest shared-memory carve-out: two CTAs per SM
+                                        (int)Shape<NW>::kSmemBudget);
+        if (attr_err == cudaSuccess)   // the largest shared-memory carve-out
             attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                             100);
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(km, vm, prm);
+    kern<<<grid, Shape<NW>::kThreads, smem, stream>>>(km, vm, prm);
     return pa::cuda_status(cudaGetLastError());
 }
 
@@ -758,7 +775,11 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
         return PA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7u)
         return PA_ERR_INVALID;
-    const int stages = choose_stages(d, B);
+    // Items of at most 48 rows (a few query tokens of a group) run the
+    // three-warp shape when its smaller ring still holds two stages.
+    const int stages3 = choose_stages(d, B, Shape<3>::kSmemBudget);
+    const bool narrow = (int64_t)max_q_len * G <= Shape<3>::kRows && stages3 >= 2;
+    const int stages = narrow ? stages3 : choose_stages(d, B, Shape<4>::kSmemBudget);
     if (stages < 2) return PA_ERR_UNSUPPORTED;
     unsigned int* err = pa::device_error_word();
     const int sms = pa::device_sm_count();
@@ -789,16 +810,25 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
     prm.num_blocks = num_blocks;
     prm.stages = stages;
     prm.items_cap = (int32_t)cap;
+    prm.rows = narrow ? Shape<3>::kRows : Shape<4>::kRows;
     prm.scale_log2 = scale * kLog2e;
     const size_t smem = make_layout(d, B, stages).total;
-    int grid = sms * kCtasPerSm;
+    int grid = sms * (narrow ? Shape<3>::kCtasPerSm : Shape<4>::kCtasPerSm);
     if (grid > kMaxCtas) grid = kMaxCtas;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf = dtype == PA_BF16;
+    if (narrow) {
+        if (d == 128)
+            return bf ? launch<128, true, 3>(km, vm, prm, smem, grid, st)
+                      : launch<128, false, 3>(km, vm, prm, smem, grid, st);
+        return bf ? launch<64, true, 3>(km, vm, prm, smem, grid, st)
+                  : launch<64, false, 3>(km, vm, prm, smem, grid, st);
+    }
     if (d == 128)
-        return dtype == PA_BF16 ? launch<128, true>(km, vm, prm, smem, grid, st)
-                                : launch<128, false>(km, vm, prm, smem, grid, st);
-    return dtype == PA_BF16 ? launch<64, true>(km, vm, prm, smem, grid, st)
-                            : launch<64, false>(km, vm, prm, smem, grid, st);
+        return bf ? launch<128, true, 4>(km, vm, prm, smem, grid, st)
+                  : launch<128, false, 4>(km, vm, prm, smem, grid, st);
+    return bf ? launch<64, true, 4>(km, vm, prm, smem, grid, st)
+              : launch<64, false, 4>(km, vm, prm, smem, grid, st);
 }
 
 }  // extern "C"

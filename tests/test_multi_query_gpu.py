@@ -183,3 +183,18 @@ def test_batch_above_the_limit_is_refused():
         _gpu(kc, vc, tbl, ln, qs, q, 0.125)
     assert binding.STATUS_NAMES[e.value.status] == "PA_ERR_UNSUPPORTED"
     assert binding.pa_check_device_errors() == 0
+
+
+@pytest.mark.parametrize("H,Hkv,d,dtype,qlens", [(8, 1, 64, torch.float16, [6, 1, 5]),
+                                                 (16, 2, 128, torch.bfloat16, [6, 3, 6]),
+                                                 (28, 4, 128, torch.float16, [6, 6, 2]),
+                                                 (4, 4, 64, torch.bfloat16, [12, 1, 7])])
+def test_three_warp_shape_every_instantiation(H, Hkv, d, dtype, qlens):
+    """Items of at most 48 rows (max_q_len x G <= 48) run three consumer warps
+    and three CTAs per SM; long contexts split them between CTAs."""
+    assert max(qlens) * (H // Hkv) <= 48
+    lens = [25000, 9000, 7]
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, H, Hkv, d, 16, dtype, 40 + H + d)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d)), "three warps")
