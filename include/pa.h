@@ -329,7 +329,9 @@ PA_API size_t pa_decode_workspace_size(int32_t B, int32_t H, int32_t d);
 
 /* Zeroes a workspace (async on stream).  Call once after allocating it; every
  * pa_decode call leaves the counters at zero again.  A workspace serves one
- * stream at a time: pa_decode calls that overlap on the GPU must not share one. */
+ * stream at a time: pa_decode calls that overlap on the GPU must not share one.
+ * A call whose bounded waits ran out (PA_DEVERR_TIMEOUT) may leave counters
+ * set: zero the workspace again before reusing it. */
 PA_API pa_status pa_decode_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* Paged decode attention ([P1] section 二: attn = softmax(Q K^T / sqrt(d)) V;
@@ -378,7 +380,8 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
  *   max_q_len    (host) an upper bound of every qlen_i (sizes the workspace)
  *   workspace    (device) >= pa_multi_query_workspace_size(B, H, Hkv, d,
  *                max_q_len) bytes, zeroed once (pa_decode_workspace_init);
- *                every call leaves the tickets at zero
+ *                every call leaves the tickets at zero (zero it again after a
+ *                call that set PA_DEVERR_TIMEOUT)
  *   other arguments as in pa_decode
  * qlen_i > n (or < 0), or a batch with more query rows than max_q_len allows,
  * skips the sequence (or the call) and sets PA_DEVERR_CONTEXT; a context
