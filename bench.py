@@ -480,13 +480,15 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
     ids = np.asarray(seqs, dtype=np.int64)
     h2d = step.layout["in_bytes"]
     d2h = step.out.numel() * step.out.element_size()
-    kv_total = 0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
         step.run(ids, stream)
-        kv_total += kv_bytes(step.context_lens.numpy(), Hkv, d, fp8=fp8)
     t1 = time.perf_counter()
+    # every step appends one token to each sequence: step k attends to the
+    # final lengths minus (steps - 1 - k)
+    final = step.context_lens.numpy().astype(np.int64)
+    kv_total = sum(kv_bytes(final - (steps - 1 - k), Hkv, d, fp8=fp8) for k in range(steps))
     if binding.pa_check_device_errors(stream):
         raise RuntimeError("device error flags set in the e2e leg")
     if not torch.isfinite(step.out.float()).all():
