@@ -245,7 +245,7 @@ def setup_workload(args):
         step_tok = np.random.default_rng(w.seed).integers(0, tr["vocab"], w.B).astype(np.int32)
         slots, pairs = alloc.append_batch(seqs, tokens=step_tok)
         assert len(pairs) == 0
-        max_blocks = int(math.ceil((int(w.context_lens.max()) + 1 + args.e2e_extra)
+        max_blocks = int(math.ceil((int(w.context_lens.max()) + 1 + 2 * args.e2e_extra)
                                    / w.block_size)) + 1
         tbl, lens = alloc.export(seqs, max_blocks)
         return w, host, alloc, slots, tbl, lens, max_blocks, seqs
@@ -262,7 +262,9 @@ def setup_workload(args):
     seqs = list(range(w.B))
     slots, pairs = alloc.append_batch(seqs)
     assert len(pairs) == 0
-    max_blocks = int(math.ceil((int(w.context_lens.max()) + args.e2e_extra) / w.block_size)) + 1
+    # room for the e2e leg's two loops of e2e_extra steps
+    max_blocks = int(math.ceil((int(w.context_lens.max()) + 2 * args.e2e_extra)
+                               / w.block_size)) + 1
     tbl, lens = alloc.export(seqs, max_blocks)
     return w, host, alloc, slots, tbl, lens, max_blocks, seqs
 
@@ -455,14 +457,17 @@ def run_gpu(args):
 
 
 def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs):
-    """Real decode steps through the C ABI with host buffers, one call per
-    step: pa_step_run appends one token per sequence with the host allocator
-    (pa_append_batch), exports the tables (pa_export) into the executor's
-    pinned staging buffer, then replays the executor's CUDA graph -- one
+    """Real decode steps through the C ABI with host buffers.  Each step is
+    pa_step_submit: the host allocator appends one token per sequence
+    (pa_append_batch) and exports the tables (pa_export) into a pinned staging
+    slot, then the executor's CUDA graph for that slot runs -- one
     host->device copy of q / new K / new V / slots / tables / lengths, the
-    append, the decode, one device->host copy of the output -- and waits for
-    it.  The inputs are written into the pinned staging once (the same
-    synthetic rows every step); each step still copies them to the device.
+    append, the decode, one device->host copy of the output -- and the host
+    waits for each step's output (pa_step_wait).  Two slots let step k + 1's
+    host work overlap step k's device work; a second loop runs the same steps
+    with a wait after every submit (pa_step_run), reported as "synchronous".
+    The inputs are written into both pinned slots once (the same synthetic
+    rows every step); each step still copies them to the device.
     Copy-on-write cannot arise here: no sequence shares a partial block."""
     import numpy as np
     import torch
@@ -473,35 +478,56 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
     B, H, Hkv, d, bs = w.B, w.H, w.Hkv, w.d, w.block_size
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     step = binding.Step(alloc, B, H, Hkv, d, max_blocks, max_blocks * bs, kc, vc, w.scale,
-                        k_scale=ks if fp8 else None, v_scale=vs if fp8 else None, dtype=dt)
-    step.q.copy_(host["q"])
-    step.k_new.copy_(host["k_new"])
-    step.v_new.copy_(host["v_new"])
+                        k_scale=ks if fp8 else None, v_scale=vs if fp8 else None, dtype=dt,
+                        depth=2)
+    for i in range(2):
+        sl = step.slot(i)
+        sl["q"].copy_(host["q"])
+        sl["k_new"].copy_(host["k_new"])
+        sl["v_new"].copy_(host["v_new"])
     ids = np.asarray(seqs, dtype=np.int64)
     h2d = step.layout["in_bytes"]
     d2h = step.out.numel() * step.out.element_size()
+
+    def kv_of_loop(final):
+        # each step appends one token to every sequence: step k of the loop
+        # attends to the final lengths minus (steps - 1 - k)
+        return sum(kv_bytes(final - (steps - 1 - k), Hkv, d, fp8=fp8) for k in range(steps))
+
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    prev = None
+    for _ in range(steps):
+        slot = step.submit(ids, stream)
+        if prev is not None:
+            step.wait(prev)              # the previous step's output is on the host
+        prev = slot
+    step.wait(prev)
+    t1 = time.perf_counter()
+    kv_pipe = kv_of_loop(step.slot(prev)["context_lens"].numpy().astype(np.int64))
     for _ in range(steps):
         step.run(ids, stream)
-    t1 = time.perf_counter()
-    # every step appends one token to each sequence: step k attends to the
-    # final lengths minus (steps - 1 - k)
-    final = step.context_lens.numpy().astype(np.int64)
-    kv_total = sum(kv_bytes(final - (steps - 1 - k), Hkv, d, fp8=fp8) for k in range(steps))
+    t2 = time.perf_counter()
+    last = (2 * steps - 1) % 2
+    kv_sync = kv_of_loop(step.slot(last)["context_lens"].numpy().astype(np.int64))
     if binding.pa_check_device_errors(stream):
         raise RuntimeError("device error flags set in the e2e leg")
-    if not torch.isfinite(step.out.float()).all():
+    if not torch.isfinite(step.slot(last)["out"].float()).all():
         raise RuntimeError("non-finite output in the e2e leg")
     step.close()
-    return {"value": round(kv_total / (t1 - t0) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(kv_pipe / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
             "gpu_launches": 2 * steps,
-            "includes": "one pa_step_run per step (C ABI): host pa_append_batch + pa_export into "
-                        "pinned staging, then the library's CUDA graph: one pinned H2D of "
+            "synchronous": {"value": round(kv_sync / (t2 - t1) / 1e9, 2), "unit": "GB/s",
+                            "ms_per_step": round((t2 - t1) * 1e3 / steps, 4),
+                            "includes": "the same steps with a wait after every submit"},
+            "includes": "per step (C ABI) pa_step_submit: host pa_append_batch + pa_export into "
+                        "a pinned staging slot, then the library's CUDA graph: one pinned H2D of "
                         "q/k_new/v_new/slots/tables/lens, reshape_and_cache%s, decode%s, one D2H "
-                        "of out; waits for the step" % (("_fp8", "_fp8") if fp8 else ("", ""))}
+                        "of out; pa_step_wait for every step's output (two slots: step k+1's "
+                        "host work overlaps step k on the device)"
+                        % (("_fp8", "_fp8") if fp8 else ("", ""))}
 
 
 def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):

@@ -451,13 +451,16 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * The copies and the two kernels are captured once, at creation, into a CUDA
  * graph owned by the executor and replayed every step.  The caller owns the
  * staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
- * torch tensor) and a device buffer, both pa_step_layout.total bytes and
- * 256-byte aligned, laid out as pa_step_layout gives.  The caller writes a
- * step's q [B][H][d] and new k / v [B][Hkv][d] (dtype) into the host buffer at
- * offsets q, k_new, v_new; the executor writes slot_mapping, block_tables,
- * context_lens and cow_pairs there itself and leaves the output [B][H][d] at
- * offset out.  The paper has no counterpart to the executor object; it exists
- * so that a serving loop pays one launch per step.
+ * torch tensor) and a device buffer, each desc.depth slots of
+ * pa_step_layout.total bytes (slot i at byte i * total), 256-byte aligned.
+ * In a slot the caller writes a step's q [B][H][d] and new k / v [B][Hkv][d]
+ * (dtype) at offsets q, k_new, v_new of the host buffer; the executor writes
+ * slot_mapping, block_tables, context_lens and cow_pairs there itself and
+ * leaves the output [B][H][d] at offset out.  Step n uses slot n % depth; with
+ * two slots a step can be submitted while the one before it still runs.  The
+ * paper has no counterpart to the executor object; it exists so that a
+ * serving loop pays one launch per step and its host bookkeeping can overlap
+ * the device work.
  * ---------------------------------------------------------------------- */
 typedef struct pa_step pa_step;
 
@@ -471,13 +474,14 @@ typedef struct pa_step_desc {
     pa_dtype dtype;           /* of q, k_new, v_new, the output and a 16-bit cache */
     float scale;              /* attention scale, 1/sqrt(d) for the pages' formula */
     int32_t fp8;              /* 1: E4M3 cache with per-(token, KV head) scales (d = 128) */
+    int32_t depth;            /* staging slots (and graphs): 1 or 2 */
 } pa_step_desc;
 
-typedef struct pa_step_layout {  /* byte offsets into both staging buffers */
+typedef struct pa_step_layout {  /* byte offsets inside one slot of either staging buffer */
     size_t q, k_new, v_new, slot_mapping, block_tables, context_lens;
     size_t in_bytes;             /* [0, in_bytes) is copied host->device each step */
     size_t cow_pairs, out;       /* copy-on-write pairs [B][2] int32; output [B][H][d] */
-    size_t total;
+    size_t total;                /* bytes of one slot */
 } pa_step_layout;
 
 /* Layout of the staging buffers for desc; PA_ERR_INVALID for a bad desc. */
@@ -494,14 +498,23 @@ PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, v
                                 void* dev_stage, void* workspace, size_t ws_bytes,
                                 pa_step** out);
 
-/* One decode step for the B sequences seq_ids (host): appends one token to
- * each (pa_append_batch), issues the copy-on-write copies that needs, exports
- * the tables, launches the graph on `stream` and waits for it, so the output
- * is in the host buffer on return.  A sequence whose length after the append
- * would exceed max_context_len or max_blocks * block_size returns
- * PA_ERR_BOUNDS before anything changes; allocator errors are those of
- * pa_append_batch (all or nothing).  The staging buffers are reused: write
- * the next step's inputs only after this call returned. */
+/* Submits one decode step for the B sequences seq_ids (host) without waiting
+ * for it: in slot n % depth (n = steps submitted so far; *slot receives it,
+ * nullable) -- after waiting for the step that last used that slot -- appends
+ * one token to each sequence (pa_append_batch), issues the copy-on-write
+ * copies that needs, exports the tables and launches the slot's graph on
+ * `stream`.  A sequence whose length after the append would exceed
+ * max_context_len or max_blocks * block_size returns PA_ERR_BOUNDS before
+ * anything changes; allocator errors are those of pa_append_batch (all or
+ * nothing).  Write a step's inputs into its slot before submitting it, and
+ * only once the slot's previous step is done (pa_step_wait). */
+PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream, int32_t* slot);
+
+/* Waits for the last step submitted in `slot`; its output is then in the
+ * slot's host region. */
+PA_API pa_status pa_step_wait(pa_step* s, int32_t slot);
+
+/* pa_step_submit followed by pa_step_wait of its slot. */
 PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream);
 
 PA_API void pa_step_destroy(pa_step* s);

@@ -44,7 +44,7 @@ class StepDesc(ctypes.Structure):
                 ("d", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("max_context_len", ctypes.c_int32), ("dtype", ctypes.c_int),
-                ("scale", ctypes.c_float), ("fp8", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("fp8", ctypes.c_int32), ("depth", ctypes.c_int32)]
 
 
 class StepLayout(ctypes.Structure):
@@ -103,6 +103,8 @@ SIGNATURES = {
     "pa_step_layout_get": (_ST, [ctypes.POINTER(StepDesc), ctypes.POINTER(StepLayout)]),
     "pa_step_create": (_ST, [ctypes.POINTER(StepDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                              ctypes.POINTER(_P)]),
+    "pa_step_submit": (_ST, [_P, _P, _P, _P]),
+    "pa_step_wait": (_ST, [_P, _I32]),
     "pa_step_run": (_ST, [_P, _P, _P]),
     "pa_step_destroy": (None, [_P]),
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -508,15 +510,17 @@ class Allocator:
 class Step:
     """The decode step executor (``pa_step_*``) for one layer's caches.
 
-    Allocates its two staging buffers (pinned host, device) and the decode
-    workspace as torch tensors and exposes the host buffer's regions as
-    tensors: fill ``q``, ``k_new`` and ``v_new`` before each :meth:`run`; the
-    step's output is then in ``out``.  With ``k_scale``/``v_scale`` the caches
-    are FP8 codes (uint8) and ``dtype`` gives the 16-bit type of the inputs."""
+    Allocates its two staging buffers (pinned host, device; ``depth`` slots
+    each) and the decode workspace as torch tensors and exposes each slot's
+    host regions as tensors (``slot(i)``; ``q``, ``k_new``, ``v_new``, ``out``
+    are slot 0's).  Fill a slot's inputs, then :meth:`run` (submit and wait),
+    or :meth:`submit` / :meth:`wait` to overlap the next step's host work with
+    this one's device work.  With ``k_scale``/``v_scale`` the caches are FP8
+    codes (uint8) and ``dtype`` gives the 16-bit type of the inputs."""
 
     def __init__(self, alloc: Allocator, B: int, H: int, Hkv: int, d: int, max_blocks: int,
                  max_context_len: int, k_cache, v_cache, scale: float, k_scale=None,
-                 v_scale=None, dtype=None):
+                 v_scale=None, dtype=None, depth: int = 1):
         import torch
         self._lib = load()
         N, bs = int(k_cache.shape[0]), int(k_cache.shape[1])
@@ -527,17 +531,18 @@ class Step:
             raise ValueError("an FP8 cache needs dtype, the 16-bit type of q and k/v_new")
         dt = dtype if fp8 else k_cache.dtype
         self.desc = StepDesc(B, H, Hkv, d, bs, N, max_blocks, max_context_len,
-                             PA_F16 if dt == torch.float16 else PA_BF16, scale, int(fp8))
+                             PA_F16 if dt == torch.float16 else PA_BF16, scale, int(fp8), depth)
         lay = StepLayout()
         _check(self._lib.pa_step_layout_get(ctypes.byref(self.desc), ctypes.byref(lay)),
                "pa_step_layout_get")
         self.layout = {f: getattr(lay, f) for f, _ in StepLayout._fields_}
         dev = k_cache.device
+        total = depth * lay.total
         # 256-byte alignment: over-allocate and take an aligned view
-        self._host_raw = torch.empty(lay.total + 256, dtype=torch.uint8, pin_memory=True)
-        self._dev_raw = torch.empty(lay.total + 256, dtype=torch.uint8, device=dev)
-        self.host = self._aligned(self._host_raw, lay.total)
-        self.dev = self._aligned(self._dev_raw, lay.total)
+        self._host_raw = torch.empty(total + 256, dtype=torch.uint8, pin_memory=True)
+        self._dev_raw = torch.empty(total + 256, dtype=torch.uint8, device=dev)
+        self.host = self._aligned(self._host_raw, total)
+        self.dev = self._aligned(self._dev_raw, total)
         self.ws = torch.zeros(pa_decode_workspace_size(B, H, d), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize(dev)
         self._caches = (k_cache, v_cache, k_scale, v_scale)
@@ -550,30 +555,50 @@ class Step:
                                         self.host.data_ptr(), self.dev.data_ptr(),
                                         self.ws.data_ptr(), self.ws.numel(),
                                         ctypes.byref(self._h)), "pa_step_create")
-
-        def region(name, shape, dtype):
-            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-            off = self.layout[name]
-            return self.host[off: off + n].view(dtype).view(*shape)
-
-        self.q = region("q", (B, H, d), dt)
-        self.k_new = region("k_new", (B, Hkv, d), dt)
-        self.v_new = region("v_new", (B, Hkv, d), dt)
-        self.out = region("out", (B, H, d), dt)
-        self.slot_mapping = region("slot_mapping", (B,), torch.int64)
-        self.block_tables = region("block_tables", (B, max_blocks), torch.int32)
-        self.context_lens = region("context_lens", (B,), torch.int32)
+        shapes = {"q": ((B, H, d), dt), "k_new": ((B, Hkv, d), dt), "v_new": ((B, Hkv, d), dt),
+                  "out": ((B, H, d), dt), "slot_mapping": ((B,), torch.int64),
+                  "block_tables": ((B, max_blocks), torch.int32),
+                  "context_lens": ((B,), torch.int32)}
+        self._slots = []
+        for i in range(depth):
+            views = {}
+            for name, (shape, dtype_) in shapes.items():
+                n = int(np.prod(shape)) * torch.empty(0, dtype=dtype_).element_size()
+                off = i * lay.total + self.layout[name]
+                views[name] = self.host[off: off + n].view(dtype_).view(*shape)
+            self._slots.append(views)
+        for name in shapes:
+            setattr(self, name, self._slots[0][name])
 
     @staticmethod
     def _aligned(raw, n):
         off = (-raw.data_ptr()) % 256
         return raw[off: off + n]
 
-    def run(self, seq_ids, stream=None) -> None:
+    def slot(self, i: int) -> dict:
+        """The host regions of staging slot i (q, k_new, v_new, out, slot_mapping,
+        block_tables, context_lens)."""
+        return self._slots[i]
+
+    def _ids(self, seq_ids):
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
         if ids.shape[0] != self.desc.B:
             raise ValueError("the executor runs %d sequences per step" % self.desc.B)
-        _check(self._lib.pa_step_run(self._h, _np_ptr(ids), _stream_ptr(stream)), "pa_step_run")
+        return ids
+
+    def submit(self, seq_ids, stream=None) -> int:
+        """Submits one step (no wait); returns its slot."""
+        slot = ctypes.c_int32()
+        _check(self._lib.pa_step_submit(self._h, _np_ptr(self._ids(seq_ids)), _stream_ptr(stream),
+                                        ctypes.byref(slot)), "pa_step_submit")
+        return slot.value
+
+    def wait(self, slot: int) -> None:
+        _check(self._lib.pa_step_wait(self._h, slot), "pa_step_wait")
+
+    def run(self, seq_ids, stream=None) -> None:
+        _check(self._lib.pa_step_run(self._h, _np_ptr(self._ids(seq_ids)), _stream_ptr(stream)),
+               "pa_step_run")
 
     def close(self):
         if self._h:

@@ -7,7 +7,9 @@
 // the append (pa_reshape_and_cache), the attention (pa_decode) and one
 // device->host copy of the output.  The device part is captured once into a CUDA graph and
 // replayed every step, so a step costs one graph launch instead of one launch
-// or copy call per operation.
+// or copy call per operation.  With two staging slots a step can be submitted
+// while the previous one still runs, so the host bookkeeping of step n + 1
+// overlaps the device work of step n.
 #include <cuda_runtime.h>
 
 #include <new>
@@ -15,21 +17,9 @@
 #include "pa.h"
 #include "pa_common.cuh"
 
-struct pa_step {
-    pa_step_desc desc;
-    pa_step_layout lay;
-    pa_allocator* alloc;
-    void* k_cache;
-    void* v_cache;
-    float* k_scale;       // FP8 caches only
-    float* v_scale;
-    unsigned char* host;  // pinned staging
-    unsigned char* dev;   // device staging
-    int64_t block_bytes;  // one block of one cache (codes for FP8)
-    cudaGraphExec_t exec;
-};
-
 namespace {
+
+constexpr int kMaxDepth = 2;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -40,7 +30,79 @@ bool desc_ok(const pa_step_desc* d) {
            d->num_blocks > 0 && d->max_blocks > 0 && d->max_context_len > 0 &&
            (int64_t)d->max_context_len <= (int64_t)d->max_blocks * d->block_size &&
            (d->dtype == PA_F16 || d->dtype == PA_BF16) && (d->fp8 == 0 || d->fp8 == 1) &&
-           (d->fp8 == 0 || d->d == 128);
+           (d->fp8 == 0 || d->d == 128) && d->depth >= 1 && d->depth <= kMaxDepth;
+}
+
+}  // namespace
+
+struct pa_step {
+    pa_step_desc desc;
+    pa_step_layout lay;     // offsets inside one slot; slot i starts at i * lay.total
+    pa_allocator* alloc;
+    void* k_cache;
+    void* v_cache;
+    float* k_scale;         // FP8 caches only
+    float* v_scale;
+    unsigned char* host;    // pinned staging, depth slots
+    unsigned char* dev;     // device staging, depth slots
+    int64_t block_bytes;    // one block of one cache (codes for FP8)
+    int64_t submitted;      // steps submitted so far (the next uses slot submitted % depth)
+    cudaGraphExec_t exec[kMaxDepth];
+    cudaEvent_t done[kMaxDepth];
+    bool pending[kMaxDepth];
+};
+
+namespace {
+
+void release(pa_step* s) {
+    for (int i = 0; i < kMaxDepth; ++i) {
+        if (s->pending[i]) cudaEventSynchronize(s->done[i]);
+        if (s->exec[i]) cudaGraphExecDestroy(s->exec[i]);
+        if (s->done[i]) cudaEventDestroy(s->done[i]);
+    }
+    delete s;
+}
+
+// Captures slot i's graph on the private stream cap: H2D of the slot's
+// inputs, the append, the decode, D2H of the slot's output.
+pa_status capture(pa_step* s, int i, void* workspace, size_t ws_bytes, cudaStream_t cap) {
+    const pa_step_desc* d = &s->desc;
+    const pa_step_layout& L = s->lay;
+    unsigned char* h = s->host + (size_t)i * L.total;
+    unsigned char* g = s->dev + (size_t)i * L.total;
+    pa_status st = PA_OK;
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, cap) != cudaSuccess)
+        st = PA_ERR_CUDA;
+    const int64_t* slots = reinterpret_cast<const int64_t*>(g + L.slot_mapping);
+    const int32_t* tables = reinterpret_cast<const int32_t*>(g + L.block_tables);
+    const int32_t* lens = reinterpret_cast<const int32_t*>(g + L.context_lens);
+    if (st == PA_OK && d->fp8)
+        st = pa_reshape_and_cache_fp8(g + L.k_new, g + L.v_new, slots, d->B, s->k_cache,
+                                      s->v_cache, s->k_scale, s->v_scale, d->num_blocks,
+                                      d->block_size, d->Hkv, d->d, d->dtype, cap);
+    else if (st == PA_OK)
+        st = pa_reshape_and_cache(g + L.k_new, g + L.v_new, slots, d->B, s->k_cache, s->v_cache,
+                                  d->num_blocks, d->block_size, d->Hkv, d->d, d->dtype, cap);
+    if (st == PA_OK && d->fp8)
+        st = pa_decode_fp8(g + L.q, s->k_cache, s->v_cache, s->k_scale, s->v_scale, tables,
+                           d->max_blocks, lens, d->max_context_len, d->B, d->H, d->Hkv, d->d,
+                           d->block_size, d->num_blocks, d->scale, d->dtype, g + L.out, workspace,
+                           ws_bytes, cap);
+    else if (st == PA_OK)
+        st = pa_decode(g + L.q, s->k_cache, s->v_cache, tables, d->max_blocks, lens,
+                       d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size, d->num_blocks,
+                       d->scale, d->dtype, g + L.out, workspace, ws_bytes, cap);
+    if (st == PA_OK &&
+        cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d->B * d->H * d->d * 2,
+                        cudaMemcpyDeviceToHost, cap) != cudaSuccess)
+        st = PA_ERR_CUDA;
+    // End the capture whatever happened, so the stream is usable again.
+    if (cudaStreamEndCapture(cap, &graph) != cudaSuccess && st == PA_OK) st = PA_ERR_CUDA;
+    if (st == PA_OK && cudaGraphInstantiate(&s->exec[i], graph, 0) != cudaSuccess) st = PA_ERR_CUDA;
+    if (graph) cudaGraphDestroy(graph);
+    return st;
 }
 
 }  // namespace
@@ -98,95 +160,74 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
     s->host = static_cast<unsigned char*>(host_stage);
     s->dev = static_cast<unsigned char*>(dev_stage);
     s->block_bytes = (int64_t)d->block_size * d->Hkv * d->d * (d->fp8 ? 1 : 2);
-    s->exec = nullptr;
-
+    s->submitted = 0;
+    for (int i = 0; i < kMaxDepth; ++i) {
+        s->exec[i] = nullptr;
+        s->done[i] = nullptr;
+        s->pending[i] = false;
+    }
     // One-time set-up of the device error word and SM count, outside the capture.
     if (!pa::device_error_word() || !pa::device_sm_count()) {
-        delete s;
+        release(s);
         return PA_ERR_CUDA;
     }
-    // The graph is captured on a private stream; it can be launched on any.
+    // The graphs are captured on a private stream; they can be launched on any.
     cudaStream_t cap = nullptr;
     if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
-        delete s;
+        release(s);
         return PA_ERR_CUDA;
     }
-    const pa_step_layout& L = s->lay;
-    unsigned char* h = s->host;
-    unsigned char* g = s->dev;
     pa_status st = PA_OK;
-    cudaGraph_t graph = nullptr;
-    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
-        st = PA_ERR_CUDA;
-    } else {
-        if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, cap) != cudaSuccess)
+    for (int i = 0; i < d->depth && st == PA_OK; ++i) {
+        if (cudaEventCreateWithFlags(&s->done[i], cudaEventDisableTiming) != cudaSuccess)
             st = PA_ERR_CUDA;
-        const int64_t* slots = reinterpret_cast<const int64_t*>(g + L.slot_mapping);
-        const int32_t* tables = reinterpret_cast<const int32_t*>(g + L.block_tables);
-        const int32_t* lens = reinterpret_cast<const int32_t*>(g + L.context_lens);
-        if (st == PA_OK && d->fp8)
-            st = pa_reshape_and_cache_fp8(g + L.k_new, g + L.v_new, slots, d->B, k_cache, v_cache,
-                                          k_scale, v_scale, d->num_blocks, d->block_size, d->Hkv,
-                                          d->d, d->dtype, cap);
-        else if (st == PA_OK)
-            st = pa_reshape_and_cache(g + L.k_new, g + L.v_new, slots, d->B, k_cache, v_cache,
-                                      d->num_blocks, d->block_size, d->Hkv, d->d, d->dtype, cap);
-        if (st == PA_OK && d->fp8)
-            st = pa_decode_fp8(g + L.q, k_cache, v_cache, k_scale, v_scale, tables, d->max_blocks,
-                               lens, d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size,
-                               d->num_blocks, d->scale, d->dtype, g + L.out, workspace, ws_bytes,
-                               cap);
-        else if (st == PA_OK)
-            st = pa_decode(g + L.q, k_cache, v_cache, tables, d->max_blocks, lens,
-                           d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size,
-                           d->num_blocks, d->scale, d->dtype, g + L.out, workspace, ws_bytes, cap);
-        if (st == PA_OK &&
-            cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d->B * d->H * d->d * 2,
-                            cudaMemcpyDeviceToHost, cap) != cudaSuccess)
-            st = PA_ERR_CUDA;
-        // End the capture whatever happened, so the stream is usable again.
-        if (cudaStreamEndCapture(cap, &graph) != cudaSuccess && st == PA_OK) st = PA_ERR_CUDA;
+        else
+            st = capture(s, i, workspace, ws_bytes, cap);
     }
-    if (st == PA_OK && cudaGraphInstantiate(&s->exec, graph, 0) != cudaSuccess) st = PA_ERR_CUDA;
-    if (graph) cudaGraphDestroy(graph);
     cudaStreamDestroy(cap);
     if (st != PA_OK) {
-        if (s->exec) cudaGraphExecDestroy(s->exec);
-        delete s;
+        release(s);
         return st;
     }
     *out = s;
     return PA_OK;
 }
 
-PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream) {
+PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream,
+                                int32_t* slot_out) {
     if (!s || !seq_ids) return PA_ERR_INVALID;
     const pa_step_desc& d = s->desc;
     const pa_step_layout& L = s->lay;
+    const int slot = (int)(s->submitted % d.depth);
+    // The slot's staging is reused: the step that last used it must be done.
+    if (s->pending[slot]) {
+        if (cudaEventSynchronize(s->done[slot]) != cudaSuccess) return PA_ERR_CUDA;
+        s->pending[slot] = false;
+    }
+    unsigned char* h = s->host + (size_t)slot * L.total;
+    unsigned char* g = s->dev + (size_t)slot * L.total;
     // Every sequence must still fit the executor's bounds after the append;
     // checked first so that a refusal changes nothing.
     for (int32_t i = 0; i < d.B; ++i) {
         int32_t len = 0, nb = 0;
         const pa_status st = pa_seq_info(s->alloc, seq_ids[i], &len, &nb);
         if (st != PA_OK) return st;
-        if (len + 1 > d.max_context_len ||
-            (len + d.block_size) / d.block_size > d.max_blocks)
+        if (len + 1 > d.max_context_len || (len + d.block_size) / d.block_size > d.max_blocks)
             return PA_ERR_BOUNDS;
     }
     int32_t ncow = 0;
-    int32_t* pairs = reinterpret_cast<int32_t*>(s->host + L.cow_pairs);
+    int32_t* pairs = reinterpret_cast<int32_t*>(h + L.cow_pairs);
     pa_status st = pa_append_batch(s->alloc, seq_ids, d.B,
-                                   reinterpret_cast<int64_t*>(s->host + L.slot_mapping), pairs,
-                                   &ncow);
+                                   reinterpret_cast<int64_t*>(h + L.slot_mapping), pairs, &ncow);
     if (st != PA_OK) return st;
     st = pa_export(s->alloc, seq_ids, d.B, d.max_blocks,
-                   reinterpret_cast<int32_t*>(s->host + L.block_tables),
-                   reinterpret_cast<int32_t*>(s->host + L.context_lens));
+                   reinterpret_cast<int32_t*>(h + L.block_tables),
+                   reinterpret_cast<int32_t*>(h + L.context_lens));
     if (st != PA_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (ncow > 0) {
         // Copy-on-write before the step's append writes the new token.
-        int32_t* dpairs = reinterpret_cast<int32_t*>(s->dev + L.cow_pairs);
+        int32_t* dpairs = reinterpret_cast<int32_t*>(g + L.cow_pairs);
         if (cudaMemcpyAsync(dpairs, pairs, (size_t)ncow * 2 * sizeof(int32_t),
                             cudaMemcpyHostToDevice, cs) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -202,14 +243,30 @@ PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream) {
             if (st != PA_OK) return st;
         }
     }
-    if (cudaGraphLaunch(s->exec, cs) != cudaSuccess) return PA_ERR_CUDA;
-    return cudaStreamSynchronize(cs) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (cudaGraphLaunch(s->exec[slot], cs) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaEventRecord(s->done[slot], cs) != cudaSuccess) return PA_ERR_CUDA;
+    s->pending[slot] = true;
+    ++s->submitted;
+    if (slot_out) *slot_out = slot;
+    return PA_OK;
+}
+
+PA_API pa_status pa_step_wait(pa_step* s, int32_t slot) {
+    if (!s || slot < 0 || slot >= s->desc.depth) return PA_ERR_INVALID;
+    if (!s->pending[slot]) return PA_OK;
+    if (cudaEventSynchronize(s->done[slot]) != cudaSuccess) return PA_ERR_CUDA;
+    s->pending[slot] = false;
+    return PA_OK;
+}
+
+PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream) {
+    int32_t slot = 0;
+    const pa_status st = pa_step_submit(s, seq_ids, stream, &slot);
+    return st != PA_OK ? st : pa_step_wait(s, slot);
 }
 
 PA_API void pa_step_destroy(pa_step* s) {
-    if (!s) return;
-    if (s->exec) cudaGraphExecDestroy(s->exec);
-    delete s;
+    if (s) release(s);
 }
 
 }  // extern "C"

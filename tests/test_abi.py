@@ -95,7 +95,7 @@ def test_cache_op_host_checks(lib):
 def test_step_layout_and_argument_checks(lib):
     """The executor's staging layout: every region 256-byte aligned, in the
     documented order, large enough for its tensor; bad descriptions refused."""
-    d = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0)
+    d = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0, 1)
     L = binding.StepLayout()
     assert lib.pa_step_layout_get(ctypes.byref(d), ctypes.byref(L)) == 0
     order = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "out"]
@@ -110,14 +110,16 @@ def test_step_layout_and_argument_checks(lib):
     assert L.in_bytes == L.cow_pairs and L.in_bytes >= L.context_lens + sizes["context_lens"]
     assert L.out - L.cow_pairs >= 64 * 2 * 4 and L.total >= L.out + sizes["out"]
     for field, bad in [("max_context_len", 2049), ("d", 96), ("block_size", 64), ("B", 0),
-                       ("Hkv", 3), ("dtype", 7), ("fp8", 2)]:
-        e = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0)
+                       ("Hkv", 3), ("dtype", 7), ("fp8", 2), ("depth", 0), ("depth", 3)]:
+        e = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0, 1)
         setattr(e, field, bad)
         assert lib.pa_step_layout_get(ctypes.byref(e), ctypes.byref(L)) == 1, field
     # creation refuses missing buffers before touching the device
     h = ctypes.c_void_p()
     assert lib.pa_step_create(ctypes.byref(d), None, None, None, None, None, None, None, None,
                               0, ctypes.byref(h)) == 1
-    e = binding.StepDesc(64, 40, 40, 64, 16, 5240, 128, 2048, 0, 0.088, 1)   # FP8 needs d 128
+    e = binding.StepDesc(64, 40, 40, 64, 16, 5240, 128, 2048, 0, 0.088, 1, 1)   # FP8 needs d 128
     assert lib.pa_step_layout_get(ctypes.byref(e), ctypes.byref(L)) == 1
     assert lib.pa_step_run(None, None, None) == 1
+    assert lib.pa_step_submit(None, None, None, None) == 1
+    assert lib.pa_step_wait(None, 0) == 1

@@ -177,3 +177,59 @@ def test_fp8_cache_with_copy_on_write():
                                 tbl, lens, 0.09)
         assert_close(step.out.clone(), ref, "fp8 step %d" % k)
     step.close()
+
+
+def test_two_slots_pipelined():
+    """depth 2: step k + 1 is submitted (its host bookkeeping done, its graph
+    queued) before step k is waited for; every step's output, slots and
+    tables are checked against the oracle replaying the steps in order, and
+    the caches at the end."""
+    B, H, Hkv, d, bs = 10, 8, 2, 128, 16
+    lens = np.random.default_rng(77).integers(1, 300, size=B)
+
+    def setup(a):
+        for i, n in enumerate(lens):
+            (a.alloc if hasattr(a, "alloc") else a.allocate)(i, int(n))
+
+    N = int(sum(math.ceil((n + 8) / bs) for n in lens) * 1.25) + 4
+    cpp, model, kc, vc = _state(N, bs, Hkv, d, torch.float16, 31, setup)
+    kd, vd = kc.cuda(), vc.cuda()
+    max_blocks = int(math.ceil((lens.max() + 8) / bs))
+    step = binding.Step(cpp, B, H, Hkv, d, max_blocks, max_blocks * bs, kd, vd, 0.1, depth=2)
+    ids = [3, 1, 4, 0, 5, 9, 2, 6, 8, 7]
+    inputs = {}
+
+    def fill(k):
+        xs = tuple(wl.normal_tensor(shape, torch.float16, 500 + 3 * k + j)
+                   for j, shape in enumerate([(B, H, d), (B, Hkv, d), (B, Hkv, d)]))
+        sl = step.slot(k % 2)
+        for name, x in zip(("q", "k_new", "v_new"), xs):
+            sl[name].copy_(x)
+        inputs[k] = xs
+
+    def check(k):
+        step.wait(k % 2)
+        q, kn, vn = inputs[k]
+        slots, pairs = model.append_batch(ids)
+        assert not pairs
+        oracle.reshape_and_cache(kn, vn, np.asarray(slots, np.int64), kc, vc)
+        tbl, lens_ = model.export(ids, max_blocks)
+        sl = step.slot(k % 2)
+        assert np.array_equal(sl["slot_mapping"].numpy(), np.asarray(slots, np.int64))
+        assert np.array_equal(sl["block_tables"].numpy(), tbl)
+        assert np.array_equal(sl["context_lens"].numpy(), lens_)
+        ref = oracle.decode(wl.bits(q), wl.bits(kc), wl.bits(vc), tbl, lens_, 0.1,
+                            oracle.DTYPE_F16, num_threads=THREADS)
+        assert_close(sl["out"].clone(), ref, "pipelined step %d" % k)
+
+    steps = 6
+    for k in range(steps):
+        if k >= 2:
+            check(k - 2)          # frees slot k % 2 for step k
+        fill(k)
+        assert step.submit(ids) == k % 2
+    for k in range(steps - 2, steps):
+        check(k)
+    assert binding.pa_check_device_errors() == 0
+    assert bit_equal(kd, kc) and bit_equal(vd, vc)
+    step.close()
