@@ -506,7 +506,8 @@ PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, v
  * `stream`.  A sequence whose length after the append would exceed
  * max_context_len or max_blocks * block_size returns PA_ERR_BOUNDS before
  * anything changes; allocator errors are those of pa_append_batch (all or
- * nothing).  Write a step's inputs into its slot before submitting it, and
+ * nothing); after a later failure (PA_ERR_CUDA from a launch) the appends
+ * stay done.  Write a step's inputs into its slot before submitting it, and
  * only once the slot's previous step is done (pa_step_wait). */
 PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream, int32_t* slot);
 
