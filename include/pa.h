@@ -25,8 +25,11 @@
  *     16-byte aligned.  A token's slot is physical_block * block_size +
  *     offset_in_block.
  *   - Supported shapes: head_dim 64 or 128; block_size 8, 16 or 32;
- *     num_heads % num_kv_heads == 0 with at most 16 query heads per KV head;
- *     fp16 or bf16 elements.  Other shapes return PA_ERR_UNSUPPORTED.
+ *     num_heads % num_kv_heads == 0; for pa_decode and pa_decode_fp8 the
+ *     group G = num_heads / num_kv_heads is at most 16 or a multiple of 16
+ *     (wider groups, e.g. multi-query attention, are processed 16 query heads
+ *     at a time); fp16 or bf16 elements.  Other shapes return
+ *     PA_ERR_UNSUPPORTED.
  */
 #ifndef PA_H_
 #define PA_H_

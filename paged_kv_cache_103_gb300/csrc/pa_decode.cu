@@ -87,7 +87,10 @@ struct DecodeParams {
     int32_t* counters;  // [B * Hkv] arrival tickets of split pairs
     float* partials;    // [2 * kMaxCtas][slot_floats]
     unsigned int* err;
-    int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages;
+    // Hkv and G as the kernel sees them: a KV head with more than kMaxG query
+    // heads is split into `subs` pairs of kMaxG heads each, pair g reading KV
+    // head g / subs (query heads g * G .. g * G + G - 1 either way).
+    int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages, subs;
     float scale_log2;
 };
 
@@ -310,11 +313,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         struct Walk {
             Segment s;
             int32_t n_raw, wbase, went, wnext;
+            int32_t kvh;  // the cache's KV head of the pair
             const int32_t* trow;
         };
         auto open = [&](int32_t at) {
             Walk w;
             w.s = find_segment(prefix, B, Hkv, at, hi);
+            w.kvh = w.s.g / p.subs;
             w.n_raw = __ldg(p.context_lens + w.s.i);
             w.trow = p.block_tables + (int64_t)w.s.i * p.max_blocks;
             w.wbase = (w.s.c0 * kChunk) >> bs_shift;
@@ -371,7 +376,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             }
                             const uint32_t off = ((uint32_t)b * kHalves << rows_shift) * 128;
                             const int32_t row = ok ? blk[b] * bs : oob_row;
-                            const int32_t z = cur.s.g * (int32_t)kHalves;
+                            const int32_t z = cur.kvh * (int32_t)kHalves;
                             pa::tma_load_3d(kdst + off, &kmap, &full[stage], 0, row, z, policy);
                             pa::tma_load_3d(kdst + L.stage_bytes / 2 + off, &vmap, &full[stage], 0,
                                             row, z, policy);
@@ -379,9 +384,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                 unsigned char* sdst = smem + L.scales + stage * L.scale_stage +
                                                       (uint32_t)b * kScaleSlotBytes;
                                 const int32_t sb = ok ? blk[b] : p.num_blocks;
-                                pa::tma_load_3d(sdst, &ksmap, &full[stage], 0, cur.s.g, sb, policy);
+                                pa::tma_load_3d(sdst, &ksmap, &full[stage], 0, cur.kvh, sb, policy);
                                 pa::tma_load_3d(sdst + L.scale_stage / 2, &vsmap, &full[stage], 0,
-                                                cur.s.g, sb, policy);
+                                                cur.kvh, sb, policy);
                             }
                         }
                     }
@@ -1171,23 +1176,31 @@ pa_status prepare(int32_t max_blocks, int32_t max_context_len, int32_t B, int32_
         max_context_len < 0 || !std::isfinite(scale))
         return PA_ERR_INVALID;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (H % Hkv != 0 || H / Hkv > kMaxG) return PA_ERR_UNSUPPORTED;
+    if (H % Hkv != 0) return PA_ERR_UNSUPPORTED;
+    // Groups wider than kMaxG query heads (multi-query attention) are split
+    // into sub-groups of kMaxG heads, each a pair of its own.
+    int G = H / Hkv, subs = 1;
+    if (G > kMaxG) {
+        if (G % kMaxG != 0) return PA_ERR_UNSUPPORTED;
+        subs = G / kMaxG;
+        G = kMaxG;
+    }
     if (d != 128 && (fp8 || d != 64)) return PA_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
     if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
     if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
     // Flattened chunk indices are int32: every sequence's chunks times Hkv.
     const int64_t max_chunks = ((int64_t)max_blocks * block_size + kChunk - 1) / kChunk;
-    if ((int64_t)B * Hkv * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
-    const int G = H / Hkv;
+    if ((int64_t)B * Hkv * subs * max_chunks >= ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
     const int stages = choose_stages(d, G, B, fp8, block_size);
     if (stages < 2) return PA_ERR_UNSUPPORTED;
     if (B > 0 && ws_bytes < pa_decode_workspace_size(B, H, d)) return PA_ERR_INVALID;
     prm->max_blocks = max_blocks;
     prm->B = B;
     prm->H = H;
-    prm->Hkv = Hkv;
+    prm->Hkv = Hkv * subs;
     prm->G = G;
+    prm->subs = subs;
     prm->bs = block_size;
     prm->num_blocks = num_blocks;
     prm->stages = stages;

@@ -63,7 +63,7 @@ def test_decode_host_checks_answer_without_a_gpu(lib):
     # H not a multiple of Hkv
     st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 5, 2, 128, 16, 8, 0.1, 0, P, P, 1 << 20, None)
     assert st == 6
-    # more than 16 query heads per KV head
+    # 17 query heads per KV head: above 16 and not a multiple of 16
     st = lib.pa_decode(P, P, P, P, 4, P, 64, 2, 34, 2, 128, 16, 8, 0.1, 0, P, P, 1 << 20, None)
     assert st == 6
     # workspace too small

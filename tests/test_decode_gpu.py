@@ -236,3 +236,26 @@ def test_batch_above_the_limit_is_refused():
     torch.cuda.synchronize()
     assert bool((run.out == 7.0).all())                    # nothing was launched
     assert binding.pa_check_device_errors() == 0
+
+
+@pytest.mark.parametrize("H,Hkv,d,bs,dtype", [(32, 1, 128, 16, torch.bfloat16),
+                                              (96, 2, 64, 8, torch.float16),
+                                              (64, 1, 128, 32, torch.float16)])
+def test_groups_wider_than_16(H, Hkv, d, bs, dtype):
+    """Multi-query attention and other groups of 32 .. 64 query heads per KV
+    head: each KV head's heads are processed 16 at a time."""
+    lens = [1, 0, 31, 33, 700, 5000, 64, 257]
+    w, host, tbl, lens = _custom(len(lens), H, Hkv, d, bs, lens, dtype=dtype, seed=H + d)
+    run = GpuRun(w, host)
+    out = run.decode(tbl, lens)
+    assert binding.pa_check_device_errors() == 0
+    ref = oracle_decode(w, host["q"], host["k_cache"], host["v_cache"], tbl, lens)
+    assert_close(out.cpu(), ref, "G=%d" % (H // Hkv))
+
+
+def test_group_above_16_not_a_multiple_is_refused():
+    w, host, tbl, lens = _custom(2, 24, 1, 64, 16, [10, 20], seed=4)
+    run = GpuRun(w, host)
+    with pytest.raises(binding.PaError) as e:
+        run.decode(tbl, lens)
+    assert binding.STATUS_NAMES[e.value.status] == "PA_ERR_UNSUPPORTED"

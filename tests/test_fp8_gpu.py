@@ -297,3 +297,13 @@ def test_decode_fp8_max_batch():
     assert binding.pa_check_device_errors() == 0
     _same_cache(run, c)
     assert_close(out.cpu(), _oracle_decode(q, c, tbl, n, scale), "fp8 B=4096")
+
+
+def test_decode_fp8_multi_query_attention():
+    """One KV head for 32 query heads (two sub-groups of 16)."""
+    lens = np.array([700, 1, 95, 4000])
+    q, c, run, tbl, n = _quantised_through_append(4, 32, 1, 16, torch.float16, lens, 21)
+    scale = 1.0 / math.sqrt(128)
+    out = run.decode(tbl, n, scale)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _oracle_decode(q, c, tbl, n, scale), "fp8 G=32")

@@ -34,7 +34,7 @@ def _shape(rng, d=None, max_b=32, max_len=9000):
     d = int(d or rng.choice([64, 128]))
     bs = int(rng.choice([8, 16, 32]))
     Hkv = int(rng.choice([1, 2, 4, 8]))
-    G = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 12, 16]))
+    G = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 12, 16, 32]))
     B = int(rng.integers(1, max_b + 1))
     kind = rng.integers(0, 4, size=B)
     lens = np.where(kind == 0, rng.integers(0, 3, size=B),
