@@ -35,6 +35,8 @@ Contents:
 * :func:`kv_bytes_per_token` / :func:`kv_cache_bytes` -- the closed forms.
 * :func:`reshape_and_cache_fp8`, :func:`decode_fp8`, :func:`e4m3_encode` -- the
   FP8 KV cache (a reading, see the comment above :data:`E4M3_MAX`).
+* :func:`reshape_and_cache_int8`, :func:`decode_int8`, :func:`int8_encode` -- the
+  INT8 KV cache (a reading, see the comment above :data:`INT8_MAX`).
 * ``BlockManagerModel.allocate_prompt`` / ``append_token`` -- automatic prefix
   caching of full blocks ([P5] section 3.2, [P1] section 4.2; a reading, see
   the class docstring).
@@ -98,9 +100,10 @@ def _load():
         lib.pa_oracle_multi_query.restype = ctypes.c_int
         lib.pa_oracle_multi_query.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                               i64, f64, i32, P, i32]
-        lib.pa_oracle_decode_fp8.restype = ctypes.c_int
-        lib.pa_oracle_decode_fp8.argtypes = [P, i32, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
-                                             i64, f64, P]
+        for name in ("pa_oracle_decode_fp8", "pa_oracle_decode_int8"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P, i32, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64, P]
         _lib = lib
     return _lib
 
@@ -270,7 +273,7 @@ def reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_codes, v_codes, k_scale,
 
 
 def decode_fp8(q, q_dtype: int, k_codes, v_codes, k_scale, v_scale, block_tables,
-               context_lens, scale: float) -> np.ndarray:
+               context_lens, scale: float, _fn="pa_oracle_decode_fp8") -> np.ndarray:
     """fp64 paged decode over an FP8 cache: the attention of :func:`decode` on
     the dequantised rows code_value * scale."""
     q = _u16(q)
@@ -283,12 +286,62 @@ def decode_fp8(q, q_dtype: int, k_codes, v_codes, k_scale, v_scale, block_tables
     B, H, d = q.shape
     N, bs, Hkv, _ = kc.shape
     out = np.empty((B, H, d), dtype=np.float64)
-    rc = _load().pa_oracle_decode_fp8(_ptr(q), q_dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
-                                      _ptr(tbl), tbl.shape[1], _ptr(lens), B, H, Hkv, d, bs, N,
-                                      float(scale), _ptr(out))
+    rc = getattr(_load(), _fn)(_ptr(q), q_dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                               _ptr(tbl), tbl.shape[1], _ptr(lens), B, H, Hkv, d, bs, N,
+                               float(scale), _ptr(out))
     if rc:
-        raise ValueError("pa_oracle_decode_fp8 failed (%d)" % rc)
+        raise ValueError("%s failed (%d)" % (_fn, rc))
     return out
+
+
+# INT8 KV cache ("LLM推理优化技术地图：从KV Cache到量化与投机解码", section 4.3: 8-bit
+# KV quantisation; the pages fix no format).  Reading: symmetric, one fp32
+# scale per (token, KV head) row, s = fl32(amax / 127); code = the integer
+# nearest fl32(x / s) (fp32 division, ties to even), clamped to [-127, 127];
+# an all-zero row gets s = 0 and zero codes.  Element = code * s.  Same
+# layouts as the FP8 cache; codes are stored as their two's-complement bytes.
+INT8_MAX = 127.0
+
+
+def int8_encode(x) -> np.ndarray:
+    """fp32 values to INT8 codes (uint8 bytes of int8): nearest integer, ties
+    to even, clamped to [-127, 127]."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    c = np.clip(np.rint(x), -INT8_MAX, INT8_MAX)
+    return c.astype(np.int64).astype(np.int8).view(np.uint8)
+
+
+def quantize_rows_int8(x_fp32):
+    """Quantise rows (last axis) of fp32 values to INT8: (codes uint8, scales fp32)."""
+    x = np.asarray(x_fp32, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1).astype(np.float32)
+    s = (amax / np.float32(INT8_MAX)).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1), s).astype(np.float32)
+    codes = int8_encode((x / safe[..., None]).astype(np.float32))
+    codes = np.where((s == 0)[..., None], 0, codes).astype(np.uint8)
+    return codes, s
+
+
+def reshape_and_cache_int8(k_new, v_new, slot_mapping, k_codes, v_codes, k_scale, v_scale):
+    """The INT8 KV append: as :func:`reshape_and_cache_fp8` with INT8 codes."""
+    bs = k_codes.shape[1]
+    kq, ks = quantize_rows_int8(k_new.float().numpy())
+    vq, vs = quantize_rows_int8(v_new.float().numpy())
+    for t in range(k_new.shape[0]):
+        s = int(slot_mapping[t])
+        if s < 0:
+            continue
+        k_codes[s // bs, s % bs] = kq[t]
+        v_codes[s // bs, s % bs] = vq[t]
+        k_scale[s // bs, :, s % bs] = ks[t]
+        v_scale[s // bs, :, s % bs] = vs[t]
+
+
+def decode_int8(q, q_dtype: int, k_codes, v_codes, k_scale, v_scale, block_tables,
+                context_lens, scale: float) -> np.ndarray:
+    """fp64 paged decode over an INT8 cache (rows code * scale)."""
+    return decode_fp8(q, q_dtype, k_codes, v_codes, k_scale, v_scale, block_tables,
+                      context_lens, scale, _fn="pa_oracle_decode_int8")
 
 
 def swap_blocks(src_pools, dst_pools, pairs) -> None:

@@ -268,9 +268,18 @@ int pa_oracle_e4m3_to_double(const uint8_t* x, int64_t count, double* y) {
     return ORC_OK;
 }
 
-int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_codes,
-                         const uint8_t* v_codes, const float* k_scale, const float* v_scale,
-                         const int32_t* block_tables, int32_t max_blocks,
+/*
+ * INT8 KV cache: a code is a two's-complement byte c in [-127, 127] and the
+ * element is c * scale (same layouts and scales as E4M3).
+ */
+static double orc_code_to_double(uint8_t b, int32_t kind) {
+    return kind == 0 ? orc_e4m3_to_double(b) : (double)(int8_t)b;
+}
+
+/* Attention over an 8-bit cache: kind 0 = E4M3 codes, 1 = INT8 codes. */
+static int orc_decode_q8(const uint16_t* q, int32_t q_dtype, int32_t kind,
+                         const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scale,
+                         const float* v_scale, const int32_t* block_tables, int32_t max_blocks,
                          const int32_t* context_lens, int32_t B, int32_t H, int32_t Hkv,
                          int32_t d, int32_t block_size, int64_t num_blocks, double scale,
                          double* out) {
@@ -302,7 +311,7 @@ int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_co
                 double ks = (double)k_scale[((int64_t)pb * Hkv + g) * block_size + j % block_size];
                 double acc = 0.0;
                 for (int32_t k = 0; k < d; ++k)
-                    acc += orc_elem(q, qoff + k, q_dtype) * (orc_e4m3_to_double(k_codes[row + k]) * ks);
+                    acc += orc_elem(q, qoff + k, q_dtype) * (orc_code_to_double(k_codes[row + k], kind) * ks);
                 s[j] = scale * acc;
             }
             double m = s[0];
@@ -319,12 +328,32 @@ int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_co
                 double vs = (double)v_scale[((int64_t)pb * Hkv + g) * block_size + j % block_size];
                 double w = s[j] / sum;
                 for (int32_t k = 0; k < d; ++k)
-                    o[k] += w * (orc_e4m3_to_double(v_codes[row + k]) * vs);
+                    o[k] += w * (orc_code_to_double(v_codes[row + k], kind) * vs);
             }
         }
     }
     free(s);
     return ORC_OK;
+}
+
+int pa_oracle_decode_fp8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_codes,
+                         const uint8_t* v_codes, const float* k_scale, const float* v_scale,
+                         const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* context_lens, int32_t B, int32_t H, int32_t Hkv,
+                         int32_t d, int32_t block_size, int64_t num_blocks, double scale,
+                         double* out) {
+    return orc_decode_q8(q, q_dtype, 0, k_codes, v_codes, k_scale, v_scale, block_tables,
+                         max_blocks, context_lens, B, H, Hkv, d, block_size, num_blocks, scale, out);
+}
+
+int pa_oracle_decode_int8(const uint16_t* q, int32_t q_dtype, const uint8_t* k_codes,
+                          const uint8_t* v_codes, const float* k_scale, const float* v_scale,
+                          const int32_t* block_tables, int32_t max_blocks,
+                          const int32_t* context_lens, int32_t B, int32_t H, int32_t Hkv,
+                          int32_t d, int32_t block_size, int64_t num_blocks, double scale,
+                          double* out) {
+    return orc_decode_q8(q, q_dtype, 1, k_codes, v_codes, k_scale, v_scale, block_tables,
+                         max_blocks, context_lens, B, H, Hkv, d, block_size, num_blocks, scale, out);
 }
 
 /*
