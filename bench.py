@@ -13,10 +13,10 @@ device->host copy of the output.
 The metric is KV-cache bytes attended per second (GB/s): the K and V bytes of
 every context token, divided by the step time.  One JSON line is printed.
 
-With ``--kv-format fp8`` the cache holds E4M3 codes with one fp32 scale per
-(token, KV head) (pa_reshape_and_cache_fp8 / pa_decode_fp8); the bytes are
-then the codes and scales actually read, and ``tokens_per_s`` compares the
-two formats.
+With ``--kv-format fp8`` (or ``int8``) the cache holds E4M3 (or INT8) codes
+with one fp32 scale per (token, KV head) (pa_reshape_and_cache_fp8 /
+pa_decode_fp8, or their _int8 forms); the bytes are then the codes and scales
+actually read, and ``tokens_per_s`` compares the formats.
 """
 from __future__ import annotations
 
@@ -233,10 +233,10 @@ def setup_workload(args):
     from paged_kv_cache_103_gb300 import binding
 
     w = WORKLOADS[args.workload](args.batch)
-    fp8 = args.kv_format == "fp8"
+    fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
     host = wl_mod().qkv(w, with_cache=not fp8)
     if fp8:
-        host.update(wl_mod().fp8_cache(w))
+        host.update(wl_mod().fp8_cache(w) if args.kv_format == "fp8" else wl_mod().int8_cache(w))
     alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
     if "trace" in w.extra:
         tr = w.extra["trace"]
@@ -288,7 +288,8 @@ def run_gpu(args):
         dist.init_process_group("nccl")
 
     w, host, alloc, slots, tbl, lens, max_blocks, seqs = setup_workload(args)
-    fp8 = args.kv_format == "fp8"
+    fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
+    fmt = args.kv_format
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -315,12 +316,14 @@ def run_gpu(args):
 
     # the step's two calls through the C ABI, for either cache format
     if fp8:
+        q8_append = getattr(binding, "pa_reshape_and_cache_" + fmt)
+        q8_decode = getattr(binding, "pa_decode_" + fmt)
+
         def append(kn_, vn_, slots_):
-            binding.pa_reshape_and_cache_fp8(kn_, vn_, slots_, kc, vc, ks, vs, stream)
+            q8_append(kn_, vn_, slots_, kc, vc, ks, vs, stream)
 
         def decode(q_, tbl_, lens_, max_len_, out_):
-            binding.pa_decode_fp8(q_, kc, vc, ks, vs, tbl_, lens_, max_len_, w.scale, out_, ws,
-                                  stream)
+            q8_decode(q_, kc, vc, ks, vs, tbl_, lens_, max_len_, w.scale, out_, ws, stream)
     else:
         def append(kn_, vn_, slots_):
             binding.pa_reshape_and_cache(kn_, vn_, slots_, kc, vc, stream)
@@ -416,13 +419,15 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 KV, f16 MMA, fp32 accumulate" if fp8 else w.dtype,
-        "data": ("synthetic (seeded N(0,1) Q and new K/V, seeded E4M3 codes and scales, seeded "
-                 "context lengths, random block placement)" if fp8 else
+        "dtype": ("%s KV, f16 MMA, fp32 accumulate" % ("e4m3" if fmt == "fp8" else "int8")
+                  if fp8 else w.dtype),
+        "data": ("synthetic (seeded N(0,1) Q and new K/V, seeded %s codes and scales, seeded "
+                 "context lengths, random block placement)" % ("E4M3" if fmt == "fp8" else "INT8")
+                 if fp8 else
                  "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)"),
-        "config": {"workload": args.workload + ("_fp8kv" if fp8 else "") + "_decode_layer_step",
-                   "batch": w.B, "kv_format": "e4m3 + fp32 scale per (token, KV head)"
-                   if fp8 else w.dtype,
+        "config": {"workload": args.workload + ("_%skv" % fmt if fp8 else "") + "_decode_layer_step",
+                   "batch": w.B, "kv_format": "%s + fp32 scale per (token, KV head)"
+                   % ("e4m3" if fmt == "fp8" else "int8") if fp8 else w.dtype,
                    "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
                    "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
                    "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
@@ -436,11 +441,12 @@ def run_gpu(args):
         "timing": "each step (append + decode) replayed from one CUDA graph, CUDA events on the "
                   "launching stream around it; after each step one decode replayed alone from "
                   "its own graph and timed for the roofline",
-        "roofline": {"kernel": "pa_decode_fp8" if fp8 else "pa_decode", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "pa_decode_" + fmt if fp8 else "pa_decode", "bound": "hbm",
+                     "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
-                     "traffic": recorded_traffic("pa_decode_fp8_llama13b.txt" if fp8
+                     "traffic": recorded_traffic("pa_decode_%s_llama13b.txt" % fmt if fp8
                                                  else "pa_decode_llama13b.txt")
                      if args.workload == "llama13b" and w.B == 64 else None,
                      "algorithmic_bytes_per_launch": alg,
@@ -449,7 +455,7 @@ def run_gpu(args):
     if "prefix_cache" in w.extra:
         result["prefix_cache"] = w.extra["prefix_cache"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds, fp8)
+        result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds, fmt)
     if rank == 0:
         print(json.dumps(result))
     if dist:
@@ -479,7 +485,7 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     step = binding.Step(alloc, B, H, Hkv, d, max_blocks, max_blocks * bs, kc, vc, w.scale,
                         k_scale=ks if fp8 else None, v_scale=vs if fp8 else None, dtype=dt,
-                        depth=2)
+                        depth=2, kv_format=args.kv_format if fp8 else "native")
     for i in range(2):
         sl = step.slot(i)
         sl["q"].copy_(host["q"])
@@ -527,10 +533,10 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
                         "q/k_new/v_new/slots/tables/lens, reshape_and_cache%s, decode%s, one D2H "
                         "of out; pa_step_wait for every step's output (two slots: step k+1's "
                         "host work overlaps step k on the device)"
-                        % (("_fp8", "_fp8") if fp8 else ("", ""))}
+                        % (("_" + args.kv_format,) * 2 if fp8 else ("", ""))}
 
 
-def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):
+def oracle_sample_run(w, host, tbl, lens, seqs, threads, fmt="native"):
     """Runs the oracle on the sequences `seqs` (cache taken as it stands)."""
     import numpy as np
 
@@ -540,23 +546,25 @@ def oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8=False):
     sel = np.asarray(seqs)
     q = wl.bits(host["q"])[sel]
     code = oracle.DTYPE_F16 if w.dtype == "f16" else oracle.DTYPE_BF16
-    if fp8:   # the FP8 oracle runs on one thread
-        return oracle.decode_fp8(q, code, host["k_codes"].numpy(), host["v_codes"].numpy(),
-                                 host["k_scale"].numpy(), host["v_scale"].numpy(), tbl[sel],
-                                 lens[sel], w.scale)
+    if fmt != "native":   # the 8-bit oracles run on one thread
+        return getattr(oracle, "decode_" + fmt)(q, code, host["k_codes"].numpy(),
+                                                host["v_codes"].numpy(), host["k_scale"].numpy(),
+                                                host["v_scale"].numpy(), tbl[sel], lens[sel],
+                                                w.scale)
     return oracle.decode(q, wl.bits(host["k_cache"]), wl.bits(host["v_cache"]), tbl[sel],
                          lens[sel], w.scale, code, num_threads=threads)
 
 
-def cpu_baseline(w, host, tbl, lens, seconds, fp8=False):
+def cpu_baseline(w, host, tbl, lens, seconds, fmt="native"):
     """The oracle on the host cores over a bounded sample of the same batch:
     whole-batch passes repeated until about `seconds` of wall time."""
+    fp8 = fmt != "native"
     threads = 1 if fp8 else os.cpu_count() or 1
     seqs = list(range(w.B))
     passes, dt = 0, 0.0
     t0 = time.perf_counter()
     while passes == 0 or dt < seconds:
-        oracle_sample_run(w, host, tbl, lens, seqs, threads, fp8)
+        oracle_sample_run(w, host, tbl, lens, seqs, threads, fmt)
         passes += 1
         dt = time.perf_counter() - t0
     kvb = passes * kv_bytes(lens, w.Hkv, w.d, fp8=fp8)
@@ -570,7 +578,7 @@ def cpu_baseline(w, host, tbl, lens, seconds, fp8=False):
         # fifth of the time
         n1, done, t1 = 0, 0, time.perf_counter()
         while n1 < w.B and (n1 == 0 or time.perf_counter() - t1 < seconds / 5):
-            oracle_sample_run(w, host, tbl, lens, [n1], 1, fp8)
+            oracle_sample_run(w, host, tbl, lens, [n1], 1, fmt)
             done += int(lens[n1])
             n1 += 1
         dt1 = time.perf_counter() - t1
@@ -876,8 +884,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kv-format", choices=["native", "fp8"], default="native",
-                    help="cache in the workload's 16-bit dtype, or E4M3 codes + fp32 scales")
+    ap.add_argument("--kv-format", choices=["native", "fp8", "int8"], default="native",
+                    help="cache in the workload's 16-bit dtype, or E4M3 / INT8 codes + fp32 scales")
     ap.add_argument("--measure", choices=["decode", "swap", "multi_query"], default="decode",
                     help="swap: device<->host block swap bandwidth; multi_query: chunked prefill "
                          "and speculative verification, instead of the decode step")

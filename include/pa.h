@@ -297,6 +297,19 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
                                           int32_t num_blocks, int32_t block_size, int32_t Hkv,
                                           int32_t d, pa_dtype dtype, void* stream);
 
+/* INT8 KV append (the other 8-bit format of [P4] section 4.3; the pages fix
+ * none, so this library takes symmetric INT8 with one fp32 scale per (token,
+ * KV head) row).  As pa_reshape_and_cache_fp8 with
+ *   s = fl32(max_i |x_i| / 127)
+ *   k_cache[slot / bs][slot % bs][h][i] = clamp(rint(fl32(x_i / s)), -127, 127)
+ * (nearest integer, ties to even; the byte of the two's-complement int8); an
+ * all-zero row stores s = 0 and zero codes.  Same arguments and errors. */
+PA_API pa_status pa_reshape_and_cache_int8(const void* k_new, const void* v_new,
+                                           const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                           void* v_cache, float* k_scale, float* v_scale,
+                                           int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                                           int32_t d, pa_dtype dtype, void* stream);
+
 /* Copy-on-write block copies ([P3] section 3.3): for every layer l and pair p,
  * block pairs[p][1] of k_caches[l] and v_caches[l] becomes a bit copy of
  * block pairs[p][0].  block_bytes = block_size * Hkv * d * element size and
@@ -420,6 +433,16 @@ PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v
                                int32_t num_blocks, float scale, pa_dtype dtype, void* out,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* pa_decode_fp8 over an INT8 cache (codes from pa_reshape_and_cache_int8):
+ * element = code * scale, widened to f16 exactly; otherwise as pa_decode_fp8. */
+PA_API pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, int32_t max_blocks,
+                                const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                                int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                                int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                                void* workspace, size_t ws_bytes, void* stream);
+
 /* pa_decode without a caller-supplied workspace, for callers that cannot
  * allocate device memory: code running inside an allocator's own hooks, or in
  * a process whose device memory is pre-partitioned by a host framework that
@@ -450,7 +473,7 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * last block is copied before it is written), one host->device copy of the
  * step's inputs and tables, pa_copy_blocks when copy-on-write arises,
  * pa_reshape_and_cache, pa_decode and one device->host copy of the output
- * (pa_reshape_and_cache_fp8 and pa_decode_fp8 over an FP8 cache).
+ * (their _fp8 / _int8 forms over an 8-bit cache).
  * The copies and the two kernels are captured once, at creation, into a CUDA
  * graph owned by the executor and replayed every step.  The caller owns the
  * staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
@@ -476,7 +499,8 @@ typedef struct pa_step_desc {
     int32_t max_context_len;  /* bound of every context length, <= max_blocks * block_size */
     pa_dtype dtype;           /* of q, k_new, v_new, the output and a 16-bit cache */
     float scale;              /* attention scale, 1/sqrt(d) for the pages' formula */
-    int32_t fp8;              /* 1: E4M3 cache with per-(token, KV head) scales (d = 128) */
+    int32_t q8;               /* 8-bit cache with per-(token, KV head) scales (d = 128):
+                                 0 none, 1 E4M3 (pa_decode_fp8), 2 INT8 (pa_decode_int8) */
     int32_t depth;            /* staging slots (and graphs): 1 or 2 */
 } pa_step_desc;
 
@@ -491,7 +515,7 @@ typedef struct pa_step_layout {  /* byte offsets inside one slot of either stagi
 PA_API pa_status pa_step_layout_get(const pa_step_desc* desc, pa_step_layout* out);
 
 /* Creates an executor for one layer's caches k_cache / v_cache (device,
- * [num_blocks][block_size][Hkv][d], dtype or, with fp8, uint8 codes plus
+ * [num_blocks][block_size][Hkv][d], dtype or, with q8, uint8 codes plus
  * k_scale / v_scale [num_blocks][Hkv][block_size] fp32; the scales are NULL
  * otherwise) and the allocator alloc (all must outlive it).  workspace (device, >= pa_decode_workspace_size(B, H, d) bytes, zeroed
  * once) is the decode's.  Captures the graph on a private stream; nothing

@@ -44,7 +44,7 @@ class StepDesc(ctypes.Structure):
                 ("d", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("max_context_len", ctypes.c_int32), ("dtype", ctypes.c_int),
-                ("scale", ctypes.c_float), ("fp8", ctypes.c_int32), ("depth", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("q8", ctypes.c_int32), ("depth", ctypes.c_int32)]
 
 
 class StepLayout(ctypes.Structure):
@@ -98,6 +98,10 @@ SIGNATURES = {
                              _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_fp8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
+    "pa_reshape_and_cache_int8": (_ST, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                        _ST, _P]),
+    "pa_decode_int8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_noalloc": (_ST, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                 _I32, _F32, _ST, _P, _P]),
     "pa_step_layout_get": (_ST, [ctypes.POINTER(StepDesc), ctypes.POINTER(StepLayout)]),
@@ -195,16 +199,23 @@ def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, stream=No
 
 
 def pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
-                             stream=None) -> None:
+                             stream=None, _name="pa_reshape_and_cache_fp8") -> None:
     """Quantising append: ``k_new/v_new [T, Hkv, 128]`` fp16/bf16, caches
     ``[N, bs, Hkv, 128]`` uint8 (E4M3 codes), scales ``[N, Hkv, bs]`` float32."""
     import torch
     T, Hkv, d = k_new.shape
     N, bs = k_cache.shape[0], k_cache.shape[1]
-    _check(load().pa_reshape_and_cache_fp8(
+    _check(getattr(load(), _name)(
         _dev(k_new), _dev(v_new), _dev(slot_mapping, torch.int64), T, _dev(k_cache, torch.uint8),
         _dev(v_cache, torch.uint8), _dev(k_scale, torch.float32), _dev(v_scale, torch.float32),
-        N, bs, Hkv, d, _dtype_code(k_new), _stream_ptr(stream)), "pa_reshape_and_cache_fp8")
+        N, bs, Hkv, d, _dtype_code(k_new), _stream_ptr(stream)), _name)
+
+
+def pa_reshape_and_cache_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                              stream=None) -> None:
+    """``pa_reshape_and_cache_fp8`` with INT8 codes (the int8 bytes in uint8 tensors)."""
+    pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                             stream, _name="pa_reshape_and_cache_int8")
 
 
 def pa_copy_blocks(k_caches, v_caches, pairs, stream=None) -> None:
@@ -297,20 +308,28 @@ def pa_multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, max
 
 
 def pa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                  max_context_len: int, scale: float, out, workspace, stream=None) -> None:
+                  max_context_len: int, scale: float, out, workspace, stream=None,
+                  _name="pa_decode_fp8") -> None:
     """``pa_decode`` over an FP8 cache: ``k_cache/v_cache [N, bs, Hkv, 128]`` uint8
     codes and ``k_scale/v_scale [N, Hkv, bs]`` float32 scales."""
     import torch
     B, H, d = q.shape
     N, bs, Hkv, _ = k_cache.shape
-    _check(load().pa_decode_fp8(_dev(q), _dev(k_cache, torch.uint8), _dev(v_cache, torch.uint8),
+    _check(getattr(load(), _name)(_dev(q), _dev(k_cache, torch.uint8), _dev(v_cache, torch.uint8),
                                 _dev(k_scale, torch.float32), _dev(v_scale, torch.float32),
                                 _dev(block_tables, torch.int32), int(block_tables.shape[1]),
                                 _dev(context_lens, torch.int32), int(max_context_len), B, H, Hkv,
                                 d, bs, N, float(scale), _dtype_code(q), _dev(out),
                                 _dev(workspace), workspace.numel() * workspace.element_size(),
                                 _stream_ptr(stream)),
-           "pa_decode_fp8")
+           _name)
+
+
+def pa_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                   max_context_len: int, scale: float, out, workspace, stream=None) -> None:
+    """``pa_decode_fp8`` over an INT8 cache (from ``pa_reshape_and_cache_int8``)."""
+    pa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                  max_context_len, scale, out, workspace, stream, _name="pa_decode_int8")
 
 
 def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
@@ -515,23 +534,36 @@ class Step:
     host regions as tensors (``slot(i)``; ``q``, ``k_new``, ``v_new``, ``out``
     are slot 0's).  Fill a slot's inputs, then :meth:`run` (submit and wait),
     or :meth:`submit` / :meth:`wait` to overlap the next step's host work with
-    this one's device work.  With ``k_scale``/``v_scale`` the caches are FP8
-    codes (uint8) and ``dtype`` gives the 16-bit type of the inputs."""
+    this one's device work.  With ``kv_format`` "fp8" or "int8" the caches
+    are 8-bit codes (uint8) with ``k_scale``/``v_scale``, and ``dtype`` gives
+    the 16-bit type of the inputs."""
 
     def __init__(self, alloc: Allocator, B: int, H: int, Hkv: int, d: int, max_blocks: int,
                  max_context_len: int, k_cache, v_cache, scale: float, k_scale=None,
-                 v_scale=None, dtype=None, depth: int = 1):
+                 v_scale=None, dtype=None, depth: int = 1, kv_format: str = "native"):
         import torch
         self._lib = load()
         N, bs = int(k_cache.shape[0]), int(k_cache.shape[1])
         if tuple(k_cache.shape) != (N, bs, Hkv, d) or v_cache.shape != k_cache.shape:
             raise ValueError("caches must be [num_blocks, block_size, Hkv, d]")
-        fp8 = k_scale is not None
-        if fp8 and dtype not in (torch.float16, torch.bfloat16):
-            raise ValueError("an FP8 cache needs dtype, the 16-bit type of q and k/v_new")
-        dt = dtype if fp8 else k_cache.dtype
+        q8 = {"native": 0, "fp8": 1, "int8": 2}[kv_format]
+        if q8 and (k_scale is None or v_scale is None or
+                   dtype not in (torch.float16, torch.bfloat16)):
+            raise ValueError("an 8-bit cache needs k_scale, v_scale and dtype (of q, k/v_new)")
+        # the library sees raw pointers: a pool of the wrong element size
+        # would be written past its end, so the format must match the tensors
+        want = (torch.uint8,) if q8 else (torch.float16, torch.bfloat16)
+        if k_cache.dtype not in want or v_cache.dtype != k_cache.dtype:
+            raise ValueError("kv_format %r needs caches of %s, got %s" % (kv_format, want,
+                                                                         k_cache.dtype))
+        if not q8 and (k_scale is not None or v_scale is not None):
+            raise ValueError("scales given for a 16-bit cache: pass kv_format")
+        if q8 and (tuple(k_scale.shape) != (N, Hkv, bs) or tuple(v_scale.shape) != (N, Hkv, bs)
+                   or k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32):
+            raise ValueError("scales must be float32 [num_blocks, Hkv, block_size]")
+        dt = dtype if q8 else k_cache.dtype
         self.desc = StepDesc(B, H, Hkv, d, bs, N, max_blocks, max_context_len,
-                             PA_F16 if dt == torch.float16 else PA_BF16, scale, int(fp8), depth)
+                             PA_F16 if dt == torch.float16 else PA_BF16, scale, q8, depth)
         lay = StepLayout()
         _check(self._lib.pa_step_layout_get(ctypes.byref(self.desc), ctypes.byref(lay)),
                "pa_step_layout_get")
@@ -550,8 +582,8 @@ class Step:
         self._h = ctypes.c_void_p()
         _check(self._lib.pa_step_create(ctypes.byref(self.desc), alloc._h, _dev(k_cache),
                                         _dev(v_cache),
-                                        _dev(k_scale, torch.float32) if fp8 else None,
-                                        _dev(v_scale, torch.float32) if fp8 else None,
+                                        _dev(k_scale, torch.float32) if q8 else None,
+                                        _dev(v_scale, torch.float32) if q8 else None,
                                         self.host.data_ptr(), self.dev.data_ptr(),
                                         self.ws.data_ptr(), self.ws.numel(),
                                         ctypes.byref(self._h)), "pa_step_create")

@@ -50,6 +50,19 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Four fp32 values -> four INT8 codes (nearest integer, ties to even,
+// clamped to [-127, 127]); the first value goes to the low byte.
+__device__ __forceinline__ uint32_t s8x4(float a, float b, float c, float d) {
+    const float v[4] = {a, b, c, d};
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = max(-127, min(127, __float2int_rn(v[i])));
+        r |= ((uint32_t)q & 0xFFu) << (8 * i);
+    }
+    return r;
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>
@@ -57,14 +70,16 @@ __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// FP8 KV append: one warp per (token, KV head) row of 128 values, each lane
-// four consecutive values.  scale = fl32(amax / 448) and code =
-// e4m3_rne_sat(fl32(x / scale)) with IEEE fp32 division; an all-zero row gets
-// scale 0 and zero codes.  Codes go to cache[slot / bs][slot % bs][h][:], the
-// scale to scale[slot / bs][h][slot % bs].
-template <typename T>
+// 8-bit KV append: one warp per (token, KV head) row of 128 values, each lane
+// four consecutive values.  FP8: scale = fl32(amax / 448) and code =
+// e4m3_rne_sat(fl32(x / scale)); INT8 (kInt8): scale = fl32(amax / 127) and
+// code = the nearest integer of fl32(x / scale), ties to even, clamped to
+// +-127.  IEEE fp32 divisions; an all-zero row gets scale 0 and zero codes.
+// Codes go to cache[slot / bs][slot % bs][h][:], the scale to
+// scale[slot / bs][h][slot % bs].
+template <typename T, bool kInt8>
 __global__ void __launch_bounds__(kThreads)
-reshape_and_cache_fp8_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
+reshape_and_cache_q8_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
                              const int64_t* __restrict__ slot_mapping, int32_t T_tokens,
                              int32_t Hkv, int32_t block_size, uint32_t* __restrict__ k_cache,
                              uint32_t* __restrict__ v_cache, float* __restrict__ k_scale,
@@ -92,12 +107,17 @@ reshape_and_cache_fp8_kernel(const T* __restrict__ k_new, const T* __restrict__ 
             float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float s = __fdiv_rn(amax, 448.0f);
+            const float s = __fdiv_rn(amax, kInt8 ? 127.0f : 448.0f);
             uint32_t packed = 0;
             if (s != 0.f) {
-                const uint16_t lo = e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
-                const uint16_t hi = e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
-                packed = (uint32_t)lo | ((uint32_t)hi << 16);
+                if constexpr (kInt8) {
+                    packed = s8x4(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s), __fdiv_rn(x[2], s),
+                                  __fdiv_rn(x[3], s));
+                } else {
+                    const uint16_t lo = e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+                    const uint16_t hi = e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+                    packed = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
             }
             uint32_t* dst = (which ? v_cache : k_cache) + (slot * Hkv + h) * 32 + lane;
             *dst = packed;
@@ -201,11 +221,15 @@ PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
     return pa::cuda_status(cudaGetLastError());
 }
 
-PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
-                                          const int64_t* slot_mapping, int32_t T, void* k_cache,
-                                          void* v_cache, float* k_scale, float* v_scale,
-                                          int32_t num_blocks, int32_t block_size, int32_t Hkv,
-                                          int32_t d, pa_dtype dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+template <bool kInt8>
+pa_status reshape_and_cache_q8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               int32_t T, void* k_cache, void* v_cache, float* k_scale,
+                               float* v_scale, int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                               int32_t d, pa_dtype dtype, void* stream) {
     if (T < 0 || num_blocks < 0 || block_size <= 0 || Hkv <= 0) return PA_ERR_INVALID;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (d != 128) return PA_ERR_UNSUPPORTED;
@@ -224,16 +248,38 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t slots = (int64_t)num_blocks * block_size;
     if (dtype == PA_BF16)
-        reshape_and_cache_fp8_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, st>>>(
+        reshape_and_cache_q8_kernel<__nv_bfloat16, kInt8><<<(unsigned)blocks, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
             slot_mapping, T, Hkv, block_size, static_cast<uint32_t*>(k_cache),
             static_cast<uint32_t*>(v_cache), k_scale, v_scale, slots, err);
     else
-        reshape_and_cache_fp8_kernel<__half><<<(unsigned)blocks, kThreads, 0, st>>>(
+        reshape_and_cache_q8_kernel<__half, kInt8><<<(unsigned)blocks, kThreads, 0, st>>>(
             static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), slot_mapping, T,
             Hkv, block_size, static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache),
             k_scale, v_scale, slots, err);
     return pa::cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                          void* v_cache, float* k_scale, float* v_scale,
+                                          int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                                          int32_t d, pa_dtype dtype, void* stream) {
+    return reshape_and_cache_q8<false>(k_new, v_new, slot_mapping, T, k_cache, v_cache, k_scale,
+                                       v_scale, num_blocks, block_size, Hkv, d, dtype, stream);
+}
+
+PA_API pa_status pa_reshape_and_cache_int8(const void* k_new, const void* v_new,
+                                           const int64_t* slot_mapping, int32_t T, void* k_cache,
+                                           void* v_cache, float* k_scale, float* v_scale,
+                                           int32_t num_blocks, int32_t block_size, int32_t Hkv,
+                                           int32_t d, pa_dtype dtype, void* stream) {
+    return reshape_and_cache_q8<true>(k_new, v_new, slot_mapping, T, k_cache, v_cache, k_scale,
+                                      v_scale, num_blocks, block_size, Hkv, d, dtype, stream);
 }
 
 PA_API pa_status pa_swap_blocks(const void* const* src_pools, void* const* dst_pools,

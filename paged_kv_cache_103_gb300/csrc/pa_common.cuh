@@ -155,6 +155,17 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t& lo, uint32_t
         : "r"(x));
 }
 
+// Four INT8 codes (two's complement, the first in the low byte) as two f16x2
+// registers, exactly: each byte b is placed under the exponent of 1024, giving
+// the f16 1024 + (b ^ 0x80) = 1152 + b, and 1152 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = x ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);   // bytes 0 and 1
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);   // bytes 2 and 3
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 // 2^k as a float for an integer k in [-126, 127].
 __device__ __forceinline__ float exp2_int(int k) { return __int_as_float((127 + k) << 23); }
 

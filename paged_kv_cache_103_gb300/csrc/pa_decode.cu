@@ -195,7 +195,16 @@ __device__ __forceinline__ uint32_t tile_offset(uint32_t t, uint32_t h, uint32_t
 
 // kFp8: the cache holds E4M3 codes with per-(token, KV head) scales (ksmap,
 // vsmap); otherwise the cache has the dtype of q and the scale maps are unused.
-template <int D, bool kBF16, int NT, bool kAsync, bool kFp8>
+// Four 8-bit codes as two f16x2 registers: E4M3, or INT8 (kInt8).
+template <bool kInt8>
+__device__ __forceinline__ void q8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    if constexpr (kInt8)
+        pa::s8x4_to_f16(x, lo, hi);
+    else
+        pa::e4m3x4_to_f16(x, lo, hi);
+}
+
+template <int D, bool kBF16, int NT, bool kAsync, bool kFp8, bool kInt8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
@@ -741,8 +750,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             uint32_t a[4];
-                            pa::e4m3x4_to_f16(u4_word(w[0][ks >> 2], ks & 3), a[0], a[2]);
-                            pa::e4m3x4_to_f16(u4_word(w[1][ks >> 2], ks & 3), a[1], a[3]);
+                            q8x4_to_f16<kInt8>(u4_word(w[0][ks >> 2], ks & 3), a[0], a[2]);
+                            q8x4_to_f16<kInt8>(u4_word(w[1][ks >> 2], ks & 3), a[1], a[3]);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
                                 pa::mma_16816<false>(st[mt][nt], a, qb[nt][ks][0], qb[nt][ks][1]);
@@ -880,8 +889,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                 const uint32_t x = q4 ? src[2 * (u >> 1)].y : src[2 * (u >> 1)].x;
                                 const uint32_t y =
                                     q4 ? src[2 * (u >> 1) + 1].y : src[2 * (u >> 1) + 1].x;
-                                pa::e4m3x4_to_f16(__byte_perm(x, y, 0x5140), af[u][0], af[u][1]);
-                                pa::e4m3x4_to_f16(__byte_perm(x, y, 0x7362), af[u][2], af[u][3]);
+                                q8x4_to_f16<kInt8>(__byte_perm(x, y, 0x5140), af[u][0], af[u][1]);
+                                q8x4_to_f16<kInt8>(__byte_perm(x, y, 0x7362), af[u][2], af[u][3]);
                             }
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -1141,11 +1150,11 @@ int choose_stages(int D, int G, int B, bool fp8, int bs) {
     return s;
 }
 
-template <int D, bool kBF16, int NT, bool kAsync, bool kFp8>
+template <int D, bool kBF16, int NT, bool kAsync, bool kFp8, bool kInt8>
 pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& ksm,
                  const CUtensorMap& vsm, const DecodeParams& prm, size_t smem,
                  cudaStream_t stream) {
-    auto kern = paged_decode_kernel<D, kBF16, NT, kAsync, kFp8>;
+    auto kern = paged_decode_kernel<D, kBF16, NT, kAsync, kFp8, kInt8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1157,14 +1166,15 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap
     return pa::cuda_status(cudaGetLastError());
 }
 
-template <int D, bool kBF16, bool kFp8>
+template <int D, bool kBF16, bool kFp8, bool kInt8 = false>
 pa_status launch_g(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& ksm,
                    const CUtensorMap& vsm, const DecodeParams& prm, size_t smem,
                    cudaStream_t stream) {
     if (async_merge(prm.G))
-        return launch<D, kBF16, 1, true, kFp8>(km, vm, ksm, vsm, prm, smem, stream);
-    return prm.G <= 8 ? launch<D, kBF16, 1, false, kFp8>(km, vm, ksm, vsm, prm, smem, stream)
-                      : launch<D, kBF16, 2, false, kFp8>(km, vm, ksm, vsm, prm, smem, stream);
+        return launch<D, kBF16, 1, true, kFp8, kInt8>(km, vm, ksm, vsm, prm, smem, stream);
+    return prm.G <= 8
+               ? launch<D, kBF16, 1, false, kFp8, kInt8>(km, vm, ksm, vsm, prm, smem, stream)
+               : launch<D, kBF16, 2, false, kFp8, kInt8>(km, vm, ksm, vsm, prm, smem, stream);
 }
 
 // Checks shared by pa_decode and pa_decode_fp8; fills everything of prm but the
@@ -1267,13 +1277,19 @@ PA_API pa_status pa_decode(const void* q, const void* k_cache, const void* v_cac
                             : launch_g<64, false, false>(km, vm, km, vm, prm, smem, st);
 }
 
-PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
-                               const float* k_scale, const float* v_scale,
-                               const int32_t* block_tables, int32_t max_blocks,
-                               const int32_t* context_lens, int32_t max_context_len, int32_t B,
-                               int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
-                               int32_t num_blocks, float scale, pa_dtype dtype, void* out,
-                               void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// pa_decode_fp8 and pa_decode_int8: the decode over an 8-bit cache of E4M3
+// (kInt8 false) or INT8 codes with per-(token, KV head) scales.
+template <bool kInt8>
+pa_status decode_q8(const void* q, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                    int32_t max_blocks, const int32_t* context_lens, int32_t max_context_len,
+                    int32_t B, int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                    int32_t num_blocks, float scale, pa_dtype dtype, void* out, void* workspace,
+                    size_t ws_bytes, void* stream) {
     DecodeParams prm;
     size_t smem = 0;
     const pa_status st0 = prepare(max_blocks, max_context_len, B, H, Hkv, d, block_size,
@@ -1310,8 +1326,36 @@ PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v
     prm.err = err;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return dtype == PA_BF16 ? launch_g<128, true, true>(km, vm, ksm, vsm, prm, smem, st)
-                            : launch_g<128, false, true>(km, vm, ksm, vsm, prm, smem, st);
+    return dtype == PA_BF16 ? launch_g<128, true, true, kInt8>(km, vm, ksm, vsm, prm, smem, st)
+                            : launch_g<128, false, true, kInt8>(km, vm, ksm, vsm, prm, smem, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                               int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                               int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    return decode_q8<false>(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks,
+                            context_lens, max_context_len, B, H, Hkv, d, block_size, num_blocks,
+                            scale, dtype, out, workspace, ws_bytes, stream);
+}
+
+PA_API pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, int32_t max_blocks,
+                                const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                                int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                                int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    return decode_q8<true>(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks,
+                           context_lens, max_context_len, B, H, Hkv, d, block_size, num_blocks,
+                           scale, dtype, out, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -29,8 +29,8 @@ bool desc_ok(const pa_step_desc* d) {
            (d->block_size == 8 || d->block_size == 16 || d->block_size == 32) &&
            d->num_blocks > 0 && d->max_blocks > 0 && d->max_context_len > 0 &&
            (int64_t)d->max_context_len <= (int64_t)d->max_blocks * d->block_size &&
-           (d->dtype == PA_F16 || d->dtype == PA_BF16) && (d->fp8 == 0 || d->fp8 == 1) &&
-           (d->fp8 == 0 || d->d == 128) && d->depth >= 1 && d->depth <= kMaxDepth;
+           (d->dtype == PA_F16 || d->dtype == PA_BF16) && d->q8 >= 0 && d->q8 <= 2 &&
+           (d->q8 == 0 || d->d == 128) && d->depth >= 1 && d->depth <= kMaxDepth;
 }
 
 }  // namespace
@@ -41,7 +41,7 @@ struct pa_step {
     pa_allocator* alloc;
     void* k_cache;
     void* v_cache;
-    float* k_scale;         // FP8 caches only
+    float* k_scale;         // 8-bit caches only
     float* v_scale;
     unsigned char* host;    // pinned staging, depth slots
     unsigned char* dev;     // device staging, depth slots
@@ -78,15 +78,15 @@ pa_status capture(pa_step* s, int i, void* workspace, size_t ws_bytes, cudaStrea
     const int64_t* slots = reinterpret_cast<const int64_t*>(g + L.slot_mapping);
     const int32_t* tables = reinterpret_cast<const int32_t*>(g + L.block_tables);
     const int32_t* lens = reinterpret_cast<const int32_t*>(g + L.context_lens);
-    if (st == PA_OK && d->fp8)
-        st = pa_reshape_and_cache_fp8(g + L.k_new, g + L.v_new, slots, d->B, s->k_cache,
+    if (st == PA_OK && d->q8)
+        st = (d->q8 == 1 ? pa_reshape_and_cache_fp8 : pa_reshape_and_cache_int8)(g + L.k_new, g + L.v_new, slots, d->B, s->k_cache,
                                       s->v_cache, s->k_scale, s->v_scale, d->num_blocks,
                                       d->block_size, d->Hkv, d->d, d->dtype, cap);
     else if (st == PA_OK)
         st = pa_reshape_and_cache(g + L.k_new, g + L.v_new, slots, d->B, s->k_cache, s->v_cache,
                                   d->num_blocks, d->block_size, d->Hkv, d->d, d->dtype, cap);
-    if (st == PA_OK && d->fp8)
-        st = pa_decode_fp8(g + L.q, s->k_cache, s->v_cache, s->k_scale, s->v_scale, tables,
+    if (st == PA_OK && d->q8)
+        st = (d->q8 == 1 ? pa_decode_fp8 : pa_decode_int8)(g + L.q, s->k_cache, s->v_cache, s->k_scale, s->v_scale, tables,
                            d->max_blocks, lens, d->max_context_len, d->B, d->H, d->Hkv, d->d,
                            d->block_size, d->num_blocks, d->scale, d->dtype, g + L.out, workspace,
                            ws_bytes, cap);
@@ -143,7 +143,7 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
     if (!desc_ok(d) || !alloc || !k_cache || !v_cache || !host_stage || !dev_stage ||
         !workspace || !out)
         return PA_ERR_INVALID;
-    if (d->fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+    if (d->q8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(host_stage) | reinterpret_cast<uintptr_t>(dev_stage)) & 255u)
         return PA_ERR_INVALID;
     if (ws_bytes < pa_decode_workspace_size(d->B, d->H, d->d)) return PA_ERR_INVALID;
@@ -155,11 +155,11 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
     s->alloc = alloc;
     s->k_cache = k_cache;
     s->v_cache = v_cache;
-    s->k_scale = d->fp8 ? k_scale : nullptr;
-    s->v_scale = d->fp8 ? v_scale : nullptr;
+    s->k_scale = d->q8 ? k_scale : nullptr;
+    s->v_scale = d->q8 ? v_scale : nullptr;
     s->host = static_cast<unsigned char*>(host_stage);
     s->dev = static_cast<unsigned char*>(dev_stage);
-    s->block_bytes = (int64_t)d->block_size * d->Hkv * d->d * (d->fp8 ? 1 : 2);
+    s->block_bytes = (int64_t)d->block_size * d->Hkv * d->d * (d->q8 ? 1 : 2);
     s->submitted = 0;
     for (int i = 0; i < kMaxDepth; ++i) {
         s->exec[i] = nullptr;
@@ -224,6 +224,27 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
                    reinterpret_cast<int32_t*>(h + L.block_tables),
                    reinterpret_cast<int32_t*>(h + L.context_lens));
     if (st != PA_OK) return st;
+    // What the graph will read, checked on the host before anything launches:
+    // every new slot inside the pool, every used table entry a pool block.
+    {
+        const int64_t* sm = reinterpret_cast<const int64_t*>(h + L.slot_mapping);
+        const int32_t* tb = reinterpret_cast<const int32_t*>(h + L.block_tables);
+        const int32_t* ln = reinterpret_cast<const int32_t*>(h + L.context_lens);
+        const int64_t nslots = (int64_t)d.num_blocks * d.block_size;
+        for (int32_t i = 0; i < d.B; ++i) {
+            if (sm[i] < 0 || sm[i] >= nslots || ln[i] < 1 || ln[i] > d.max_context_len)
+                return PA_ERR_BOUNDS;
+            const int32_t used = (ln[i] + d.block_size - 1) / d.block_size;
+            for (int32_t j = 0; j < used; ++j) {
+                const int32_t b = tb[(int64_t)i * d.max_blocks + j];
+                if (b < 0 || b >= d.num_blocks) return PA_ERR_BOUNDS;
+            }
+        }
+        for (int32_t p = 0; p < ncow; ++p)
+            if (pairs[2 * p] < 0 || pairs[2 * p] >= d.num_blocks || pairs[2 * p + 1] < 0 ||
+                pairs[2 * p + 1] >= d.num_blocks)
+                return PA_ERR_BOUNDS;
+    }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (ncow > 0) {
         // Copy-on-write before the step's append writes the new token.
@@ -235,7 +256,7 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
         void* vc = s->v_cache;
         st = pa_copy_blocks(&kc, &vc, 1, dpairs, ncow, s->block_bytes, d.num_blocks, cs);
         if (st != PA_OK) return st;
-        if (d.fp8) {   // and the blocks' scales, [num_blocks][Hkv][block_size] fp32
+        if (d.q8) {   // and the blocks' scales, [num_blocks][Hkv][block_size] fp32
             void* ks = s->k_scale;
             void* vs = s->v_scale;
             st = pa_copy_blocks(&ks, &vs, 1, dpairs, ncow, (int64_t)d.Hkv * d.block_size * 4,

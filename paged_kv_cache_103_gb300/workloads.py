@@ -232,6 +232,22 @@ def fp8_cache(w: Workload, seed_offset: int = 0):
     return out
 
 
+def int8_cache(w: Workload, seed_offset: int = 0):
+    """Seeded INT8 cache contents on the host, drawn directly: codes
+    ``[N,bs,Hkv,d]`` (int8 values uniform over -127..127, stored as uint8
+    bytes) and ``k_scale``/``v_scale [N,Hkv,bs]`` float32 uniform in
+    [0.014, 0.042] (the size of amax / 127 for N(0, 1) rows of 128)."""
+    rng = np.random.default_rng(w.seed * 16 + 7 + seed_offset)
+    shape = (w.num_blocks, w.block_size, w.Hkv, w.d)
+    out = {}
+    for name in ("k", "v"):
+        codes = rng.integers(-127, 128, size=shape, dtype=np.int64).astype(np.int8)
+        out[name + "_codes"] = torch.from_numpy(codes.view(np.uint8))
+        out[name + "_scale"] = torch.from_numpy(
+            rng.uniform(0.014, 0.042, size=(w.num_blocks, w.Hkv, w.block_size)).astype(np.float32))
+    return out
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """The uint16 bit patterns of an fp16 / bf16 host tensor (no copy)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -110,7 +110,7 @@ def test_step_layout_and_argument_checks(lib):
     assert L.in_bytes == L.cow_pairs and L.in_bytes >= L.context_lens + sizes["context_lens"]
     assert L.out - L.cow_pairs >= 64 * 2 * 4 and L.total >= L.out + sizes["out"]
     for field, bad in [("max_context_len", 2049), ("d", 96), ("block_size", 64), ("B", 0),
-                       ("Hkv", 3), ("dtype", 7), ("fp8", 2), ("depth", 0), ("depth", 3)]:
+                       ("Hkv", 3), ("dtype", 7), ("q8", 3), ("depth", 0), ("depth", 3)]:
         e = binding.StepDesc(64, 40, 40, 128, 16, 5240, 128, 2048, 0, 0.088, 0, 1)
         setattr(e, field, bad)
         assert lib.pa_step_layout_get(ctypes.byref(e), ctypes.byref(L)) == 1, field
@@ -123,3 +123,26 @@ def test_step_layout_and_argument_checks(lib):
     assert lib.pa_step_run(None, None, None) == 1
     assert lib.pa_step_submit(None, None, None, None) == 1
     assert lib.pa_step_wait(None, 0) == 1
+
+
+def test_step_refuses_a_cache_of_the_wrong_format(lib):
+    """The executor takes raw pool pointers, so the binding checks that the
+    cache tensors match kv_format before anything reaches the library: an
+    8-bit pool read as a 16-bit one would be written past its end."""
+    import torch
+    N, bs, Hkv, d = 8, 16, 2, 128
+    u8 = torch.zeros((N, bs, Hkv, d), dtype=torch.uint8)
+    f16 = torch.zeros((N, bs, Hkv, d), dtype=torch.float16)
+    sc = torch.zeros((N, Hkv, bs), dtype=torch.float32)
+    alloc = binding.Allocator(N, bs)
+    cases = [dict(k_cache=u8, v_cache=u8, k_scale=sc, v_scale=sc, dtype=torch.bfloat16),
+             dict(k_cache=u8, v_cache=u8),
+             dict(k_cache=f16, v_cache=f16, k_scale=sc, v_scale=sc, dtype=torch.float16,
+                  kv_format="int8"),
+             dict(k_cache=u8, v_cache=u8, k_scale=sc[:, :1], v_scale=sc, dtype=torch.float16,
+                  kv_format="fp8"),
+             dict(k_cache=u8, v_cache=u8, k_scale=sc.double(), v_scale=sc.double(),
+                  dtype=torch.float16, kv_format="int8")]
+    for kw in cases:
+        with pytest.raises(ValueError):
+            binding.Step(alloc, 2, 4, Hkv, d, 4, 64, scale=0.1, **kw)

@@ -131,9 +131,11 @@ def test_bound_refusal_changes_nothing():
     step.close()
 
 
-def test_fp8_cache_with_copy_on_write():
-    """The same step over an FP8 cache: forks share a partial last block, so
-    the first step copies codes and scales before quantising the new rows."""
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_8bit_cache_with_copy_on_write(fmt):
+    """The same step over an FP8 or INT8 cache: forks share a partial last
+    block, so the first step copies codes and scales before quantising the
+    new rows."""
     B, H, Hkv, d, bs, N = 6, 8, 2, 128, 16, 40
 
     def setup(a):
@@ -147,10 +149,11 @@ def test_fp8_cache_with_copy_on_write():
     setup(cpp)
     setup(model)
     w = wl.Workload("fp8_step", B, H, Hkv, d, bs, "bf16", np.full(B, 37, np.int32), N, order, 13)
-    c = wl.fp8_cache(w)
+    c = wl.fp8_cache(w) if fmt == "fp8" else wl.int8_cache(w)
     dev = {k: v.cuda() for k, v in c.items()}
     step = binding.Step(cpp, B, H, Hkv, d, 4, 64, dev["k_codes"], dev["v_codes"], 0.09,
-                        k_scale=dev["k_scale"], v_scale=dev["v_scale"], dtype=torch.bfloat16)
+                        k_scale=dev["k_scale"], v_scale=dev["v_scale"], dtype=torch.bfloat16,
+                        kv_format=fmt)
     ids = [4, 1, 0, 5, 3, 2]
     for k in range(2):
         q = wl.normal_tensor((B, H, d), torch.bfloat16, 40 + k)
@@ -165,17 +168,17 @@ def test_fp8_cache_with_copy_on_write():
         assert len(pairs) == (B - 1 if k == 0 else 0)
         if pairs:
             oracle.copy_blocks([c["k_codes"], c["k_scale"]], [c["v_codes"], c["v_scale"]], pairs)
-        oracle.reshape_and_cache_fp8(kn, vn, np.asarray(slots, np.int64), c["k_codes"].numpy(),
-                                     c["v_codes"].numpy(), c["k_scale"].numpy(),
-                                     c["v_scale"].numpy())
+        getattr(oracle, "reshape_and_cache_" + fmt)(
+            kn, vn, np.asarray(slots, np.int64), c["k_codes"].numpy(), c["v_codes"].numpy(),
+            c["k_scale"].numpy(), c["v_scale"].numpy())
         for name in c:
             assert torch.equal(dev[name].cpu(), c[name]), (k, name)
         tbl, lens = model.export(ids, 4)
         assert np.array_equal(step.block_tables.numpy(), tbl)
-        ref = oracle.decode_fp8(wl.bits(q), oracle.DTYPE_BF16, c["k_codes"].numpy(),
-                                c["v_codes"].numpy(), c["k_scale"].numpy(), c["v_scale"].numpy(),
-                                tbl, lens, 0.09)
-        assert_close(step.out.clone(), ref, "fp8 step %d" % k)
+        ref = getattr(oracle, "decode_" + fmt)(wl.bits(q), oracle.DTYPE_BF16, c["k_codes"].numpy(),
+                                               c["v_codes"].numpy(), c["k_scale"].numpy(),
+                                               c["v_scale"].numpy(), tbl, lens, 0.09)
+        assert_close(step.out.clone(), ref, "%s step %d" % (fmt, k))
     step.close()
 
 
