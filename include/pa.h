@@ -519,7 +519,8 @@ PA_API pa_status pa_step_layout_get(const pa_step_desc* desc, pa_step_layout* ou
  * k_scale / v_scale [num_blocks][Hkv][block_size] fp32; the scales are NULL
  * otherwise) and the allocator alloc (all must outlive it).  workspace (device, >= pa_decode_workspace_size(B, H, d) bytes, zeroed
  * once) is the decode's.  Captures the graph on a private stream; nothing
- * runs.  PA_ERR_INVALID for bad arguments or misaligned staging. */
+ * runs.  PA_ERR_INVALID for bad arguments, misaligned staging, or an allocator
+ * whose pool size or block size differs from desc's. */
 PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, void* k_cache,
                                 void* v_cache, float* k_scale, float* v_scale, void* host_stage,
                                 void* dev_stage, void* workspace, size_t ws_bytes,

@@ -147,6 +147,11 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
     if ((reinterpret_cast<uintptr_t>(host_stage) | reinterpret_cast<uintptr_t>(dev_stage)) & 255u)
         return PA_ERR_INVALID;
     if (ws_bytes < pa_decode_workspace_size(d->B, d->H, d->d)) return PA_ERR_INVALID;
+    // the allocator's pool must be the cache's: its blocks and slots index it
+    pa_alloc_stats as;
+    if (pa_alloc_stats_get(alloc, &as) != PA_OK || as.num_blocks != d->num_blocks ||
+        as.block_size != d->block_size)
+        return PA_ERR_INVALID;
     *out = nullptr;
     pa_step* s = new (std::nothrow) pa_step;
     if (!s) return PA_ERR_OOM;

@@ -146,3 +146,19 @@ def test_step_refuses_a_cache_of_the_wrong_format(lib):
     for kw in cases:
         with pytest.raises(ValueError):
             binding.Step(alloc, 2, 4, Hkv, d, 4, 64, scale=0.1, **kw)
+
+
+def test_step_create_refuses_an_allocator_of_another_pool(lib):
+    """The executor indexes the cache with the allocator's blocks and slots, so
+    an allocator whose pool or block size differs from the description is
+    refused before anything touches a pointer (the pointers here are never
+    dereferenced)."""
+    fake = ctypes.c_void_p(1 << 20)                     # 256-byte aligned, never used
+    ws = lib.pa_decode_workspace_size(4, 8, 128)
+    for n, bs in [(64, 16), (32, 8)]:                   # the description says 32 x 16
+        a = binding.Allocator(n, bs)
+        d = binding.StepDesc(4, 8, 2, 128, 16, 32, 8, 128, 0, 0.088, 0, 1)
+        h = ctypes.c_void_p()
+        assert lib.pa_step_create(ctypes.byref(d), a._h, fake, fake, None, None, fake, fake, fake,
+                                  ws, ctypes.byref(h)) == 1
+        assert not h.value
