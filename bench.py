@@ -466,11 +466,12 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
     """Real decode steps through the C ABI with host buffers.  Each step is
     pa_step_submit: the host allocator appends one token per sequence
     (pa_append_batch) and exports the tables (pa_export) into a pinned staging
-    slot, then the executor's CUDA graph for that slot runs -- one
-    host->device copy of q / new K / new V / slots / tables / lengths, the
-    append, the decode, one device->host copy of the output -- and the host
-    waits for each step's output (pa_step_wait).  Two slots let step k + 1's
-    host work overlap step k's device work; a second loop runs the same steps
+    slot, then one host->device copy of q / new K / new V / slots / tables /
+    lengths (the executor's copy-in stream), the executor's CUDA graph of the
+    append and the decode, and one device->host copy of the output (its
+    copy-out stream); the host waits for each step's output (pa_step_wait).
+    Two slots let step k + 1's host work and input copy overlap step k's
+    decode; a second loop runs the same steps
     with a wait after every submit (pa_step_run), reported as "synchronous".
     The inputs are written into both pinned slots once (the same synthetic
     rows every step); each step still copies them to the device.
@@ -529,10 +530,11 @@ def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs)
                             "ms_per_step": round((t2 - t1) * 1e3 / steps, 4),
                             "includes": "the same steps with a wait after every submit"},
             "includes": "per step (C ABI) pa_step_submit: host pa_append_batch + pa_export into "
-                        "a pinned staging slot, then the library's CUDA graph: one pinned H2D of "
-                        "q/k_new/v_new/slots/tables/lens, reshape_and_cache%s, decode%s, one D2H "
-                        "of out; pa_step_wait for every step's output (two slots: step k+1's "
-                        "host work overlaps step k on the device)"
+                        "a pinned staging slot, one pinned H2D of q/k_new/v_new/slots/tables/lens "
+                        "(copy-in stream), the library's CUDA graph of reshape_and_cache%s and "
+                        "decode%s, one D2H of out (copy-out stream); pa_step_wait for every "
+                        "step's output (two slots: step k+1's host work and input copy overlap "
+                        "step k's decode, step k's output copy overlaps step k+1's)"
                         % (("_" + args.kv_format,) * 2 if fp8 else ("", ""))}
 
 

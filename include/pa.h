@@ -474,8 +474,12 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * step's inputs and tables, pa_copy_blocks when copy-on-write arises,
  * pa_reshape_and_cache, pa_decode and one device->host copy of the output
  * (their _fp8 / _int8 forms over an 8-bit cache).
- * The copies and the two kernels are captured once, at creation, into a CUDA
- * graph owned by the executor and replayed every step.  The caller owns the
+ * The two kernels are captured once per slot, at creation, into a CUDA graph
+ * owned by the executor and replayed every step on the caller's stream; the
+ * input copy runs on the executor's own copy-in stream and the output copy on
+ * its copy-out stream, so a step's inputs travel while the previous step's
+ * decode runs and its output travels while the next one's does.  The caller
+ * owns the
  * staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
  * torch tensor) and a device buffer, each desc.depth slots of
  * pa_step_layout.total bytes (slot i at byte i * total), 256-byte aligned.
@@ -527,20 +531,26 @@ PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, v
                                 pa_step** out);
 
 /* Submits one decode step for the B sequences seq_ids (host) without waiting
- * for it: in slot n % depth (n = steps submitted so far; *slot receives it,
- * nullable) -- after waiting for the step that last used that slot -- appends
- * one token to each sequence (pa_append_batch), issues the copy-on-write
- * copies that needs, exports the tables and launches the slot's graph on
- * `stream`.  A sequence whose length after the append would exceed
- * max_context_len or max_blocks * block_size returns PA_ERR_BOUNDS before
- * anything changes; allocator errors are those of pa_append_batch (all or
- * nothing); after a later failure (PA_ERR_CUDA from a launch) the appends
- * stay done.  Write a step's inputs into its slot before submitting it, and
- * only once the slot's previous step is done (pa_step_wait). */
+ * for it, in slot n % depth (n = steps submitted so far; *slot receives it,
+ * nullable), after waiting for the step that last used that slot: appends one
+ * token to each sequence (pa_append_batch), exports the tables, copies the
+ * slot's inputs to the device on the copy-in stream, and on `stream` -- once
+ * they are there -- issues the copy-on-write copies the appends need and
+ * launches the slot's graph; the output copy follows on the copy-out stream.
+ * Work the caller later orders on `stream` runs after the step's decode but
+ * not necessarily after its output copy: pa_step_wait is what guarantees the
+ * output is on the host.  A sequence whose length after the append would
+ * exceed max_context_len or max_blocks * block_size returns PA_ERR_BOUNDS
+ * before anything changes; allocator errors are those of pa_append_batch (all
+ * or nothing).  After the appends, a slot, table entry or copy pair outside
+ * the pool (an allocator that does not match the cache) returns PA_ERR_BOUNDS
+ * and a failed CUDA call PA_ERR_CUDA, both before any launch, with the appends
+ * done.  Write a step's inputs into its slot before submitting it, and only
+ * once the slot's previous step is done (pa_step_wait). */
 PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream, int32_t* slot);
 
 /* Waits for the last step submitted in `slot`; its output is then in the
- * slot's host region. */
+ * slot's host region.  PA_ERR_INVALID for a slot outside 0 .. depth - 1. */
 PA_API pa_status pa_step_wait(pa_step* s, int32_t slot);
 
 /* pa_step_submit followed by pa_step_wait of its slot. */

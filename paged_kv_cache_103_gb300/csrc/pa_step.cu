@@ -47,8 +47,12 @@ struct pa_step {
     unsigned char* dev;     // device staging, depth slots
     int64_t block_bytes;    // one block of one cache (codes for FP8)
     int64_t submitted;      // steps submitted so far (the next uses slot submitted % depth)
-    cudaGraphExec_t exec[kMaxDepth];
-    cudaEvent_t done[kMaxDepth];
+    cudaStream_t in_stream;   // host->device copies of the inputs
+    cudaStream_t out_stream;  // device->host copies of the outputs
+    cudaGraphExec_t exec[kMaxDepth];  // per slot: the append and the decode
+    cudaEvent_t in_done[kMaxDepth];   // the slot's inputs are on the device
+    cudaEvent_t comp_done[kMaxDepth]; // the slot's decode has finished
+    cudaEvent_t done[kMaxDepth];      // the slot's output is on the host
     bool pending[kMaxDepth];
 };
 
@@ -58,23 +62,26 @@ void release(pa_step* s) {
     for (int i = 0; i < kMaxDepth; ++i) {
         if (s->pending[i]) cudaEventSynchronize(s->done[i]);
         if (s->exec[i]) cudaGraphExecDestroy(s->exec[i]);
+        if (s->in_done[i]) cudaEventDestroy(s->in_done[i]);
+        if (s->comp_done[i]) cudaEventDestroy(s->comp_done[i]);
         if (s->done[i]) cudaEventDestroy(s->done[i]);
     }
+    if (s->in_stream) cudaStreamDestroy(s->in_stream);
+    if (s->out_stream) cudaStreamDestroy(s->out_stream);
     delete s;
 }
 
-// Captures slot i's graph on the private stream cap: H2D of the slot's
-// inputs, the append, the decode, D2H of the slot's output.
+// Captures slot i's graph on the private stream cap: the append and the
+// decode over the slot's device staging.  The copies in and out are issued
+// per step on the executor's copy streams (pa_step_submit), so that the next
+// step's inputs travel while this step's decode runs.
 pa_status capture(pa_step* s, int i, void* workspace, size_t ws_bytes, cudaStream_t cap) {
     const pa_step_desc* d = &s->desc;
     const pa_step_layout& L = s->lay;
-    unsigned char* h = s->host + (size_t)i * L.total;
     unsigned char* g = s->dev + (size_t)i * L.total;
     pa_status st = PA_OK;
     cudaGraph_t graph = nullptr;
     if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) return PA_ERR_CUDA;
-    if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, cap) != cudaSuccess)
-        st = PA_ERR_CUDA;
     const int64_t* slots = reinterpret_cast<const int64_t*>(g + L.slot_mapping);
     const int32_t* tables = reinterpret_cast<const int32_t*>(g + L.block_tables);
     const int32_t* lens = reinterpret_cast<const int32_t*>(g + L.context_lens);
@@ -94,10 +101,6 @@ pa_status capture(pa_step* s, int i, void* workspace, size_t ws_bytes, cudaStrea
         st = pa_decode(g + L.q, s->k_cache, s->v_cache, tables, d->max_blocks, lens,
                        d->max_context_len, d->B, d->H, d->Hkv, d->d, d->block_size, d->num_blocks,
                        d->scale, d->dtype, g + L.out, workspace, ws_bytes, cap);
-    if (st == PA_OK &&
-        cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d->B * d->H * d->d * 2,
-                        cudaMemcpyDeviceToHost, cap) != cudaSuccess)
-        st = PA_ERR_CUDA;
     // End the capture whatever happened, so the stream is usable again.
     if (cudaStreamEndCapture(cap, &graph) != cudaSuccess && st == PA_OK) st = PA_ERR_CUDA;
     if (st == PA_OK && cudaGraphInstantiate(&s->exec[i], graph, 0) != cudaSuccess) st = PA_ERR_CUDA;
@@ -166,9 +169,10 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
     s->dev = static_cast<unsigned char*>(dev_stage);
     s->block_bytes = (int64_t)d->block_size * d->Hkv * d->d * (d->q8 ? 1 : 2);
     s->submitted = 0;
+    s->in_stream = s->out_stream = nullptr;
     for (int i = 0; i < kMaxDepth; ++i) {
         s->exec[i] = nullptr;
-        s->done[i] = nullptr;
+        s->in_done[i] = s->comp_done[i] = s->done[i] = nullptr;
         s->pending[i] = false;
     }
     // One-time set-up of the device error word and SM count, outside the capture.
@@ -183,8 +187,13 @@ PA_API pa_status pa_step_create(const pa_step_desc* d, pa_allocator* alloc, void
         return PA_ERR_CUDA;
     }
     pa_status st = PA_OK;
+    if (cudaStreamCreateWithFlags(&s->in_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s->out_stream, cudaStreamNonBlocking) != cudaSuccess)
+        st = PA_ERR_CUDA;
     for (int i = 0; i < d->depth && st == PA_OK; ++i) {
-        if (cudaEventCreateWithFlags(&s->done[i], cudaEventDisableTiming) != cudaSuccess)
+        if (cudaEventCreateWithFlags(&s->in_done[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s->comp_done[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s->done[i], cudaEventDisableTiming) != cudaSuccess)
             st = PA_ERR_CUDA;
         else
             st = capture(s, i, workspace, ws_bytes, cap);
@@ -251,6 +260,13 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
                 return PA_ERR_BOUNDS;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // Inputs in on the copy-in stream: nothing on the device still reads this
+    // slot (its last step's output copy is done, waited above), so the copy
+    // can run while the previous step's decode does.
+    if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, s->in_stream) != cudaSuccess ||
+        cudaEventRecord(s->in_done[slot], s->in_stream) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, s->in_done[slot], 0) != cudaSuccess)
+        return PA_ERR_CUDA;
     if (ncow > 0) {
         // Copy-on-write before the step's append writes the new token.
         int32_t* dpairs = reinterpret_cast<int32_t*>(g + L.cow_pairs);
@@ -269,8 +285,16 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
             if (st != PA_OK) return st;
         }
     }
-    if (cudaGraphLaunch(s->exec[slot], cs) != cudaSuccess) return PA_ERR_CUDA;
-    if (cudaEventRecord(s->done[slot], cs) != cudaSuccess) return PA_ERR_CUDA;
+    // The append and the decode, in order on the caller's stream (so one step's
+    // copy-on-write and append follow the previous step's decode); then the
+    // output out on the copy-out stream, while the next step's decode runs.
+    if (cudaGraphLaunch(s->exec[slot], cs) != cudaSuccess ||
+        cudaEventRecord(s->comp_done[slot], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(s->out_stream, s->comp_done[slot], 0) != cudaSuccess ||
+        cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d.B * d.H * d.d * 2, cudaMemcpyDeviceToHost,
+                        s->out_stream) != cudaSuccess ||
+        cudaEventRecord(s->done[slot], s->out_stream) != cudaSuccess)
+        return PA_ERR_CUDA;
     s->pending[slot] = true;
     ++s->submitted;
     if (slot_out) *slot_out = slot;
