@@ -233,6 +233,17 @@ def setup_workload(args):
     from paged_kv_cache_103_gb300 import binding
 
     w = WORKLOADS[args.workload](args.batch)
+    if "trace" not in w.extra:
+        # Room for the e2e leg's two loops of e2e_extra appended tokens per
+        # sequence: extra blocks at the back of the free list, so the batch's
+        # own blocks (and the timed decode over them) are as the workload has
+        # them.  (The prefix-cached trace keeps its pool: its size is part of
+        # that workload.)
+        grow = w.B * (int(math.ceil((2 * args.e2e_extra + 1) / w.block_size)) + 1)
+        w.free_order = np.concatenate([np.asarray(w.free_order, dtype=np.int32),
+                                       np.arange(w.num_blocks, w.num_blocks + grow,
+                                                 dtype=np.int32)])
+        w.num_blocks += grow
     fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
     host = wl_mod().qkv(w, with_cache=not fp8)
     if fp8:
@@ -815,6 +826,17 @@ def run_multi_query(args):
     flops = 4.0 * pf["H"] * pf["d"] * keys
     tflops = flops / (t_pf * 1e-3) / 1e12
     peak_t, peak_kind = load_tensor_peak()
+    # the ceiling of the mma.sync m16n8k16 path itself (bf16), same process
+    sink = torch.empty(binding.pa_decode_grid_size() * 4 * 256, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.pa_measure_mma_ceiling(True, 1024, sink)
+    torch.cuda.synchronize()
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record()
+    mma_flops = sum(binding.pa_measure_mma_ceiling(True, 1024, sink) for _ in range(5))
+    m1.record()
+    torch.cuda.synchronize()
+    mma_ceiling = mma_flops / (m0.elapsed_time(m1) * 1e-3) / 1e12
     # speculative verification
     w = wl_mod().qwen_longtail(16)
     lens = (np.asarray(w.context_lens, np.int64) + 6).tolist()
@@ -860,14 +882,20 @@ def run_multi_query(args):
                      "peak_source": "%s bf16_tflops (cuBLAS burst)" % peak_kind,
                      "flops_per_launch": flops,
                      "note": "mma.sync m16n8k16 path; bf16 PV carries a residual operand "
-                             "(1.5x the MMAs of the plain count)"},
+                             "(1.5x the MMAs of the plain count)",
+                     "mma_sync_ceiling": {
+                         "value": round(mma_ceiling, 1), "unit": "TFLOP/s",
+                         "how": "pa_measure_mma_ceiling: 2 CTAs x 8 warps per SM, 8 independent "
+                                "bf16 m16n8k16 MMAs per round from registers, CUDA events over 5 "
+                                "launches",
+                         "mma_work_frac": round(1.5 * tflops / mma_ceiling, 4)}},
         "e2e": None,
         "speculative_verification": {
             "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t_sv * 1e3, 2),
             "pct_of_hbm_peak": round(100 * gbs / peak_h, 1), "tokens": 6 * w.B,
             "config": "qwen long-tail batch, 128 sequences x 6 query tokens, 28 / 4 heads, "
                       "block 16, L2 flushed between launches"},
-        "gpu_launches": 2 * (reps + 3),
+        "gpu_launches": 2 * (reps + 3) + 8,
         "config": {"workload": "chunked prefill: 4 sequences x 2048-token chunk on 6144 cached "
                                "tokens, 32 / 8 heads of 128, bf16, block 16",
                    "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}}))

@@ -571,6 +571,19 @@ PA_API pa_status pa_check_device_errors(void* stream, uint32_t* flags);
  * path without stalling a real pipeline. */
 PA_API pa_status pa_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
+/* Measurement aid: the throughput ceiling of the legacy tensor-core path the
+ * attention kernels use (mma.sync m16n8k16, f16 or -- bf16 != 0 -- bf16
+ * operands, fp32 accumulation).  Launches two CTAs of eight warps per SM; each
+ * warp issues `iters` (1 .. 2^20) rounds of 8 independent MMAs from registers
+ * and writes one float per thread to sink (device, >= SMs x 2 x 256 floats,
+ * contents meaningless).  *flops (host) receives the launch's floating-point
+ * operations (2 per multiply-add); time the launch with events on `stream`.
+ * PA_ERR_INVALID for bad arguments or a small sink.  The paper has no
+ * counterpart; it gives the kernels' MMA-bound work a denominator measured on
+ * the same path. */
+PA_API pa_status pa_measure_mma_ceiling(int32_t bf16, int32_t iters, float* sink,
+                                        size_t sink_bytes, int64_t* flops, void* stream);
+
 /* Number of decode CTAs pa_decode launches on the current device (one per SM
  * times the resident CTAs per SM), for launch accounting; 0 on error. */
 PA_API int32_t pa_decode_grid_size(void);

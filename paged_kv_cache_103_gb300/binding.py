@@ -114,6 +114,7 @@ SIGNATURES = {
     "pa_check_device_errors": (_ST, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "pa_decode_grid_size": (_I32, []),
     "pa_selftest_wait_timeout": (_ST, [ctypes.c_uint32, _P]),
+    "pa_measure_mma_ceiling": (_ST, [_I32, _I32, _P, _SZ, ctypes.POINTER(_I64), _P]),
 }
 
 
@@ -362,6 +363,17 @@ def pa_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     pa_check_device_errors()."""
     _check(load().pa_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)),
            "pa_selftest_wait_timeout")
+
+
+def pa_measure_mma_ceiling(bf16: bool, iters: int, sink, stream=None) -> int:
+    """Launches the mma.sync throughput-ceiling kernel (see pa.h) writing into
+    the device tensor ``sink``; returns the launch's floating-point operations."""
+    flops = ctypes.c_int64(0)
+    _check(load().pa_measure_mma_ceiling(int(bool(bf16)), int(iters), sink.data_ptr(),
+                                         sink.numel() * sink.element_size(),
+                                         ctypes.byref(flops), _stream_ptr(stream)),
+           "pa_measure_mma_ceiling")
+    return int(flops.value)
 
 
 def pa_decode_grid_size() -> int:

@@ -1,6 +1,7 @@
 // Runtime pieces of the C ABI: status strings, the per-device error word that
-// kernels raise bits in (instead of trapping), SM-count caching and the decode
-// workspace initialisation.
+// kernels raise bits in (instead of trapping), SM-count caching, the decode
+// workspace initialisation, and two measurement aids (the bounded-wait self
+// test and the mma.sync throughput ceiling).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -31,6 +32,33 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, unsigned int* err) {
     const bool done = pa::mbar_wait(&bar, 0, limit_ns);
     if (!__all_sync(0xffffffffu, done) && threadIdx.x == 0)
         pa::raise_error(err, PA_DEVERR_TIMEOUT);
+}
+
+// Throughput ceiling of the mma.sync m16n8k16 path the attention kernels
+// use: every warp issues kMmaChains independent MMAs per iteration from
+// registers (no memory traffic in the loop) and writes one float at the end.
+constexpr int kMmaChains = 8;
+constexpr int kMmaWarps = 8;         // per CTA
+constexpr int kMmaCtasPerSm = 2;
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kMmaWarps * 32)
+mma_ceiling_kernel(int32_t iters, uint32_t seed, float* sink) {
+    // small finite f16 / bf16 pairs (the exponent field kept below its top)
+    uint32_t a[4] = {seed & 0x3bff3bffu, (seed * 3u) & 0x3bff3bffu, (seed * 5u) & 0x3bff3bffu,
+                     (seed * 7u) & 0x3bff3bffu};
+    const uint32_t b0 = (seed * 11u) & 0x3bff3bffu, b1 = (seed * 13u) & 0x3bff3bffu;
+    float d[kMmaChains][4];
+#pragma unroll
+    for (int j = 0; j < kMmaChains; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+    for (int32_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < kMmaChains; ++j) pa::mma_16816<kBF16>(d[j], a, b0, b1);
+    }
+    float t = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMmaChains; ++j) t += d[j][0] + d[j][1] + d[j][2] + d[j][3];
+    sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = t;
 }
 
 }  // namespace
@@ -104,6 +132,23 @@ PA_API pa_status pa_selftest_wait_timeout(uint32_t limit_us, void* stream) {
     if (!err) return PA_ERR_CUDA;
     wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
         (uint64_t)limit_us * 1000u, err);
+    return pa::cuda_status(cudaGetLastError());
+}
+
+PA_API pa_status pa_measure_mma_ceiling(int32_t bf16, int32_t iters, float* sink,
+                                        size_t sink_bytes, int64_t* flops, void* stream) {
+    if (iters <= 0 || iters > (1 << 20) || !sink || !flops) return PA_ERR_INVALID;
+    const int sms = pa::device_sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    const int grid = sms * kMmaCtasPerSm;
+    if (sink_bytes < (size_t)grid * kMmaWarps * 32 * sizeof(float)) return PA_ERR_INVALID;
+    // 2 flops per multiply-add, 16 x 8 x 16 multiply-adds per MMA
+    *flops = (int64_t)2 * 16 * 8 * 16 * kMmaChains * iters * (int64_t)grid * kMmaWarps;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (bf16)
+        mma_ceiling_kernel<true><<<grid, kMmaWarps * 32, 0, st>>>(iters, 0x9e3779b9u, sink);
+    else
+        mma_ceiling_kernel<false><<<grid, kMmaWarps * 32, 0, st>>>(iters, 0x9e3779b9u, sink);
     return pa::cuda_status(cudaGetLastError());
 }
 

@@ -162,3 +162,13 @@ def test_step_create_refuses_an_allocator_of_another_pool(lib):
         assert lib.pa_step_create(ctypes.byref(d), a._h, fake, fake, None, None, fake, fake, fake,
                                   ws, ctypes.byref(h)) == 1
         assert not h.value
+
+
+def test_mma_ceiling_argument_checks(lib):
+    """The measurement aid refuses bad arguments before touching the device."""
+    f = ctypes.c_int64(0)
+    sink = ctypes.c_void_p(1 << 20)                     # never dereferenced
+    assert lib.pa_measure_mma_ceiling(1, 0, sink, 1 << 20, ctypes.byref(f), None) == 1
+    assert lib.pa_measure_mma_ceiling(1, (1 << 20) + 1, sink, 1 << 20, ctypes.byref(f), None) == 1
+    assert lib.pa_measure_mma_ceiling(1, 16, None, 1 << 20, ctypes.byref(f), None) == 1
+    assert lib.pa_measure_mma_ceiling(1, 16, sink, 1 << 20, None, None) == 1
