@@ -829,11 +829,11 @@ def run_multi_query(args):
     # the ceiling of the mma.sync m16n8k16 path itself (bf16), same process
     sink = torch.empty(binding.pa_decode_grid_size() * 4 * 256, dtype=torch.float32, device=dev)
     for _ in range(3):
-        binding.pa_measure_mma_ceiling(True, 1024, sink)
+        binding.pa_measure_mma_ceiling(True, 4096, sink)
     torch.cuda.synchronize()
     m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     m0.record()
-    mma_flops = sum(binding.pa_measure_mma_ceiling(True, 1024, sink) for _ in range(5))
+    mma_flops = sum(binding.pa_measure_mma_ceiling(True, 4096, sink) for _ in range(5))
     m1.record()
     torch.cuda.synchronize()
     mma_ceiling = mma_flops / (m0.elapsed_time(m1) * 1e-3) / 1e12
