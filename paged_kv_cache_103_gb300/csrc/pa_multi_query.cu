@@ -412,6 +412,10 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         const int32_t warp_lim = __reduce_max_sync(0xffffffffu, max(lim[0], lim[1]));
+        // keys up to the smallest limit of the warp's valid rows are visible to all
+        // of them (rows past the tile are never read)
+        const int32_t warp_min_lim = __reduce_min_sync(
+            0xffffffffu, (int)min(valid[0] ? lim[0] : INT32_MAX, valid[1] ? lim[1] : INT32_MAX));
 
         for (int32_t c = sg.c0; c < sg.c0 + sg.len; ++c) {
             const bool ready = dead || pa::mbar_wait(&full[stage], use, kWaitLimitNs);
@@ -462,35 +466,55 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                             pa::mma_16816<kBF16>(s[2 * np + 1], qa[ks], b[2], b[3]);
                         }
                     }
-                    // causal mask, online softmax (rows qr and qr + 8 of this warp)
+                    // causal mask, online softmax (rows qr and qr + 8 of this warp);
+                    // a half every valid row sees whole needs no mask (rows past
+                    // the tile have zero q and are never stored)
                     float mx[2] = {-INFINITY, -INFINITY};
+                    if (hkey0 + 31 <= warp_min_lim) {
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
+                        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int32_t key = hkey0 + 8 * nt + qc + (e & 1);
-                            const float x = key <= lim[e >> 1] ? s[nt][e] * p.scale_log2 : -INFINITY;
-                            s[nt][e] = x;
-                            mx[e >> 1] = fmaxf(mx[e >> 1], x);
-                        }
+                            for (int e = 0; e < 4; ++e) {
+                                const float x = s[nt][e] * p.scale_log2;
+                                s[nt][e] = x;
+                                mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                            }
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int32_t key = hkey0 + 8 * nt + qc + (e & 1);
+                                const float x =
+                                    key <= lim[e >> 1] ? s[nt][e] * p.scale_log2 : -INFINITY;
+                                s[nt][e] = x;
+                                mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                            }
+                    }
                     float alpha[2], msafe[2];
+                    bool grew = false;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         float v = mx[h2];
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
                         const float m_new = fmaxf(m_run[h2], v);
+                        grew |= m_new > m_run[h2];
                         msafe[h2] = m_new == -INFINITY ? 0.f : m_new;
                         alpha[h2] = pa::fast_exp2(m_run[h2] - msafe[h2]);
                         m_run[h2] = m_new;
                         l_run[h2] *= alpha[h2];
                     }
+                    // O needs the rescale only when some row's maximum grew (a
+                    // row whose maximum stays has alpha = 1 exactly)
+                    if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
-                    for (int nt = 0; nt < D / 8; ++nt) {
-                        o[nt][0] *= alpha[0];
-                        o[nt][1] *= alpha[0];
-                        o[nt][2] *= alpha[1];
-                        o[nt][3] *= alpha[1];
+                        for (int nt = 0; nt < D / 8; ++nt) {
+                            o[nt][0] *= alpha[0];
+                            o[nt][1] *= alpha[0];
+                            o[nt][2] *= alpha[1];
+                            o[nt][3] *= alpha[1];
+                        }
                     }
                     // P as A fragments (k-step = 16 keys = n-tiles 2 ks2, 2 ks2 + 1).
                     // bf16 keeps 8 bits of P: a second, residual part (pl)
