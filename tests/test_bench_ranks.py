@@ -49,3 +49,23 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, None, None) == 3.5
     assert bench.whole_job_rate(100, 1, 2.0) == pytest.approx(50000.0)
+
+
+def test_reference_arm_under_two_ranks_prints_one_line():
+    """`bench.py --impl reference` launched as two ranks: rank 0 alone times
+    the oracle and prints the one JSON line; rank 1 exits 0 without work."""
+    import json
+    import subprocess
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3",
+           "--workload", "gqa7b_1x1024", "--ref-step-seconds", "0.2"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
+    assert out["cpu_baseline"]["kind"] == "oracle"
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
