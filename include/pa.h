@@ -556,6 +556,11 @@ PA_API pa_status pa_step_wait(pa_step* s, int32_t slot);
 /* pa_step_submit followed by pa_step_wait of its slot. */
 PA_API pa_status pa_step_run(pa_step* s, const int64_t* seq_ids, void* stream);
 
+/* Waits for every submitted step's output and for the executor's own copy
+ * streams, then frees the executor (graphs, streams, events); the staging
+ * buffers and workspace stay the caller's.  After a submit that failed with
+ * PA_ERR_CUDA, kernels it did launch on the caller's stream are the caller's
+ * to wait for (a stream synchronize) before freeing what they use. */
 PA_API void pa_step_destroy(pa_step* s);
 
 /* Synchronises `stream`, returns the current device's error word in *flags

@@ -59,6 +59,11 @@ struct pa_step {
 namespace {
 
 void release(pa_step* s) {
+    // Copies of a submit that failed half way are not marked pending: drain the
+    // copy streams too, so that nothing still reads or writes the caller's
+    // staging once this returns.
+    if (s->in_stream) cudaStreamSynchronize(s->in_stream);
+    if (s->out_stream) cudaStreamSynchronize(s->out_stream);
     for (int i = 0; i < kMaxDepth; ++i) {
         if (s->pending[i]) cudaEventSynchronize(s->done[i]);
         if (s->exec[i]) cudaGraphExecDestroy(s->exec[i]);
