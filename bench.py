@@ -611,7 +611,11 @@ def run_reference(args):
     import numpy as np
 
     w = WORKLOADS[args.workload](args.batch)
-    host = wl.qkv(w)
+    fmt = args.kv_format
+    fp8 = fmt != "native"                 # an 8-bit cache: E4M3 or INT8 codes
+    host = wl.qkv(w, with_cache=not fp8)
+    if fp8:
+        host.update(wl.fp8_cache(w) if fmt == "fp8" else wl.int8_cache(w))
     m = oracle.BlockManagerModel(w.num_blocks, w.block_size, w.free_order)
     if w.prefix_len:
         m.allocate(0, w.prefix_len)
@@ -624,37 +628,46 @@ def run_reference(args):
         for i in range(w.B):
             m.allocate(i, int(w.context_lens[i]) - 1)
     slots, _ = m.append_batch(range(w.B))
-    oracle.reshape_and_cache(host["k_new"], host["v_new"], slots, host["k_cache"],
-                             host["v_cache"])
+    if fp8:
+        getattr(oracle, "reshape_and_cache_" + fmt)(
+            host["k_new"], host["v_new"], slots, host["k_codes"].numpy(), host["v_codes"].numpy(),
+            host["k_scale"].numpy(), host["v_scale"].numpy())
+    else:
+        oracle.reshape_and_cache(host["k_new"], host["v_new"], slots, host["k_cache"],
+                                 host["v_cache"])
     tbl, lens = m.export(range(w.B))
-    threads = os.cpu_count() or 1
+    threads = 1 if fp8 else os.cpu_count() or 1   # the 8-bit oracles run on one thread
     # each step: a bounded sample of sequences, sized so that the whole run takes
     # about two minutes (and a step at most `ref_step_seconds`)
     per_step = min(args.ref_step_seconds, 120.0 / max(1, args.steps + args.warmup))
     t0 = time.perf_counter()
-    oracle_sample_run(w, host, tbl, lens, [0], 1)
+    oracle_sample_run(w, host, tbl, lens, [0], 1, fmt)
     one = max(time.perf_counter() - t0, 1e-4)   # one sequence on one thread
     k = int(max(1, min(w.B, min(threads, w.B) * per_step / one)))
     seqs = list(range(k))
     for _ in range(args.warmup):
-        oracle_sample_run(w, host, tbl, lens, seqs[:1], threads)
+        oracle_sample_run(w, host, tbl, lens, seqs[:1], threads, fmt)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_sample_run(w, host, tbl, lens, seqs, threads)
+        oracle_sample_run(w, host, tbl, lens, seqs, threads, fmt)
     dt = (time.perf_counter() - t0) / args.steps
-    value = kv_bytes(lens[:k], w.Hkv, w.d) / dt / 1e9
+    value = kv_bytes(lens[:k], w.Hkv, w.d, fp8=fp8) / dt / 1e9
     used = min(threads, k)
     sample = ("first %d of %d sequences of the batch per step (%d context tokens), all heads, "
-              "fp64 C oracle on %d threads" % (k, w.B, int(lens[:k].sum()), used))
+              "fp64 C oracle%s on %d threads" % (k, w.B, int(lens[:k].sum()),
+                                                 " over the %s cache" % fmt if fp8 else "", used))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)",
-        "config": {"workload": args.workload + "_decode_layer_step", "batch": w.B,
+        "config": {"workload": args.workload + ("_%skv" % fmt if fp8 else "") + "_decode_layer_step",
+                   "batch": w.B, "kv_format": "%s + fp32 scale per (token, KV head)"
+                   % ("e4m3" if fmt == "fp8" else "int8") if fp8 else w.dtype,
                    "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
-                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload]},
+                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
+                   "total_context_tokens": int(lens.sum())},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
