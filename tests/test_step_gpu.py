@@ -236,3 +236,92 @@ def test_two_slots_pipelined():
     assert binding.pa_check_device_errors() == 0
     assert bit_equal(kd, kc) and bit_equal(vd, vc)
     step.close()
+
+
+def test_pipelined_forks_frees_and_copy_on_write():
+    """depth 2 with the batch changing under the executor: before each submit
+    one sequence of the batch is freed (the step before, which reads it, may
+    still run) and a fork of another takes its place, so the fork's first
+    append copies its parent's partial last block.  The pool has no spare
+    blocks, so freed blocks come back as copy destinations and new blocks
+    while the previous step is in flight.  The oracle model replays the same
+    operations in order; every step's slots, tables, output and the final
+    caches are checked."""
+    B, H, Hkv, d, bs = 8, 8, 2, 128, 16
+    rng = np.random.default_rng(1)
+    lens = rng.integers(20, 120, size=B)
+    lens = np.where(lens % bs == 0, lens + 3, lens)
+    N = int(sum(math.ceil(int(n) / bs) for n in lens))
+    order = np.random.default_rng(1001).permutation(N).astype(np.int32)
+    cpp = binding.Allocator(N, bs, order)
+    model = oracle.BlockManagerModel(N, bs, order)
+    for i, n in enumerate(lens):
+        cpp.alloc(i, int(n))
+        model.allocate(i, int(n))
+    kc = wl.normal_tensor((N, bs, Hkv, d), torch.float16, 71)
+    vc = wl.normal_tensor((N, bs, Hkv, d), torch.float16, 72)
+    nan_tails(model, kc, vc)
+    kd, vd = kc.cuda(), vc.cuda()
+    steps = 12
+    max_blocks = int(math.ceil((lens.max() + steps + 1) / bs)) + 1
+    step = binding.Step(cpp, B, H, Hkv, d, max_blocks, max_blocks * bs, kd, vd, 0.1, depth=2)
+    ids = list(range(B))
+    log, inputs, cows = [], {}, []
+    replayed = [0]
+
+    def fill(k):
+        xs = tuple(wl.normal_tensor(shape, torch.float16, 900 + 3 * k + j)
+                   for j, shape in enumerate([(B, H, d), (B, Hkv, d), (B, Hkv, d)]))
+        sl = step.slot(k % 2)
+        for name, x in zip(("q", "k_new", "v_new"), xs):
+            sl[name].copy_(x)
+        inputs[k] = xs
+
+    def check(k):
+        step.wait(k % 2)
+        while True:
+            op = log[replayed[0]]
+            replayed[0] += 1
+            if op[0] == "free":
+                model.free(op[1])
+            elif op[0] == "fork":
+                model.fork(op[1], op[2])
+            else:
+                break
+        _, kk, ids_k = op
+        assert kk == k
+        q, kn, vn = inputs[k]
+        slots, pairs = model.append_batch(ids_k)
+        if pairs:
+            oracle.copy_blocks([kc], [vc], pairs)
+        oracle.reshape_and_cache(kn, vn, np.asarray(slots, np.int64), kc, vc)
+        cows.append(len(pairs))
+        tbl, lens_ = model.export(ids_k, max_blocks)
+        sl = step.slot(k % 2)
+        assert np.array_equal(sl["slot_mapping"].numpy(), np.asarray(slots, np.int64)), k
+        assert np.array_equal(sl["block_tables"].numpy(), tbl), k
+        assert np.array_equal(sl["context_lens"].numpy(), lens_), k
+        ref = oracle.decode(wl.bits(q), wl.bits(kc), wl.bits(vc), tbl, lens_, 0.1,
+                            oracle.DTYPE_F16, num_threads=THREADS)
+        assert_close(sl["out"].clone(), ref, "step %d with forks and frees" % k)
+
+    for k in range(steps):
+        if k >= 2:
+            check(k - 2)          # frees slot k % 2 for step k
+        if k >= 1:
+            j = (3 * k) % B
+            x, parent, child = ids[j], ids[(j + 1 + k % (B - 1)) % B], 100 + k
+            cpp.free(x)
+            log.append(("free", x))
+            cpp.fork(parent, child)
+            log.append(("fork", parent, child))
+            ids[j] = child
+        fill(k)
+        log.append(("step", k, list(ids)))
+        assert step.submit(ids) == k % 2
+    for k in range(steps - 2, steps):
+        check(k)
+    assert sum(cows) >= steps - 2
+    assert binding.pa_check_device_errors() == 0
+    assert bit_equal(kd, kc) and bit_equal(vd, vc)
+    step.close()
