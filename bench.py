@@ -223,6 +223,36 @@ def play_trace(alloc, tr):
             "note": "host allocator via ctypes; the cached tokens skip prefill"}
 
 
+def grow_pool_for_e2e(w, e2e_extra):
+    """Room for the e2e leg's two loops of e2e_extra appended tokens per
+    sequence: extra blocks at the back of the free list, so the batch's own
+    blocks (and the timed decode over them) are as the workload has them.
+    The prefix-cached trace keeps its pool: its size is part of that workload."""
+    import numpy as np
+
+    if "trace" in w.extra:
+        return
+    grow = w.B * (int(math.ceil((2 * e2e_extra + 1) / w.block_size)) + 1)
+    w.free_order = np.concatenate([np.asarray(w.free_order, dtype=np.int32),
+                                   np.arange(w.num_blocks, w.num_blocks + grow, dtype=np.int32)])
+    w.num_blocks += grow
+
+
+def populate(alloc, w):
+    """Every sequence's history in the allocator (all but the step's own
+    token): prefix-shared workloads fork one prompt and append each suffix."""
+    if w.prefix_len:
+        alloc.alloc(0, w.prefix_len)
+        for s in range(1, w.B):
+            alloc.fork(0, s)
+        for s in range(w.B):
+            for _ in range(int(w.context_lens[s]) - 1 - w.prefix_len):
+                alloc.append_slot(s)
+    else:
+        for i in range(w.B):
+            alloc.alloc(i, int(w.context_lens[i]) - 1)
+
+
 def setup_workload(args):
     """The named workload, its host tensors and the product allocator holding
     every sequence's history; the step's own token is appended last, so the
@@ -233,17 +263,7 @@ def setup_workload(args):
     from paged_kv_cache_103_gb300 import binding
 
     w = WORKLOADS[args.workload](args.batch)
-    if "trace" not in w.extra:
-        # Room for the e2e leg's two loops of e2e_extra appended tokens per
-        # sequence: extra blocks at the back of the free list, so the batch's
-        # own blocks (and the timed decode over them) are as the workload has
-        # them.  (The prefix-cached trace keeps its pool: its size is part of
-        # that workload.)
-        grow = w.B * (int(math.ceil((2 * args.e2e_extra + 1) / w.block_size)) + 1)
-        w.free_order = np.concatenate([np.asarray(w.free_order, dtype=np.int32),
-                                       np.arange(w.num_blocks, w.num_blocks + grow,
-                                                 dtype=np.int32)])
-        w.num_blocks += grow
+    grow_pool_for_e2e(w, args.e2e_extra)
     fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
     host = wl_mod().qkv(w, with_cache=not fp8)
     if fp8:
@@ -260,16 +280,7 @@ def setup_workload(args):
                                    / w.block_size)) + 1
         tbl, lens = alloc.export(seqs, max_blocks)
         return w, host, alloc, slots, tbl, lens, max_blocks, seqs
-    if w.prefix_len:
-        alloc.alloc(0, w.prefix_len)
-        for s in range(1, w.B):
-            alloc.fork(0, s)
-        for s in range(w.B):
-            for _ in range(int(w.context_lens[s]) - 1 - w.prefix_len):
-                alloc.append_slot(s)
-    else:
-        for i in range(w.B):
-            alloc.alloc(i, int(w.context_lens[i]) - 1)
+    populate(alloc, w)
     seqs = list(range(w.B))
     slots, pairs = alloc.append_batch(seqs)
     assert len(pairs) == 0

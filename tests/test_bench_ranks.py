@@ -69,3 +69,28 @@ def test_reference_arm_under_two_ranks_prints_one_line():
     assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
     assert out["cpu_baseline"]["kind"] == "oracle"
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
+
+
+def test_e2e_appends_fit_the_grown_pool():
+    """For every workload built on a fresh allocator, the bench's pool growth
+    leaves the batch's tables as the workload has them and holds the e2e
+    leg's two loops of appended tokens (the default 64 each)."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_103_gb300 import binding
+    extra = 64
+    for name, make in sorted(bench.WORKLOADS.items()):
+        w = make(None)
+        if "trace" in w.extra:
+            continue
+        plain = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
+        bench.populate(plain, w)
+        bench.grow_pool_for_e2e(w, extra)
+        alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
+        bench.populate(alloc, w)
+        seqs = list(range(w.B))
+        width = int(np.ceil((w.context_lens.max() + 2 * extra + 1) / w.block_size)) + 1
+        assert np.array_equal(plain.export(seqs, width)[0], alloc.export(seqs, width)[0]), name
+        for _ in range(2 * extra + 1):
+            alloc.append_batch(seqs)
