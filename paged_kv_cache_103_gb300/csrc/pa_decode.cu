@@ -700,9 +700,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                             vmul[mt][h] = sv;
                             vmax = fmaxf(vmax, sv);
                         }
-                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
-                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
-                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+                    // the warp's largest scale magnitude in one reduction: the
+                    // bit patterns of non-negative floats order like the values
+                    vmax = __uint_as_float(
+                        __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(vmax))));
                     if (vmax > 0.f) {
                         const int e = min(vexp, 141 - pa::biased_exponent(vmax));
                         if (e < vexp) {
