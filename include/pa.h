@@ -434,7 +434,8 @@ PA_API pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v
                                void* workspace, size_t ws_bytes, void* stream);
 
 /* pa_decode_fp8 over an INT8 cache (codes from pa_reshape_and_cache_int8):
- * element = code * scale, widened to f16 exactly; otherwise as pa_decode_fp8. */
+ * each element is code * scale; the int8 code is widened to f16 exactly and
+ * the scales are applied as for E4M3.  Otherwise as pa_decode_fp8. */
 PA_API pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache,
                                 const float* k_scale, const float* v_scale,
                                 const int32_t* block_tables, int32_t max_blocks,
