@@ -172,3 +172,23 @@ def test_mma_ceiling_argument_checks(lib):
     assert lib.pa_measure_mma_ceiling(1, (1 << 20) + 1, sink, 1 << 20, ctypes.byref(f), None) == 1
     assert lib.pa_measure_mma_ceiling(1, 16, None, 1 << 20, ctypes.byref(f), None) == 1
     assert lib.pa_measure_mma_ceiling(1, 16, sink, 1 << 20, None, None) == 1
+
+
+def _declared_parameter_counts():
+    """name -> number of parameters, from every PA_API declaration of pa.h."""
+    with open(os.path.join(ROOT, "include", "pa.h"), encoding="utf-8") as f:
+        text = re.sub(r"/\*.*?\*/", " ", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"PA_API\s+[^;(]*?\b(pa_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature of the binding takes as many arguments as the
+    header declares (a drift here would pass garbage through the C ABI)."""
+    counts = _declared_parameter_counts()
+    assert set(counts) == set(binding.SIGNATURES)
+    for name, (_, args) in binding.SIGNATURES.items():
+        assert len(args) == counts[name], (name, len(args), counts[name])
