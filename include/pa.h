@@ -480,8 +480,7 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * input copy runs on the executor's own copy-in stream and the output copy on
  * its copy-out stream, so a step's inputs travel while the previous step's
  * decode runs and its output travels while the next one's does.  The caller
- * owns the
- * staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
+ * owns the staging buffers: a page-locked host buffer (cudaHostAlloc, or a pinned
  * torch tensor) and a device buffer, each desc.depth slots of
  * pa_step_layout.total bytes (slot i at byte i * total), 256-byte aligned.
  * In a slot the caller writes a step's q [B][H][d] and new k / v [B][Hkv][d]
@@ -491,7 +490,8 @@ PA_API pa_status pa_decode_noalloc(const void* q, const void* k_cache, const voi
  * two slots a step can be submitted while the one before it still runs.  The
  * paper has no counterpart to the executor object; it exists so that a
  * serving loop pays one launch per step and its host bookkeeping can overlap
- * the device work.
+ * the device work.  Like the allocator it drives, an executor is not
+ * thread-safe: one host thread submits and waits at a time.
  * ---------------------------------------------------------------------- */
 typedef struct pa_step pa_step;
 
