@@ -5,11 +5,13 @@
 // 推理学会「分页注意力」", section 3.3: copy-on-write of a shared last block);
 // the device part is one host->device copy of the step's inputs and tables,
 // the append (pa_reshape_and_cache), the attention (pa_decode) and one
-// device->host copy of the output.  The device part is captured once into a CUDA graph and
-// replayed every step, so a step costs one graph launch instead of one launch
-// or copy call per operation.  With two staging slots a step can be submitted
-// while the previous one still runs, so the host bookkeeping of step n + 1
-// overlaps the device work of step n.
+// device->host copy of the output.  The two kernels are captured once per
+// staging slot into a CUDA graph and replayed every step on the caller's
+// stream; the copies run on the executor's own copy-in and copy-out streams,
+// ordered against the graph by events.  With two staging slots a step can be
+// submitted while the previous one still runs: the host bookkeeping and the
+// input copy of step n + 1 overlap the decode of step n, and the output copy
+// of step n overlaps the decode of step n + 1.
 #include <cuda_runtime.h>
 
 #include <new>
