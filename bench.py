@@ -683,6 +683,7 @@ def run_reference(args):
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "gpu_launches": 0, "roofline": None, "clocks": None,   # the oracle runs on the host
     }))
 
 
