@@ -106,3 +106,79 @@ def test_swap_blocks_flags_bad_pairs():
     binding.pa_swap_blocks([src], [dst], pairs)
     assert binding.pa_check_device_errors() & binding.DEVERR["PAIR"]
     assert torch.count_nonzero(dst).item() == dst[2].numel()      # only block 2 written
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_swap_round_trip_of_an_8bit_cache(fmt):
+    """An 8-bit cache swaps as two pool pairs moved with the same block pairs:
+    the codes [N, bs, Hkv, 128] and the scales [N, Hkv, bs].  After swap-out,
+    reuse and overwrite of the freed device blocks (NaN codes and scales) and
+    swap-in, the blocks are bit copies and the 8-bit decode is bit-identical
+    to the one before, and within tolerance of the oracle."""
+    bs, Hkv, d, H, N, HB = 16, 4, 128, 28, 700, 300
+    a = binding.Allocator(N, bs, np.random.default_rng(3).permutation(N).astype(np.int32))
+    a.set_swap_pool(HB)
+    lens = np.random.default_rng(4).integers(100, 1500, 6).astype(np.int32)
+    for i, n in enumerate(lens):
+        a.alloc(i, int(n))
+    w = wl.Workload("swap8", len(lens), H, Hkv, d, bs, "bf16", lens, N,
+                    np.arange(N, dtype=np.int32), 41)
+    c = wl.fp8_cache(w) if fmt == "fp8" else wl.int8_cache(w)
+    codes = [c["k_codes"].cuda(), c["v_codes"].cuda()]
+    scales = [c["k_scale"].cuda(), c["v_scale"].cuda()]
+    hcodes = [torch.zeros(HB, bs, Hkv, d, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    hscales = [torch.zeros(HB, Hkv, bs, dtype=torch.float32).pin_memory() for _ in range(2)]
+    B = len(lens)
+    tbl, ln = a.export(list(range(B)), 128)
+    q = wl.normal_tensor((B, H, d), torch.bfloat16, 6).cuda()
+    ws = torch.empty(binding.pa_decode_workspace_size(B, H, d), dtype=torch.uint8, device="cuda")
+    binding.pa_decode_workspace_init(ws)
+    decode8 = getattr(binding, "pa_decode_" + fmt)
+
+    def decode(tb, l):
+        out = torch.empty_like(q)
+        decode8(q, codes[0], codes[1], scales[0], scales[1], torch.from_numpy(tb).cuda(),
+                torch.from_numpy(l).cuda(), int(l.max()), 1 / math.sqrt(d), out, ws)
+        return out.cpu()
+
+    before = decode(tbl, ln)
+    out_pairs = {}
+    for s in (0, 3, 5):
+        p = a.swap_out(s)
+        out_pairs[s] = p
+        pt = _pairs(p, "device")
+        binding.pa_swap_blocks(codes, hcodes, pt)
+        binding.pa_swap_blocks(scales, hscales, pt)
+    torch.cuda.synchronize()
+    a.alloc(100, int(a.stats()["free_blocks"]) * bs)
+    tb100, _ = a.export([100], N)
+    used = torch.from_numpy(tb100[0][tb100[0] >= 0]).long().cuda()
+    for pl in codes:
+        pl[used] = 0x7F
+    for pl in scales:
+        pl[used] = float("nan")
+    a.free(100)
+    in_pairs = {}
+    for s in (5, 0, 3):
+        p = a.swap_in(s)
+        in_pairs[s] = p
+        pt = _pairs(p, "pinned")
+        binding.pa_swap_blocks(hcodes, codes, pt)
+        binding.pa_swap_blocks(hscales, scales, pt)
+    assert binding.pa_check_device_errors() == 0
+    for s in (0, 3, 5):
+        src = torch.from_numpy(out_pairs[s][:, 0]).long()
+        hosts = {h: dblk for h, dblk in in_pairs[s]}
+        new = torch.from_numpy(np.array([hosts[h] for h in out_pairs[s][:, 1]])).long().cuda()
+        for j, name in enumerate(("k", "v")):
+            assert torch.equal(codes[j][new].cpu(), c[name + "_codes"][src])
+            assert torch.equal(scales[j][new].cpu().view(torch.int32),
+                               c[name + "_scale"][src].view(torch.int32))
+    tbl2, ln2 = a.export(list(range(B)), 128)
+    after = decode(tbl2, ln2)
+    assert torch.equal(after.view(torch.int16), before.view(torch.int16))
+    ref = getattr(oracle, "decode_" + fmt)(wl.bits(q.cpu()), oracle.DTYPE_BF16,
+                                           c["k_codes"].numpy(), c["v_codes"].numpy(),
+                                           c["k_scale"].numpy(), c["v_scale"].numpy(), tbl, ln,
+                                           1 / math.sqrt(d))
+    assert_close(after, ref, "%s decode after swap-in" % fmt)
