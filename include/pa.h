@@ -303,7 +303,9 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new,
  *   s = fl32(max_i |x_i| / 127)
  *   k_cache[slot / bs][slot % bs][h][i] = clamp(rint(fl32(x_i / s)), -127, 127)
  * (nearest integer, ties to even; the byte of the two's-complement int8); an
- * all-zero row stores s = 0 and zero codes.  Same arguments and errors. */
+ * all-zero row stores s = 0 and zero codes.  INT8 has no NaN or infinity
+ * code: rows holding either are outside this contract (their codes and scale
+ * are unspecified).  Same arguments and errors. */
 PA_API pa_status pa_reshape_and_cache_int8(const void* k_new, const void* v_new,
                                            const int64_t* slot_mapping, int32_t T, void* k_cache,
                                            void* v_cache, float* k_scale, float* v_scale,
