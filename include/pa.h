@@ -284,7 +284,9 @@ PA_API pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
  *   s = fl32(max_i |x_i| / 448)
  *   k_cache[slot / bs][slot % bs][h][i] = E4M3(fl32(x_i / s))   (RNE, saturating)
  *   k_scale[slot / bs][h][slot % bs] = s
- * (IEEE fp32 divisions); an all-zero row stores s = 0 and zero codes.  The
+ * (IEEE fp32 divisions); an all-zero row stores s = 0 and zero codes.  Rows
+ * holding NaN or infinity are outside this contract (their scale is not
+ * defined by the formula above; codes and scale are unspecified).  The
  * same for V.  A negative slot is padding and is skipped; a slot >=
  * num_blocks * block_size is skipped and sets PA_DEVERR_SLOT.
  *   k_new, v_new     (device) [T][Hkv][d] fp16/bf16 (dtype), d = 128
