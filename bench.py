@@ -134,14 +134,18 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, t_pre=None):
+        """Clocks over [t_pre, t1]: the untimed pre-roll (if any) and the timed
+        region right after it, one stretch of the same load."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
-        inside = [s for t, s in self.samples if t0 <= t <= t1]
-        note = "timed region"
+        start = t0 if t_pre is None else t_pre
+        inside = [s for t, s in self.samples if start <= t <= t1]
+        timed = sum(1 for t, _ in self.samples if t0 <= t <= t1)
+        note = "timed region" if t_pre is None else "pre-roll + timed region (one stretch of load)"
         if not inside:   # region shorter than the sampling period: nearest samples
-            inside = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+            inside = [s for t, s in self.samples if start - 0.25 <= t <= t1 + 0.25]
             note = "within 250 ms of the timed region"
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -156,7 +160,8 @@ class ClockSampler:
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm), "window": note}
+                "samples": len(sm), "samples_in_timed_region": timed, "window": note,
+                "window_s": round(t1 - start, 3)}
 
 
 WORKLOADS = {
@@ -182,6 +187,42 @@ CONTEXT_MIX = {
     "multiturn_prefix": "end of 4-turn conversations: 1024-token shared system prompt, user "
                         "U[32,256] and reply U[64,512] tokens per turn, prefix-cached allocation",
 }
+
+
+def preroll_replays(stream, replay, seconds):
+    """Untimed replays for about `seconds` of GPU time, queued back to back
+    (one replay is timed first to size the count)."""
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay()
+        e1.record(stream)
+    e1.synchronize()
+    one = max(e0.elapsed_time(e1) * 1e-3, 1e-6)
+    n = max(1, int(math.ceil(seconds / one)))
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            replay()
+    return {"replays": n + 1, "seconds": round((n + 1) * one, 3), "timed": False}
+
+
+def unique_roofline(roof, alg_unique, dec_ms, peak):
+    """For workloads whose tables share blocks: `achieved` and `frac` divide
+    the unique bytes (a shared block's rows once: the most DRAM has to move),
+    the logical ones (a shared block once per sequence that reads it) move to
+    `achieved_logical` / `frac_logical`."""
+    achieved = alg_unique / (dec_ms * 1e-3) / 1e9
+    roof["achieved_logical"] = roof["achieved"]
+    roof["frac_logical"] = roof["frac"]
+    roof["logical_bytes_per_launch"] = roof["algorithmic_bytes_per_launch"]
+    roof["algorithmic_bytes_per_launch"] = int(alg_unique)
+    roof["achieved"] = round(achieved, 1)
+    roof["frac"] = round(achieved / peak, 4)
+    roof["bytes"] = ("unique: K/V of the distinct cache rows the tables reach (a shared block's "
+                     "rows once) + q + out + table entries + lengths")
+    return roof
 
 
 def wl_mod():
@@ -253,21 +294,15 @@ def populate(alloc, w):
             alloc.alloc(i, int(w.context_lens[i]) - 1)
 
 
-def setup_workload(args):
-    """The named workload, its host tensors and the product allocator holding
-    every sequence's history; the step's own token is appended last, so the
-    decode reads context_lens[i] tokens including it.  Returns the decode
-    batch's sequence ids too."""
+def build_tables(w, e2e_extra):
+    """The product allocator holding every sequence's history (all but the
+    step's own token), then the step's token appended; returns the allocator,
+    the step's slots, the exported tables and lengths, the table width and the
+    decode batch's sequence ids."""
     import numpy as np
 
     from paged_kv_cache_103_gb300 import binding
 
-    w = WORKLOADS[args.workload](args.batch)
-    grow_pool_for_e2e(w, args.e2e_extra)
-    fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
-    host = wl_mod().qkv(w, with_cache=not fp8)
-    if fp8:
-        host.update(wl_mod().fp8_cache(w) if args.kv_format == "fp8" else wl_mod().int8_cache(w))
     alloc = binding.Allocator(w.num_blocks, w.block_size, w.free_order)
     if "trace" in w.extra:
         tr = w.extra["trace"]
@@ -276,18 +311,65 @@ def setup_workload(args):
         step_tok = np.random.default_rng(w.seed).integers(0, tr["vocab"], w.B).astype(np.int32)
         slots, pairs = alloc.append_batch(seqs, tokens=step_tok)
         assert len(pairs) == 0
-        max_blocks = int(math.ceil((int(w.context_lens.max()) + 1 + 2 * args.e2e_extra)
+        max_blocks = int(math.ceil((int(w.context_lens.max()) + 1 + 2 * e2e_extra)
                                    / w.block_size)) + 1
         tbl, lens = alloc.export(seqs, max_blocks)
-        return w, host, alloc, slots, tbl, lens, max_blocks, seqs
+        return alloc, slots, tbl, lens, max_blocks, seqs
     populate(alloc, w)
     seqs = list(range(w.B))
     slots, pairs = alloc.append_batch(seqs)
     assert len(pairs) == 0
     # room for the e2e leg's two loops of e2e_extra steps
-    max_blocks = int(math.ceil((int(w.context_lens.max()) + 2 * args.e2e_extra)
+    max_blocks = int(math.ceil((int(w.context_lens.max()) + 2 * e2e_extra)
                                / w.block_size)) + 1
     tbl, lens = alloc.export(seqs, max_blocks)
+    return alloc, slots, tbl, lens, max_blocks, seqs
+
+
+def unique_kv_bytes(tbl, lens, bs, Hkv, d, e=2, fp8=False):
+    """K and V bytes of the distinct cache rows a decode reads: a physical
+    block shared by several tables counts once, with the most rows any of
+    them uses."""
+    rows = {}
+    for i, n in enumerate(lens):
+        n = int(n)
+        for j in range((n + bs - 1) // bs):
+            b = int(tbl[i, j])
+            r = min(bs, n - j * bs)
+            if rows.get(b, 0) < r:
+                rows[b] = r
+    tokens = sum(rows.values())
+    return 2 * tokens * Hkv * ((d + 4) if fp8 else d * e)
+
+
+def headline_config(args, w, lens, kvb, flush_l2):
+    """The `config` object of the JSON line; both arms print the same one."""
+    fp8 = args.kv_format != "native"
+    fmt = args.kv_format
+    l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9) if not flush_l2
+               else "L2 flushed between steps (512 MiB write + read outside the timed kernels; %.3f GB "
+                    "of KV per step)" % (kvb / 1e9))
+    return {"workload": args.workload + ("_%skv" % fmt if fp8 else "") + "_decode_layer_step",
+            "batch": w.B, "kv_format": "%s + fp32 scale per (token, KV head)"
+            % ("e4m3" if fmt == "fp8" else "int8") if fp8 else w.dtype,
+            "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
+            "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
+            "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
+            "l2": l2_note}
+
+
+def setup_workload(args):
+    """The named workload, its host tensors and the product allocator holding
+    every sequence's history; the step's own token is appended last, so the
+    decode reads context_lens[i] tokens including it.  Returns the decode
+    batch's sequence ids too."""
+    w = WORKLOADS[args.workload](args.batch)
+    grow_pool_for_e2e(w, args.e2e_extra)
+    fp8 = args.kv_format != "native"      # an 8-bit cache: E4M3 or INT8 codes
+    host = wl_mod().qkv(w, with_cache=not fp8)
+    if fp8:
+        host.update(wl_mod().fp8_cache(w) if args.kv_format == "fp8" else wl_mod().int8_cache(w))
+    alloc, slots, tbl, lens, max_blocks, seqs = build_tables(w, args.e2e_extra)
     return w, host, alloc, slots, tbl, lens, max_blocks, seqs
 
 
@@ -386,14 +468,21 @@ def run_gpu(args):
     evd = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
 
     def evict():
         flush_buf.zero_()                   # write, then read back so
         torch.count_nonzero(flush_buf)      # that no dirty lines remain
+
+    # Untimed pre-roll: step replays for at least `preroll_s` seconds right
+    # before the timed region, so that clocks and power have settled and the
+    # clock sampler has samples under this load.
+    t_pre0 = time.time()
+    preroll = preroll_replays(stream, lambda: (evict() if flush_l2 else None, g_step.replay()),
+                              args.preroll_s)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
 
     # each timed step is followed by one decode-alone replay, timed on its own
     # for the roofline; the step rate counts the step events only
@@ -417,8 +506,6 @@ def run_gpu(args):
     decode_ms = [evd[2 * k].elapsed_time(evd[2 * k + 1]) for k in range(K)]
     total_ms = sum(step_ms)              # the steps' kernels only
     total_ms = max_over_ranks(total_ms, dist, dev)
-    if sampler:
-        sampler.stop()
     flags = binding.pa_check_device_errors(stream)
     if flags:
         raise RuntimeError("device error flags 0x%x in the timed region" % flags)
@@ -434,9 +521,6 @@ def run_gpu(args):
     e2e = run_e2e(args, w, host, alloc, kc, vc, ks if fp8 else None, vs if fp8 else None,
                   stream, max_blocks, fp8, seqs)
 
-    l2_note = ("inputs larger than L2 (%.2f GB of KV per step)" % (kvb / 1e9) if not flush_l2
-               else "L2 flushed between steps (512 MiB write + read outside the timed kernels; %.3f GB "
-                    "of KV per step)" % (kvb / 1e9))
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -447,17 +531,12 @@ def run_gpu(args):
                  "context lengths, random block placement)" % ("E4M3" if fmt == "fp8" else "INT8")
                  if fp8 else
                  "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)"),
-        "config": {"workload": args.workload + ("_%skv" % fmt if fp8 else "") + "_decode_layer_step",
-                   "batch": w.B, "kv_format": "%s + fp32 scale per (token, KV head)"
-                   % ("e4m3" if fmt == "fp8" else "int8") if fp8 else w.dtype,
-                   "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
-                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
-                   "total_context_tokens": int(lens.sum()), "pool_blocks": w.num_blocks,
-                   "l2": l2_note},
+        "config": headline_config(args, w, lens, kvb, flush_l2),
         "pct_of_hbm_peak": round(100 * value / peak, 1),
         "tokens_per_s": round(w.B / (ms_per_step * 1e-3 * w.layers), 1),
         "us_per_layer_step": round(ms_per_step * 1e3, 2),
-        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+        "clocks": sampler.summary(t_wall0, t_wall1, t_pre0) if sampler else None,
+        "preroll": preroll,
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "timing": "each step (append + decode) replayed from one CUDA graph, CUDA events on the "
@@ -476,12 +555,190 @@ def run_gpu(args):
     }
     if "prefix_cache" in w.extra:
         result["prefix_cache"] = w.extra["prefix_cache"]
+    if w.prefix_len or "trace" in w.extra:
+        ukv = unique_kv_bytes(tbl, lens, w.block_size, w.Hkv, w.d, fp8=fp8)
+        unique_roofline(result["roofline"], alg - kvb + ukv, dec_avg_ms, peak)
+        result["unique_kv_gbs"] = round(ukv / (ms_per_step * 1e-3) / 1e9, 2)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, host, tbl, lens, args.cpu_seconds, fmt)
+    # free the headline's buffers before the sweep
+    del host, kc, vc, q, out, ws, kn, vn, g_step, g_decode, flush_buf
+    if fp8:
+        del ks, vs
+    torch.cuda.empty_cache()
+    if args.sweep != "none" and not fp8 and args.workload == "llama13b":
+        result["sweep"], result["launch_floor"] = run_sweep(args, dev, stream, sampler, peak,
+                                                             peak_kind, local)
+    if sampler:
+        sampler.stop()
     if rank == 0:
         print(json.dumps(result))
     if dist:
         dist.destroy_process_group()
+
+
+SWEEP = ["gqa7b_1x1024", "gqa7b_8x4096", "gqa7b_8x8192", "gqa7b_16x32768",
+         "qwen_longtail_bs8", "qwen_longtail_bs16", "qwen_longtail_bs32",
+         "prefix_share", "multiturn_prefix"]
+
+
+def launch_floor(dev, stream, reps=50, n=32):
+    """The launch-latency floor on this machine: a one-element fill kernel (it
+    stands for an empty kernel) replayed from a one-node CUDA graph between
+    two events, median of `reps`; and per launch inside a graph of `n` such
+    kernels."""
+    import torch
+
+    x = torch.zeros(1, device=dev)
+    g1, gn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        x.fill_(1.0)
+    with torch.cuda.graph(gn, stream=stream):
+        for _ in range(n):
+            x.fill_(1.0)
+    ts1, tsn = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g1.replay()
+            gn.replay()
+        for _ in range(reps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            g1.replay()
+            e[1].record(stream)
+            e[2].record(stream)
+            gn.replay()
+            e[3].record(stream)
+            e[3].synchronize()
+            ts1.append(e[0].elapsed_time(e[1]) * 1e3)
+            tsn.append(e[2].elapsed_time(e[3]) * 1e3 / n)
+    return {"single_graph_replay_us": round(statistics.median(ts1), 2),
+            "per_launch_in_graph_us": round(statistics.median(tsn), 2),
+            "kernel": "one-element fill (stands for an empty kernel)",
+            "how": "median of %d: one-node graph replay between two events; a %d-node graph "
+                   "replay / %d" % (reps, n, n)}
+
+
+def sweep_entry(name, args, dev, stream, sampler, peak, floor):
+    """One decode workload of the sweep, timed as a model runs it: one CUDA
+    graph holds one layer-step's decode per layer (at least the model's
+    layer count), each over its own layer's cache.  Caches are cycled so that
+    at least 4x L2 of other layers' KV is read between two reads of one cache
+    (the tables, lengths and q are shared by the layers, as a model's are).
+    Timed: K graph replays between events after an untimed pre-roll;
+    avg_launch_us = replay time / launches.  Context: one launch alone after
+    an L2 flush (events around a one-launch graph), and the launch floor."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_103_gb300 import binding
+
+    w = WORKLOADS[name](None)
+    alloc, _, tbl, lens, max_blocks, _ = build_tables(w, 0)
+    alloc.close()
+    B, H, Hkv, d, bs, N = w.B, w.H, w.Hkv, w.d, w.block_size, w.num_blocks
+    dt = w.torch_dtype
+    pool_bytes = 2 * N * bs * Hkv * d * 2
+    n_caches = max(1, int(math.ceil(4 * L2_BYTES / pool_bytes)))
+    n_launch = n_caches * int(math.ceil(w.layers / n_caches))
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    kc = torch.randn((n_caches, N, bs, Hkv, d), generator=gen, device=dev, dtype=dt)
+    vc = torch.randn((n_caches, N, bs, Hkv, d), generator=gen, device=dev, dtype=dt)
+    q = torch.randn((B, H, d), generator=gen, device=dev, dtype=dt)
+    out = torch.empty_like(q)
+    ws = torch.empty(binding.pa_decode_workspace_size(B, H, d), dtype=torch.uint8, device=dev)
+    tbl_d = torch.from_numpy(tbl).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        binding.pa_decode_workspace_init(ws, stream)
+    max_len = int(lens.max())
+
+    def decode(c):
+        binding.pa_decode(q, kc[c], vc[c], tbl_d, lens_d, max_len, w.scale, out, ws, stream)
+
+    g_layers, g_one = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_layers, stream=stream):
+        for layer in range(n_launch):
+            decode(layer % n_caches)
+    with torch.cuda.graph(g_one, stream=stream):
+        decode(0)
+    K = min(args.steps, 50)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_layers.replay()
+    t_pre = time.time()
+    pre = preroll_replays(stream, g_layers.replay, args.sweep_preroll_s)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            ev[2 * k].record(stream)
+            g_layers.replay()
+            ev[2 * k + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    rep_ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(K)]
+    clocks = sampler.summary(t0, t1, t_pre) if sampler else None
+    # one launch alone, L2 flushed before it (outside the events)
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.zero_()
+            torch.count_nonzero(flush)
+            ev1[2 * k].record(stream)
+            g_one.replay()
+            ev1[2 * k + 1].record(stream)
+    torch.cuda.synchronize()
+    one_ms = [ev1[2 * k].elapsed_time(ev1[2 * k + 1]) for k in range(K)]
+    flags = binding.pa_check_device_errors(stream)
+    if flags:
+        raise RuntimeError("device error flags 0x%x in sweep entry %s" % (flags, name))
+    if not torch.isfinite(out.float()).all():
+        raise RuntimeError("non-finite decode output in sweep entry %s" % name)
+    avg_ms = sum(rep_ms) / K / n_launch
+    kvb = kv_bytes(lens, Hkv, d)
+    alg = algorithmic_bytes(lens, B, H, Hkv, d, bs)
+    achieved = alg / (avg_ms * 1e-3) / 1e9
+    roof = {"kernel": "pa_decode", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": alg, "avg_launch_us": round(avg_ms * 1e3, 2),
+            "traffic": None}
+    entry = {"workload": name + "_decode_layer_step", "batch": B, "q_heads": H, "kv_heads": Hkv,
+             "head_dim": d, "block_size": bs, "dtype": w.dtype,
+             "context_lens": CONTEXT_MIX[name], "total_context_tokens": int(lens.sum()),
+             "kv_gbs": round(kvb / (avg_ms * 1e-3) / 1e9, 1),
+             "us_per_layer_step": round(avg_ms * 1e3, 2),
+             "tokens_per_s": round(B / (avg_ms * 1e-3 * w.layers), 1),
+             "roofline": roof,
+             "single_launch_us": round(statistics.median(one_ms) * 1e3, 2),
+             "launch_floor_us": floor["single_graph_replay_us"],
+             "graph": {"launches": n_launch, "distinct_layer_caches": n_caches,
+                       "model_layers": w.layers, "replays_timed": K,
+                       "l2": "%.0f MB of other layers' KV read between two reads of one cache"
+                             % ((n_caches - 1) * kvb / 1e6) if n_caches > 1 else
+                             "one cache of %.2f GB KV (> 4x L2)" % (kvb / 1e9)},
+             "preroll": pre, "clocks": clocks, "gpu_launches": K * (n_launch + 1)}
+    if w.prefix_len or "trace" in w.extra:
+        ukv = unique_kv_bytes(tbl, lens, bs, Hkv, d)
+        unique_roofline(roof, alg - kvb + ukv, avg_ms, peak)
+        entry["unique_kv_gbs"] = round(ukv / (avg_ms * 1e-3) / 1e9, 1)
+    if "prefix_cache" in w.extra:
+        entry["prefix_cache"] = w.extra["prefix_cache"]
+    del kc, vc, q, out, ws, flush, g_layers, g_one
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_sweep(args, dev, stream, sampler, peak, peak_kind, local):
+    """The other decode workloads after the headline, in the same process:
+    7B GQA at its four (batch, length) points, the Qwen long tail at block
+    size 8 / 16 / 32 and the two prefix-sharing workloads."""
+    floor = launch_floor(dev, stream)
+    names = SWEEP if args.sweep == "all" else args.sweep.split(",")
+    entries = [sweep_entry(n, args, dev, stream, sampler, peak, floor) for n in names]
+    return entries, floor
 
 
 def run_e2e(args, w, host, alloc, kc, vc, ks, vs, stream, max_blocks, fp8, seqs):
@@ -622,6 +879,7 @@ def run_reference(args):
     import numpy as np
 
     w = WORKLOADS[args.workload](args.batch)
+    grow_pool_for_e2e(w, args.e2e_extra)     # the GPU arm's pool (spare blocks at the back)
     fmt = args.kv_format
     fp8 = fmt != "native"                 # an 8-bit cache: E4M3 or INT8 codes
     host = wl.qkv(w, with_cache=not fp8)
@@ -663,6 +921,7 @@ def run_reference(args):
         oracle_sample_run(w, host, tbl, lens, seqs, threads, fmt)
     dt = (time.perf_counter() - t0) / args.steps
     value = kv_bytes(lens[:k], w.Hkv, w.d, fp8=fp8) / dt / 1e9
+    kvb_all = kv_bytes(lens, w.Hkv, w.d, fp8=fp8)
     used = min(threads, k)
     sample = ("first %d of %d sequences of the batch per step (%d context tokens), all heads, "
               "fp64 C oracle%s on %d threads" % (k, w.B, int(lens[:k].sum()),
@@ -673,12 +932,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) Q/K/V, seeded context lengths, random block placement)",
-        "config": {"workload": args.workload + ("_%skv" % fmt if fp8 else "") + "_decode_layer_step",
-                   "batch": w.B, "kv_format": "%s + fp32 scale per (token, KV head)"
-                   % ("e4m3" if fmt == "fp8" else "int8") if fp8 else w.dtype,
-                   "q_heads": w.H, "kv_heads": w.Hkv, "head_dim": w.d,
-                   "block_size": w.block_size, "context_lens": CONTEXT_MIX[args.workload],
-                   "total_context_tokens": int(lens.sum())},
+        "config": headline_config(args, w, lens, kvb_all, kvb_all < 2 * L2_BYTES),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -939,6 +1193,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default="all",
+                    help="after the llama13b headline, time these decode workloads too: 'all', "
+                         "'none' or a comma-separated list of workload names")
+    ap.add_argument("--preroll-s", type=float, default=0.3,
+                    help="seconds of untimed step replays right before the timed region")
+    ap.add_argument("--sweep-preroll-s", type=float, default=0.1,
+                    help="seconds of untimed replays before each sweep entry's timed replays")
     ap.add_argument("--kv-format", choices=["native", "fp8", "int8"], default="native",
                     help="cache in the workload's 16-bit dtype, or E4M3 / INT8 codes + fp32 scales")
     ap.add_argument("--measure", choices=["decode", "swap", "multi_query"], default="decode",

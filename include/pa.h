@@ -458,7 +458,9 @@ PA_API pa_status pa_decode_int8(const void* q, const void* k_cache, const void* 
  * until the process exits; a batch whose pa_decode_workspace_size(B, H, d)
  * exceeds it returns PA_ERR_UNSUPPORTED.  The call allocates nothing: the
  * first call on a device looks up the array's device address (so make that
- * first call before any stream capture), and every call clears the arrival
+ * first call before any stream capture); the address is kept per device and
+ * context, so the first call after a device reset (a new context) looks it
+ * up again.  Every call clears the arrival
  * counters with an async memset on `stream`.  All calls share the one array,
  * which keeps the last call's partial results: calls that overlap on the GPU
  * (different streams, or different host threads) race and must be serialised
@@ -544,7 +546,10 @@ PA_API pa_status pa_step_create(const pa_step_desc* desc, pa_allocator* alloc, v
  * launches the slot's graph; the output copy follows on the copy-out stream.
  * Work the caller later orders on `stream` runs after the step's decode but
  * not necessarily after its output copy: pa_step_wait is what guarantees the
- * output is on the host.  A sequence whose length after the append would
+ * output is on the host.  Steps may be submitted on different streams: every
+ * step's copy-on-write, append and decode wait for the previous step's decode
+ * (they share the cache and the decode workspace), so alternating streams
+ * orders the kernels as one stream would.  A sequence whose length after the append would
  * exceed max_context_len or max_blocks * block_size returns PA_ERR_BOUNDS
  * before anything changes; allocator errors are those of pa_append_batch (all
  * or nothing).  After the appends, a slot, table entry or copy pair outside

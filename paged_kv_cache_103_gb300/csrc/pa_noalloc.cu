@@ -10,7 +10,11 @@
 //
 // The array's name, used in host code, is only a host-side stand-in; its
 // device address is looked up once per device with cudaGetSymbolAddress
-// (with that device current) and cached.
+// (with that device current) and cached together with the device's current
+// context.  A device reset tears the context down and unloads the module, so
+// a call under a different context looks the address up again instead of
+// using a stale one.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,18 +28,45 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the current device's scratch array, set up on first use.
+// The driver's cuCtxGetCurrent, reached through the runtime (no link-time
+// dependence on the driver library).
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Device address of the current device's scratch array, set up on the first
+// use under each context of the device.
 pa_status scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+        // The lookup also makes the device's primary context current if no
+        // context was yet; the context is then what the cached address keys on.
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return PA_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return PA_OK;

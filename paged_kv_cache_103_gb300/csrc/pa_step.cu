@@ -270,26 +270,39 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
     // Inputs in on the copy-in stream: nothing on the device still reads this
     // slot (its last step's output copy is done, waited above), so the copy
     // can run while the previous step's decode does.
-    if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, s->in_stream) != cudaSuccess ||
-        cudaEventRecord(s->in_done[slot], s->in_stream) != cudaSuccess ||
-        cudaStreamWaitEvent(cs, s->in_done[slot], 0) != cudaSuccess)
+    if (cudaMemcpyAsync(g, h, L.in_bytes, cudaMemcpyHostToDevice, s->in_stream) != cudaSuccess)
         return PA_ERR_CUDA;
+    // From here on a failure returns with the copy queued: wait for it, so
+    // the slot's host staging is free again when the caller retries.
+    auto fail = [&](pa_status e) {
+        cudaStreamSynchronize(s->in_stream);
+        return e;
+    };
+    if (cudaEventRecord(s->in_done[slot], s->in_stream) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, s->in_done[slot], 0) != cudaSuccess)
+        return fail(PA_ERR_CUDA);
+    // Every step's kernels share the decode workspace and the cache: this
+    // step's copy-on-write, append and decode start after the previous step's
+    // decode, whichever stream that one was submitted on.
+    if (s->submitted > 0 &&
+        cudaStreamWaitEvent(cs, s->comp_done[(s->submitted - 1) % d.depth], 0) != cudaSuccess)
+        return fail(PA_ERR_CUDA);
     if (ncow > 0) {
         // Copy-on-write before the step's append writes the new token.
         int32_t* dpairs = reinterpret_cast<int32_t*>(g + L.cow_pairs);
         if (cudaMemcpyAsync(dpairs, pairs, (size_t)ncow * 2 * sizeof(int32_t),
                             cudaMemcpyHostToDevice, cs) != cudaSuccess)
-            return PA_ERR_CUDA;
+            return fail(PA_ERR_CUDA);
         void* kc = s->k_cache;
         void* vc = s->v_cache;
         st = pa_copy_blocks(&kc, &vc, 1, dpairs, ncow, s->block_bytes, d.num_blocks, cs);
-        if (st != PA_OK) return st;
+        if (st != PA_OK) return fail(st);
         if (d.q8) {   // and the blocks' scales, [num_blocks][Hkv][block_size] fp32
             void* ks = s->k_scale;
             void* vs = s->v_scale;
             st = pa_copy_blocks(&ks, &vs, 1, dpairs, ncow, (int64_t)d.Hkv * d.block_size * 4,
                                 d.num_blocks, cs);
-            if (st != PA_OK) return st;
+            if (st != PA_OK) return fail(st);
         }
     }
     // The append and the decode, in order on the caller's stream (so one step's
@@ -301,7 +314,7 @@ PA_API pa_status pa_step_submit(pa_step* s, const int64_t* seq_ids, void* stream
         cudaMemcpyAsync(h + L.out, g + L.out, (size_t)d.B * d.H * d.d * 2, cudaMemcpyDeviceToHost,
                         s->out_stream) != cudaSuccess ||
         cudaEventRecord(s->done[slot], s->out_stream) != cudaSuccess)
-        return PA_ERR_CUDA;
+        return fail(PA_ERR_CUDA);
     s->pending[slot] = true;
     ++s->submitted;
     if (slot_out) *slot_out = slot;

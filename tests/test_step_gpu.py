@@ -238,7 +238,8 @@ def test_two_slots_pipelined():
     step.close()
 
 
-def test_pipelined_forks_frees_and_copy_on_write():
+@pytest.mark.parametrize("streams", [1, 2])
+def test_pipelined_forks_frees_and_copy_on_write(streams):
     """depth 2 with the batch changing under the executor: before each submit
     one sequence of the batch is freed (the step before, which reads it, may
     still run) and a fork of another takes its place, so the fork's first
@@ -246,7 +247,9 @@ def test_pipelined_forks_frees_and_copy_on_write():
     blocks, so freed blocks come back as copy destinations and new blocks
     while the previous step is in flight.  The oracle model replays the same
     operations in order; every step's slots, tables, output and the final
-    caches are checked."""
+    caches are checked.  With two streams consecutive steps are submitted on
+    different streams (double-buffering by stream): the executor must still
+    run each step's kernels after the previous step's decode."""
     B, H, Hkv, d, bs = 8, 8, 2, 128, 16
     rng = np.random.default_rng(1)
     lens = rng.integers(20, 120, size=B)
@@ -268,6 +271,7 @@ def test_pipelined_forks_frees_and_copy_on_write():
     ids = list(range(B))
     log, inputs, cows = [], {}, []
     replayed = [0]
+    subs = [torch.cuda.Stream() for _ in range(streams)]
 
     def fill(k):
         xs = tuple(wl.normal_tensor(shape, torch.float16, 900 + 3 * k + j)
@@ -318,9 +322,10 @@ def test_pipelined_forks_frees_and_copy_on_write():
             ids[j] = child
         fill(k)
         log.append(("step", k, list(ids)))
-        assert step.submit(ids) == k % 2
+        assert step.submit(ids, subs[k % streams]) == k % 2
     for k in range(steps - 2, steps):
         check(k)
+    torch.cuda.synchronize()
     assert sum(cows) >= steps - 2
     assert binding.pa_check_device_errors() == 0
     assert bit_equal(kd, kc) and bit_equal(vd, vc)

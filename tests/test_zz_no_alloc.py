@@ -74,3 +74,27 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
                                q.data_ptr(), 16, big_B, 4096, 256, 128, 16, 1, 0.1, 1,
                                q.data_ptr(), None)
     assert st == 6
+
+
+def test_noalloc_on_a_side_stream_matches_workspace_entry_point():
+    """The entry point on a non-default stream, twice in a row: its counter
+    clear and its decode are both ordered on that stream."""
+    w = wl.gqa7b(8, 4096)
+    t, tbl, lens = _case(w)
+    max_len = int(w.context_lens.max())
+    ref = torch.empty_like(t["q"])
+    ws = torch.empty(binding.pa_decode_workspace_size(w.B, w.H, w.d), dtype=torch.uint8,
+                     device="cuda")
+    binding.pa_decode_workspace_init(ws)
+    binding.pa_decode(t["q"], t["k_cache"], t["v_cache"], tbl, lens, max_len, w.scale, ref, ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    for _ in range(2):
+        out = torch.full_like(t["q"], float("nan"))
+        side.wait_stream(torch.cuda.current_stream())
+        binding.pa_decode_noalloc(t["q"], t["k_cache"], t["v_cache"], tbl, lens, max_len,
+                                  w.scale, out, stream=side)
+        assert binding.pa_check_device_errors(side) == 0
+        a, b = out.double().cpu(), ref.double().cpu()
+        assert torch.isfinite(a).all()
+        assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
