@@ -1075,10 +1075,14 @@ def run_multi_query(args):
                     lens=np.asarray(lens), qlens=np.asarray(qlens), H=H, Hkv=Hkv, d=d,
                     maxq=int(max(qlens)))
 
-    def time_it(c, reps, flush=None):
+    def time_it(c, reps, flush=None, tc=False):
         def run():
-            binding.pa_multi_query(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"], c["maxq"],
-                                   1 / math.sqrt(c["d"]), c["out"], c["ws"])
+            if tc:
+                binding.pa_multi_query_tc(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"],
+                                          1 / math.sqrt(c["d"]), c["out"])
+            else:
+                binding.pa_multi_query(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"],
+                                       c["maxq"], 1 / math.sqrt(c["d"]), c["out"], c["ws"])
         for _ in range(3):
             run()
         torch.cuda.synchronize()
@@ -1100,10 +1104,14 @@ def run_multi_query(args):
     reps = max(5, min(args.steps, 50))
     # chunked prefill
     pf = make([8192] * 4, [2048] * 4, 32, 8, 128, 16, 31)
-    t_pf = time_it(pf, reps)
+    t_pf_legacy = time_it(pf, reps)
+    out_legacy = pf["out"].clone()
+    t_pf = time_it(pf, reps, tc=True)
+    agree = float((pf["out"].float() - out_legacy.float()).abs().max())
     keys = sum(sum(n - ql + r + 1 for r in range(ql)) for n, ql in zip(pf["lens"], pf["qlens"]))
     flops = 4.0 * pf["H"] * pf["d"] * keys
     tflops = flops / (t_pf * 1e-3) / 1e12
+    tflops_legacy = flops / (t_pf_legacy * 1e-3) / 1e12
     peak_t, peak_kind = load_tensor_peak()
     # the ceiling of the mma.sync m16n8k16 path itself (bf16), same process
     sink = torch.empty(binding.pa_decode_grid_size() * 4 * 256, dtype=torch.float32, device=dev)
@@ -1156,25 +1164,31 @@ def run_multi_query(args):
         "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": reps, "warmup": 3,
         "ms_per_step": round(t_pf, 4), "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic (N(0,1) Q/K/V, random block placement)",
-        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_t,
+        "roofline": {"kernel": "pa_multi_query_tc", "bound": "tensor",
+                     "achieved": round(tflops, 1), "peak": peak_t,
                      "unit": "TFLOP/s", "frac": round(tflops / peak_t, 4),
                      "peak_source": "%s bf16_tflops (cuBLAS burst)" % peak_kind,
-                     "flops_per_launch": flops,
-                     "note": "mma.sync m16n8k16 path; bf16 PV carries a residual operand "
-                             "(1.5x the MMAs of the plain count)",
+                     "flops_per_launch": flops, "avg_launch_us": round(t_pf * 1e3, 2),
+                     "note": "tcgen05.mma (M = N = 128, accumulators in TMEM), useful flops only",
+                     "mma_sync_kernel": {
+                         "kernel": "pa_multi_query", "value": round(tflops_legacy, 1),
+                         "unit": "TFLOP/s", "us_per_launch": round(t_pf_legacy * 1e3, 2),
+                         "max_abs_diff_vs_tc": agree,
+                         "note": "mma.sync m16n8k16 path; bf16 PV carries a residual operand "
+                                 "(1.5x the MMAs of the plain count)"},
                      "mma_sync_ceiling": {
                          "value": round(mma_ceiling, 1), "unit": "TFLOP/s",
                          "how": "pa_measure_mma_ceiling: 2 CTAs x 8 warps per SM, 8 independent "
                                 "bf16 m16n8k16 MMAs per round from registers, CUDA events over 5 "
                                 "launches",
-                         "mma_work_frac": round(1.5 * tflops / mma_ceiling, 4)}},
+                         "mma_sync_work_frac": round(1.5 * tflops_legacy / mma_ceiling, 4)}},
         "e2e": None,
         "speculative_verification": {
             "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t_sv * 1e3, 2),
             "pct_of_hbm_peak": round(100 * gbs / peak_h, 1), "tokens": 6 * w.B,
             "config": "qwen long-tail batch, 128 sequences x 6 query tokens, 28 / 4 heads, "
                       "block 16, L2 flushed between launches"},
-        "gpu_launches": 2 * (reps + 3) + 8,
+        "gpu_launches": 3 * (reps + 3) + 8,
         "config": {"workload": "chunked prefill: 4 sequences x 2048-token chunk on 6144 cached "
                                "tokens, 32 / 8 heads of 128, bf16, block 16",
                    "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}}))

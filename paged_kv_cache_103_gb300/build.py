@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpa.so")
 
 CUDA_SOURCES = ["pa_decode.cu", "pa_cache.cu", "pa_runtime.cu", "pa_noalloc.cu", "pa_multi_query.cu",
-                "pa_step.cu"]
+                "pa_multi_query_tc.cu", "pa_step.cu"]
 CXX_SOURCES = ["pa_allocator.cpp"]
 HEADERS = ["pa_common.cuh"]
 
