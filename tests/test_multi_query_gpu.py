@@ -101,19 +101,21 @@ def test_chunked_prefill_chunk_of_512():
     assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128)), "chunk 512")
 
 
-def test_chunked_prefill_chunk_of_2048_sampled_rows():
-    """A 2048-token chunk on top of 6144 cached tokens, checked on sampled
-    rows: row r equals the oracle's single-query attention over its own
-    causal prefix (n - qlen + r + 1 tokens)."""
+def test_chunked_prefill_chunk_of_2048_whole_tiles():
+    """A 2048-token chunk on top of 6144 cached tokens (GQA 32 / 8, bf16).  A
+    64-row tile is 16 tokens x the 4 heads of a KV head; whole tiles (every
+    head of 16 consecutive tokens) are checked every 64 tokens across the
+    chunk, including its first and last tiles: token t attends to 6144 + t + 1
+    keys."""
     n, qlen, H, Hkv, d = 8192, 2048, 32, 8, 128
     kc, vc, tbl, ln, qs, q = _setup([n], [qlen], H, Hkv, d, 16, torch.bfloat16, 23)
     out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(d)).cpu()
     assert binding.pa_check_device_errors() == 0
-    for r in [0, 1, 63, 64, 777, 1500, 2046, 2047]:
-        ref = oracle.multi_query(wl.bits(q[r:r + 1]), [0, 1], wl.bits(kc), wl.bits(vc), tbl,
-                                 [n - qlen + r + 1], 1 / math.sqrt(d), oracle.DTYPE_BF16,
+    for t0 in list(range(0, qlen, 64)) + [qlen - 16]:
+        ref = oracle.multi_query(wl.bits(q[t0:t0 + 16]), [0, 16], wl.bits(kc), wl.bits(vc), tbl,
+                                 [n - qlen + t0 + 16], 1 / math.sqrt(d), oracle.DTYPE_BF16,
                                  num_threads=THREADS)
-        assert_close(out[r:r + 1], ref, "chunk 2048 row %d" % r)
+        assert_close(out[t0:t0 + 16], ref, "chunk 2048 tokens %d.." % t0)
 
 
 def test_single_query_matches_decode_reference():
