@@ -63,9 +63,22 @@ namespace {
 constexpr int kChunk = 32;           // tokens per pipeline stage (16 or 32)
 constexpr int kKeyTiles = kChunk / 16;  // 16-key MMA tiles per chunk
 constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarps = 2;
-constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
+// Producer warps: two for a 16-bit cache (even and odd chunks); one per
+// consumer warp for an 8-bit cache, each refilling only that consumer's
+// stages, with the registers rebalanced between the two warpgroups.
+__host__ __device__ constexpr int producer_warps(bool fp8) { return fp8 ? 4 : 2; }
+__host__ __device__ constexpr int cta_threads(bool fp8) {
+    return (kConsumerWarps + producer_warps(fp8)) * 32;
+}
+// 8-bit register split: launched at 128 registers a thread (256 threads, two
+// CTAs per SM); the producer warpgroup gives back down to 72 and the consumer
+// warpgroup takes 184: 128 x 72 + 128 x 184 = 256 x 128.
+constexpr int kQ8LaunchRegs = 128;
+constexpr int kQ8ProducerRegs = 72;
+constexpr int kQ8ConsumerRegs = 184;
+static_assert(128 * kQ8ProducerRegs + 128 * kQ8ConsumerRegs == 256 * kQ8LaunchRegs,
+              "8-bit register split");
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 16;
 constexpr int kMaxG = 16;            // query heads per KV head (two 8-wide MMA tiles)
@@ -205,12 +218,14 @@ __device__ __forceinline__ void q8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& 
 }
 
 template <int D, bool kBF16, int NT, bool kAsync, bool kFp8, bool kInt8>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(cta_threads(kFp8), kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap ksmap,
                     const __grid_constant__ CUtensorMap vsmap, const DecodeParams p) {
     static_assert(!kFp8 || D == 128, "FP8 rows are one 128-byte swizzle row");
+    constexpr int kProducerWarps = producer_warps(kFp8);
+    constexpr int kThreads = cta_threads(kFp8);
     constexpr uint32_t kHalves = kFp8 ? 1 : D / 64;  // 128-byte pieces of a token row
     const int32_t B = p.B, Hkv = p.Hkv, G = p.G, bs = p.bs, S = p.stages;
     const Layout L = make_layout(D, G, B, S, kAsync ? 2 : 1, kFp8, bs);
@@ -300,7 +315,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (warp >= kConsumerWarps) {
         // =========================== producer warps ===========================
-        const int prod = warp - kConsumerWarps;  // issues the chunks k with k % 2 == prod
+        // 8-bit caches: the producer warpgroup gives registers back before
+        // anything else (the consumers' increase waits for them).
+        if constexpr (kFp8) pa::setmaxnreg_dec<kQ8ProducerRegs>();
+        const int prod = warp - kConsumerWarps;  // issues the chunks k with k % kProducerWarps == prod
         if (lane == 0 && prod == 0) {
             pa::prefetch_tensormap(&kmap);
             pa::prefetch_tensormap(&vmap);
@@ -418,6 +436,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 
     // ============================= consumer warps =============================
+    if constexpr (kFp8) pa::setmaxnreg_inc<kQ8ConsumerRegs>();
     const int cr = lane >> 2;        // fragment row inside an 8-row group
     const int cc = 2 * (lane & 3);   // fragment column pair
     const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix / row this lane addresses
@@ -1138,12 +1157,13 @@ size_t counters_bytes(int32_t B, int32_t H) {
 bool async_merge(int G) { return G <= 2; }
 
 int choose_stages(int D, int G, int B, bool fp8, int bs) {
+    const int align = fp8 ? producer_warps(true) : 2;   // stages per producer turn
     const Layout L0 = make_layout(D, G, B, 0, async_merge(G) ? 2 : 1, fp8, bs);
     if (L0.total >= kSmemBudget) return 0;
     const uint32_t per_stage = L0.stage_bytes + L0.scale_stage;
     int s = (int)((kSmemBudget - L0.total) / per_stage);
     if (s > kMaxStages) s = kMaxStages;
-    s &= ~1;  // each producer owns every other stage
+    s -= s % align;  // each producer owns every align-th stage
     // Wider groups make the consumers the limit: give every consumer warp the
     // same number of stages.  Narrow ones are bound by bytes in flight: keep
     // the deepest ring.
@@ -1158,12 +1178,19 @@ pa_status launch(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap
     auto kern = paged_decode_kernel<D, kBF16, NT, kAsync, kFp8, kInt8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int regs = 0;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBudget);
+        cudaFuncAttributes fa{};
+        if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
+        regs = fa.numRegs;
     });
     if (attr_err != cudaSuccess) return PA_ERR_CUDA;
-    kern<<<pa_decode_grid_size(), kThreads, smem, stream>>>(km, vm, ksm, vsm, prm);
+    // The 8-bit register split adds up only against this launch allocation: a
+    // kernel built with another count would wait forever in setmaxnreg.
+    if (kFp8 && regs != kQ8LaunchRegs) return PA_ERR_UNSUPPORTED;
+    kern<<<pa_decode_grid_size(), cta_threads(kFp8), smem, stream>>>(km, vm, ksm, vsm, prm);
     return pa::cuda_status(cudaGetLastError());
 }
 

@@ -22,7 +22,8 @@
 //  * Four consumer warps own 16 rows each and run FlashAttention-style over
 //    the chunks in 32-key halves: S = Q K^T and O += P V as m16n8k16
 //    tensor-core MMAs (P stays in registers as the A operand; a bf16 P carries
-//    its rounding residual as a second operand), online softmax in base 2 with
+//    its rounding residual as a second operand in warps that hold a row of
+//    fewer than 256 keys), online softmax in base 2 with
 //    the per-row causal limit, normalisation once at the end.  V rows past the
 //    context are zeroed in shared memory before use (unwritten slots may hold
 //    NaN).
@@ -46,6 +47,10 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxCtas = 512;
 constexpr int kMinChunksPerCta = 4;
+// A bf16 P keeps 8 significant bits; warps with a row of fewer keys than this
+// add P's rounding residual as a second product (about 16 bits).  Over more
+// keys the rounding errors of P average out.
+constexpr int kResidualKeys = 256;
 
 // Launch shapes: NW consumer warps of 16 rows each plus one producer warp per
 // CTA.  Four run two CTAs per SM with 113 KB of shared memory each; three
@@ -416,6 +421,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
         // of them (rows past the tile are never read)
         const int32_t warp_min_lim = __reduce_min_sync(
             0xffffffffu, (int)min(valid[0] ? lim[0] : INT32_MAX, valid[1] ? lim[1] : INT32_MAX));
+        const bool residual = kBF16 && warp_min_lim < kResidualKeys - 1;
 
         for (int32_t c = sg.c0; c < sg.c0 + sg.len; ++c) {
             const bool ready = dead || pa::mbar_wait(&full[stage], use, kWaitLimitNs);
@@ -517,9 +523,10 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                         }
                     }
                     // P as A fragments (k-step = 16 keys = n-tiles 2 ks2, 2 ks2 + 1).
-                    // bf16 keeps 8 bits of P: a second, residual part (pl)
-                    // restores about 16, so a row of a few keys whose V terms
-                    // cancel stays within the tolerance; f16 P (11 bits) needs none.
+                    // bf16 keeps 8 bits of P: for warps with a short row a
+                    // second, residual part (pl) restores about 16, so a row of
+                    // a few keys whose V terms cancel stays within the
+                    // tolerance; f16 P (11 bits) needs none.
                     uint32_t pa_[2][4], pl[2][4];
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt) {
@@ -533,7 +540,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                         const uint32_t h23 = pa::pack2<kBF16>(e4[2], e4[3]);
                         pa_[nt >> 1][(nt & 1) * 2] = h01;
                         pa_[nt >> 1][(nt & 1) * 2 + 1] = h23;
-                        if constexpr (kBF16) {
+                        if (residual) {
                             pl[nt >> 1][(nt & 1) * 2] = pa::bf16x2_residual(h01, e4[0], e4[1]);
                             pl[nt >> 1][(nt & 1) * 2 + 1] = pa::bf16x2_residual(h23, e4[2], e4[3]);
                         }
@@ -553,7 +560,7 @@ multi_query_kernel(const __grid_constant__ CUtensorMap kmap,
                                               b[0], b[1], b[2], b[3]);
                             pa::mma_16816<kBF16>(o[2 * np2], a, b[0], b[1]);
                             pa::mma_16816<kBF16>(o[2 * np2 + 1], a, b[2], b[3]);
-                            if constexpr (kBF16) {
+                            if (residual) {
                                 pa::mma_16816<kBF16>(o[2 * np2], al, b[0], b[1]);
                                 pa::mma_16816<kBF16>(o[2 * np2 + 1], al, b[2], b[3]);
                             }
