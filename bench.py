@@ -1174,14 +1174,14 @@ def run_multi_query(args):
                          "kernel": "pa_multi_query", "value": round(tflops_legacy, 1),
                          "unit": "TFLOP/s", "us_per_launch": round(t_pf_legacy * 1e3, 2),
                          "max_abs_diff_vs_tc": agree,
-                         "note": "mma.sync m16n8k16 path; bf16 PV carries a residual operand "
-                                 "(1.5x the MMAs of the plain count)"},
+                         "note": "mma.sync m16n8k16 path (a bf16 P's residual product only "
+                                 "in warps holding a row of fewer than 256 keys: none here)"},
                      "mma_sync_ceiling": {
                          "value": round(mma_ceiling, 1), "unit": "TFLOP/s",
                          "how": "pa_measure_mma_ceiling: 2 CTAs x 8 warps per SM, 8 independent "
                                 "bf16 m16n8k16 MMAs per round from registers, CUDA events over 5 "
                                 "launches",
-                         "mma_sync_work_frac": round(1.5 * tflops_legacy / mma_ceiling, 4)}},
+                         "mma_sync_work_frac": round(tflops_legacy / mma_ceiling, 4)}},
         "e2e": None,
         "speculative_verification": {
             "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t_sv * 1e3, 2),

@@ -104,6 +104,7 @@ struct DecodeParams {
     // heads is split into `subs` pairs of kMaxG heads each, pair g reading KV
     // head g / subs (query heads g * G .. g * G + G - 1 either way).
     int32_t max_blocks, B, H, Hkv, G, bs, num_blocks, stages, subs;
+    int32_t len_hint;   // the caller's max_context_len: a guess of every context's length
     float scale_log2;
 };
 
@@ -251,6 +252,30 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // Rows of one TMA box: a whole block, or a chunk-sized slice of a larger one.
     const uint32_t rows_shift = (uint32_t)(31 - __clz(bs < kChunk ? bs : kChunk));
 
+    // ---- a producer's first table window, guessed before the lengths arrive:
+    // were every context len_hint tokens long, this CTA's share would start at
+    // chunk lo_g of sequence g_i.  The window is loaded now, in the shadow of
+    // the length scan, and used only if the scan confirms the guess (batches
+    // of equal lengths); otherwise it is read again after the scan.
+    int32_t g_i = -1, g_wbase = -1, g_went = -1, g_wnext = -1;
+    if (warp >= kConsumerWarps && p.len_hint > 0) {
+        const int32_t nc = (min(p.len_hint, max_len) + kChunk - 1) / kChunk;
+        const int64_t Wg = (int64_t)B * Hkv * nc;
+        int64_t Cg = Wg / kMinChunksPerCta;
+        if (Cg > (int64_t)gridDim.x) Cg = gridDim.x;
+        if (Cg < 1) Cg = 1;
+        if (nc > 0 && (int64_t)blockIdx.x < Cg) {
+            const int32_t lo_g = cta_begin(blockIdx.x, Wg, Cg);
+            g_i = lo_g / (Hkv * nc);
+            const int32_t c0 = (lo_g - g_i * Hkv * nc) % nc;
+            g_wbase = (c0 * kChunk) >> (31 - __clz(bs));
+            const int32_t* trow = p.block_tables + (int64_t)g_i * p.max_blocks;
+            const int32_t j = g_wbase + lane;
+            g_went = j < p.max_blocks ? __ldg(trow + j) : -1;
+            g_wnext = j + 32 < p.max_blocks ? __ldg(trow + j + 32) : -1;
+        }
+    }
+
     // ---- prefix of chunk counts: prefix[i] = Hkv * sum_{i' < i} ceil(n_i' / 32)
     {
         const int per = (B + kThreads - 1) / kThreads;
@@ -350,6 +375,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             w.n_raw = __ldg(p.context_lens + w.s.i);
             w.trow = p.block_tables + (int64_t)w.s.i * p.max_blocks;
             w.wbase = (w.s.c0 * kChunk) >> bs_shift;
+            if (w.s.i == g_i && w.wbase == g_wbase) {   // the window loaded at entry
+                w.went = g_went;
+                w.wnext = g_wnext;
+                g_i = -1;
+                return w;
+            }
             const int32_t j = w.wbase + lane;
             w.went = j < p.max_blocks ? __ldg(w.trow + j) : -1;
             w.wnext = j + 32 < p.max_blocks ? __ldg(w.trow + j + 32) : -1;
@@ -1242,6 +1273,7 @@ pa_status prepare(int32_t max_blocks, int32_t max_context_len, int32_t B, int32_
     prm->bs = block_size;
     prm->num_blocks = num_blocks;
     prm->stages = stages;
+    prm->len_hint = max_context_len;
     prm->scale_log2 = scale * kLog2e;
     *smem = make_layout(d, G, B, stages, async_merge(G) ? 2 : 1, fp8, block_size).total;
     return PA_OK;
