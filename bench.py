@@ -1070,7 +1070,11 @@ def run_multi_query(args):
                                                                 int(max(qlens))),
                          dtype=torch.uint8, device=dev)
         binding.pa_decode_workspace_init(ws)
-        return dict(kc=kc, vc=vc, q=q, out=out, ws=ws, tbl=torch.from_numpy(tbl).to(dev),
+        ws_tc = torch.empty(binding.pa_multi_query_tc_workspace_size(len(lens), H, Hkv, d),
+                            dtype=torch.uint8, device=dev)
+        binding.pa_decode_workspace_init(ws_tc)
+        return dict(kc=kc, vc=vc, q=q, out=out, ws=ws, ws_tc=ws_tc,
+                    tbl=torch.from_numpy(tbl).to(dev),
                     ln=torch.from_numpy(ln).to(dev), qs=torch.from_numpy(qs).to(dev),
                     lens=np.asarray(lens), qlens=np.asarray(qlens), H=H, Hkv=Hkv, d=d,
                     maxq=int(max(qlens)))
@@ -1079,7 +1083,7 @@ def run_multi_query(args):
         def run():
             if tc:
                 binding.pa_multi_query_tc(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"],
-                                          1 / math.sqrt(c["d"]), c["out"])
+                                          c["maxq"], 1 / math.sqrt(c["d"]), c["out"], c["ws_tc"])
             else:
                 binding.pa_multi_query(c["q"], c["qs"], c["kc"], c["vc"], c["tbl"], c["ln"],
                                        c["maxq"], 1 / math.sqrt(c["d"]), c["out"], c["ws"])
@@ -1129,9 +1133,13 @@ def run_multi_query(args):
     lens = (np.asarray(w.context_lens, np.int64) + 6).tolist()
     sv = make(lens, [6] * w.B, w.H, w.Hkv, w.d, 16, 32)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    t_sv = time_it(sv, reps, flush)
+    t_sv_legacy = time_it(sv, reps, flush)
+    sv_legacy = sv["out"].clone()
+    t_sv = time_it(sv, reps, flush, tc=True)
+    sv_agree = float((sv["out"].float() - sv_legacy.float()).abs().max())
     kv = kv_bytes(lens, w.Hkv, w.d)
     gbs = kv / (t_sv * 1e-3) / 1e9
+    gbs_legacy = kv / (t_sv_legacy * 1e-3) / 1e9
     peak_h, _ = load_peak()
     # the oracle on the host cores: 256 query rows of the first prefill sequence (each over its
     # full causal context), same tables and cache contents
@@ -1184,11 +1192,17 @@ def run_multi_query(args):
                          "mma_sync_work_frac": round(tflops_legacy / mma_ceiling, 4)}},
         "e2e": None,
         "speculative_verification": {
+            "kernel": "pa_multi_query_tc (one query tile per sequence and KV head, key tiles "
+                      "split evenly over the CTAs)",
             "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t_sv * 1e3, 2),
             "pct_of_hbm_peak": round(100 * gbs / peak_h, 1), "tokens": 6 * w.B,
+            "mma_sync_kernel": {"kernel": "pa_multi_query", "value": round(gbs_legacy, 1),
+                                "us_per_launch": round(t_sv_legacy * 1e3, 2),
+                                "pct_of_hbm_peak": round(100 * gbs_legacy / peak_h, 1),
+                                "max_abs_diff_vs_tc": sv_agree},
             "config": "qwen long-tail batch, 128 sequences x 6 query tokens, 28 / 4 heads, "
                       "block 16, L2 flushed between launches"},
-        "gpu_launches": 3 * (reps + 3) + 8,
+        "gpu_launches": 4 * (reps + 3) + 8,
         "config": {"workload": "chunked prefill: 4 sequences x 2048-token chunk on 6144 cached "
                                "tokens, 32 / 8 heads of 128, bf16, block 16",
                    "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}}))

@@ -418,24 +418,37 @@ PA_API pa_status pa_multi_query(const void* q, const int32_t* q_start, const voi
                                 void* stream);
 
 /* pa_multi_query on the 5th-generation tensor cores (tcgen05, accumulators in
- * tensor memory) for the chunked-prefill shape ([P3] section 5: a long
- * prompt's prefill cut into chunks that run between decode steps): the same
- * result as pa_multi_query, computed over 128-row tiles of (query token, query
- * head of a KV head's group) rows and 128-key tiles, so it pays off when
- * qlen * (H / Hkv) fills such tiles.  One CTA per SM; each tile is finished by
- * one CTA, so no workspace is needed.
+ * tensor memory): the same result as pa_multi_query ([P3] section 5: chunked
+ * prefill, speculative verification).  Rows are (query token, query head of a
+ * KV head's group) pairs, token-major, in 128-row tiles against 128-key tiles.
+ * Two modes, chosen per call:
+ *  - max_q_len * (H / Hkv) <= 128 (every sequence's rows fit one tile:
+ *    speculative verification, decode-like batches; any grouping up to 128):
+ *    the (sequence, KV head, key tile) list is split evenly over one CTA per
+ *    SM; pairs split between CTAs are merged through the workspace;
+ *  - otherwise (prefill chunks; H / Hkv a power of two): two query tiles of a
+ *    (sequence, KV head) share each key tile; no workspace is used.
  *   q_rows       rows of q and out (= q_start[B]); rows past it read as zeros
- *   d            128 only; H / Hkv a power of two up to 128
- *   q, out       16-byte aligned; other arguments as in pa_multi_query
+ *   max_q_len    (host) an upper bound of every qlen_i; a sequence above it is
+ *                skipped and sets PA_DEVERR_CONTEXT
+ *   d            128 only
+ *   q, out       16-byte aligned
+ *   workspace    (device, 256-byte aligned) >= pa_multi_query_tc_workspace_size
+ *                bytes, zeroed once (pa_decode_workspace_init); every call leaves
+ *                its tickets at zero (zero it again after a call that set
+ *                PA_DEVERR_TIMEOUT); unused (may be NULL) in the second mode
+ *   other arguments as in pa_multi_query
  * Errors as pa_multi_query; PA_ERR_UNSUPPORTED for other head dims or
  * groupings.  A bf16 P is rounded to 8 bits; tiles whose first row has fewer
  * than 256 keys add P's rounding residual as a second product. */
+PA_API size_t pa_multi_query_tc_workspace_size(int32_t B, int32_t H, int32_t Hkv, int32_t d);
 PA_API pa_status pa_multi_query_tc(const void* q, const int32_t* q_start, int32_t q_rows,
                                    const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int32_t max_blocks,
-                                   const int32_t* context_lens, int32_t B, int32_t H,
-                                   int32_t Hkv, int32_t d, int32_t block_size, int32_t num_blocks,
-                                   float scale, pa_dtype dtype, void* out, void* stream);
+                                   const int32_t* context_lens, int32_t max_q_len, int32_t B,
+                                   int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                                   int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                                   void* workspace, size_t ws_bytes, void* stream);
 
 /* pa_decode over an FP8 cache written by pa_reshape_and_cache_fp8 ([P4]
  * section 4.3).  Computes what pa_decode computes with

@@ -96,8 +96,9 @@ SIGNATURES = {
     "pa_multi_query_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pa_multi_query": (_ST, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                              _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
+    "pa_multi_query_tc_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "pa_multi_query_tc": (_ST, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
-                                _I32, ctypes.c_float, _ST, _P, _P]),
+                                _I32, _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_decode_fp8": (_ST, [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                             _I32, ctypes.c_float, _ST, _P, _P, _SZ, _P]),
     "pa_reshape_and_cache_int8": (_ST, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
@@ -310,19 +311,28 @@ def pa_multi_query(q, q_start, k_cache, v_cache, block_tables, context_lens, max
            "pa_multi_query")
 
 
-def pa_multi_query_tc(q, q_start, k_cache, v_cache, block_tables, context_lens, scale: float,
-                      out, stream=None) -> None:
+def pa_multi_query_tc_workspace_size(B: int, H: int, Hkv: int, d: int) -> int:
+    return int(load().pa_multi_query_tc_workspace_size(B, H, Hkv, d))
+
+
+def pa_multi_query_tc(q, q_start, k_cache, v_cache, block_tables, context_lens, max_q_len: int,
+                      scale: float, out, workspace=None, stream=None) -> None:
     """``pa_multi_query`` on the tcgen05 tensor cores: ``q/out [T, H, 128]``,
     ``q_start [B+1]`` int32, caches ``[N, bs, Hkv, 128]``, ``block_tables
-    [B, max_blocks]`` and ``context_lens [B]`` int32; no workspace."""
+    [B, max_blocks]`` and ``context_lens [B]`` int32; ``workspace`` a
+    zero-initialised byte tensor of ``pa_multi_query_tc_workspace_size``
+    bytes (needed when ``max_q_len * H / Hkv <= 128``)."""
     import torch
     T, H, d = q.shape
     N, bs, Hkv, _ = k_cache.shape
     B = int(context_lens.shape[0])
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (
+        _dev(workspace), workspace.numel() * workspace.element_size())
     _check(load().pa_multi_query_tc(_dev(q), _dev(q_start, torch.int32), T, _dev(k_cache),
                                     _dev(v_cache), _dev(block_tables, torch.int32),
                                     int(block_tables.shape[1]), _dev(context_lens, torch.int32),
-                                    B, H, Hkv, d, bs, N, float(scale), _dtype_code(q), _dev(out),
+                                    int(max_q_len), B, H, Hkv, d, bs, N, float(scale),
+                                    _dtype_code(q), _dev(out), ws_ptr, ws_bytes,
                                     _stream_ptr(stream)),
            "pa_multi_query_tc")
 

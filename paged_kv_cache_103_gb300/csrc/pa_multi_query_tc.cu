@@ -87,7 +87,8 @@ __host__ __device__ constexpr uint32_t smem_total(int B) {
 // mbarrier slots; the per-tile ones come in pairs (tile w at + w)
 enum : int {
     kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
-    kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18
+    kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18, kWs1 = 19,
+    kQFull1 = 20, kQEmpty1 = 21   // the split mode's second Q stage
 };
 
 struct Params {
@@ -729,6 +730,685 @@ multi_query_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 }
 
+// ---- one query tile per (sequence, KV head): the split mode -------------------------
+// Launches in which every sequence's rows fit one 128-row tile (max_q_len * G
+// <= 128: speculative verification, decode-like batches; any G up to 128)
+// split the work like the decode: the flattened list of (sequence i, KV head g,
+// 128-key tile) is cut into equal contiguous shares over the CTAs.  Inside a
+// share the two softmax warpgroups take alternate key tiles of the same query
+// tile (warpgroup w the tiles j with j % 2 == w) and warpgroup 0 merges the
+// two states from TMEM at the pair's end.  A pair split between CTAs leaves
+// its (M, L, O) rows in one of the CTA's two workspace slots; the last CTA to
+// finish the pair -- an acquire-release ticket, never a wait -- folds them.
+
+constexpr int kMinTilesPerCta = 2;
+constexpr uint32_t kSOffQ = 0;                                   // two Q stages
+constexpr uint32_t kSOffK = kSOffQ + 2 * kTileBytes;
+constexpr uint32_t kSOffV = kSOffK + kKStages * kTileBytes;
+constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // warpgroup 1's m, l [2][128]
+constexpr uint32_t kSOffBar = kSOffRow + 2 * kM * 4;
+constexpr uint32_t kSOffMisc = kSOffBar + kNumBars * 8;           // TMEM base, dead flag, last flag
+constexpr uint32_t kSOffPrefix = kSOffMisc + 16;
+constexpr size_t kSlotFloats = (size_t)kM * (kD + 2);            // O rows, then M, then L
+
+__host__ __device__ constexpr uint32_t split_smem_total(int B) {
+    return 1024 + kSOffPrefix + (uint32_t)(B + 1) * 4;
+}
+
+struct SParams {
+    const int32_t* q_start;
+    uint16_t* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* counters;   // [B * Hkv] tickets of split pairs
+    float* partials;     // [2 * gridDim.x] slots of kSlotFloats
+    unsigned int* err;
+    int32_t max_blocks, B, H, Hkv, G, tm, bs, num_blocks, max_q_len;
+    float scale_log2;
+};
+
+struct SSeg {
+    int32_t i, g, kt0, len, nkt, a;   // a: flattened index of the pair's first key tile
+    int32_t n, qlen, q0;
+};
+
+__device__ __forceinline__ int32_t s_begin(int64_t c, int64_t F, int64_t C) {
+    return (int32_t)(c * F / C);
+}
+
+__device__ __forceinline__ SSeg s_segment(const SParams& p, const int32_t* prefix, int32_t pos,
+                                          int32_t hi) {
+    int32_t lo = 0, hb = p.B;   // largest i with prefix[i] <= pos
+    while (hb - lo > 1) {
+        const int32_t mid = (lo + hb) >> 1;
+        if (prefix[mid] <= pos) lo = mid; else hb = mid;
+    }
+    SSeg s;
+    s.i = lo;
+    s.nkt = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+    const int32_t local = pos - prefix[lo];
+    s.g = local / s.nkt;
+    s.kt0 = local - s.g * s.nkt;
+    s.a = prefix[lo] + s.g * s.nkt;
+    s.len = min(hi - pos, s.nkt - s.kt0);
+    s.n = clamp_len(__ldg(p.context_lens + lo), p.max_blocks * p.bs);
+    s.q0 = __ldg(p.q_start + lo);
+    s.qlen = __ldg(p.q_start + lo + 1) - s.q0;
+    return s;
+}
+
+// A TMA producer warp's walk over its CTA's share: per segment (the Q tile
+// first when with_q), the key tiles kt0 .. kt0 + len - 1 of pair (i, g).
+__device__ __forceinline__ void s_produce(const SParams& p, const int32_t* prefix, int32_t lo,
+                                          int32_t hi, const CUtensorMap* map,
+                                          const CUtensorMap* qmap, bool with_q,
+                                          unsigned char* smem, uint32_t ring_off, uint64_t* full,
+                                          uint64_t* empty, int stages, uint64_t* bar,
+                                          volatile int* dead, int lane) {
+    const uint64_t kv_policy = pa::l2_policy_evict_first();   // streamed once
+    const uint64_t q_policy = pa::l2_policy_evict_first();
+    const int32_t oob_row = p.num_blocks * p.bs;
+    const int32_t nb_shift = 31 - __clz(p.bs);
+    const int32_t bpt = kN >> nb_shift;
+    uint32_t kt = 0;
+    int32_t r = 0, q_issued = 0;
+    for (int32_t pos = lo; pos < hi; ++r) {
+        const SSeg sg = s_segment(p, prefix, pos, hi);
+        pos += sg.len;
+        if (with_q) {
+            // Q stage r % 2: the next segment's Q travels while this one computes
+            const int qs = r & 1;
+            uint64_t* qfull = &bar[qs ? kQFull1 : kQFull];
+            if (r >= 2 && !warp_wait(&bar[qs ? kQEmpty1 : kQEmpty], (uint32_t)(((r >> 1) - 1) & 1),
+                                     dead))
+                break;
+            if (lane == 0) {
+                // two boxes of tm tokens x G heads x 128 bytes (126 rows for G = 7;
+                // the tile's last rows then keep stale values, never stored)
+                pa::mbar_arrive_expect_tx(qfull, 2u * p.tm * p.G * 128u);
+                for (int h = 0; h < 2; ++h)
+                    pa::tma_load_4d(smem + kSOffQ + qs * kTileBytes + h * kHalfBytes, qmap, qfull,
+                                    0, sg.g * p.G, sg.q0, h, q_policy);
+            }
+            q_issued = r + 1;
+        }
+        const int32_t* trow = p.block_tables + (int64_t)sg.i * p.max_blocks;
+        const int32_t nblk = (sg.n + p.bs - 1) >> nb_shift;
+        auto entry = [&](int32_t j) {
+            const int32_t jb = j * bpt + lane;
+            if (lane >= bpt || jb >= nblk) return -1;
+            const int32_t e = __ldg(trow + jb);
+            if (e < 0 || e >= p.num_blocks) {
+                pa::raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                return -1;
+            }
+            return e;
+        };
+        int32_t blk = entry(sg.kt0);
+        bool ok_all = true;
+        for (int32_t j = 0; j < sg.len; ++j) {
+            const int32_t blk_next = j + 1 < sg.len ? entry(sg.kt0 + j + 1) : -1;
+            int32_t rows[16];
+#pragma unroll
+            for (int q8 = 0; q8 < 16; ++q8) {
+                const int32_t e = __shfl_sync(0xffffffffu, blk, (q8 * 8) >> nb_shift);
+                rows[q8] = e >= 0 ? e * p.bs + ((q8 * 8) & (p.bs - 1)) : oob_row;
+            }
+            const uint32_t st = kt % stages;
+            if (kt >= (uint32_t)stages && !warp_wait(&empty[st], (kt / stages - 1) & 1, dead)) {
+                ok_all = false;
+                break;
+            }
+            if (lane == 0) {
+                pa::mbar_arrive_expect_tx(&full[st], kTileBytes);
+                unsigned char* dst = smem + ring_off + st * kTileBytes;
+#pragma unroll
+                for (int q8 = 0; q8 < 16; ++q8)
+                    pa::tma_load_3d(dst + q8 * 2048, map, &full[st], 0, rows[q8], sg.g * 2,
+                                    kv_policy);
+            }
+            ++kt;
+            __syncwarp();
+            blk = blk_next;
+        }
+        if (!ok_all) break;
+    }
+    if (*dead && lane == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+    for (int32_t u = q_issued > 2 ? q_issued - 2 : 0; u < q_issued; ++u)
+        pa::mbar_wait(&bar[(u & 1) ? kQFull1 : kQFull], (uint32_t)((u >> 1) & 1), kWaitLimitNs);
+    for (uint32_t u = kt > (uint32_t)stages ? kt - stages : 0; u < kt; ++u)
+        pa::mbar_wait(&full[u % stages], (u / stages) & 1, kWaitLimitNs);
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
+                            const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const SParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSOffMisc);
+    volatile int* dead = reinterpret_cast<volatile int*>(smem + kSOffMisc + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);
+    float* row_m1 = reinterpret_cast<float*>(smem + kSOffRow);
+    float* row_l1 = row_m1 + kM;
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSOffPrefix);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t B = p.B;
+    const int32_t max_len = p.max_blocks * p.bs;
+
+    // ---- prefix of key tiles: prefix[i] = Hkv * sum_{i' < i} ceil(n_i' / 128),
+    // by warp 0 (lane l sums a contiguous slice of the sequences, then a scan)
+    if (warp == 0) {
+        const int32_t per = (B + 31) / 32;
+        const int32_t beg = min(lane * per, B), end = min(beg + per, B);
+        auto tiles_of = [&](int32_t i, bool flag) {
+            const int32_t raw = __ldg(p.context_lens + i);
+            const int32_t n = clamp_len(raw, max_len);
+            const int32_t ql = __ldg(p.q_start + i + 1) - __ldg(p.q_start + i);
+            const bool bad = raw < 0 || ql < 0 || ql > n || ql > p.max_q_len;
+            if (flag && blockIdx.x == 0) {
+                if (raw > max_len) pa::raise_error(p.err, PA_DEVERR_TABLE_WIDTH);
+                if (bad) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
+            }
+            return (ql > 0 && !bad) ? p.Hkv * ((n + kN - 1) / kN) : 0;
+        };
+        int32_t local = 0;
+        for (int32_t i = beg; i < end; ++i) local += tiles_of(i, true);
+        int32_t x = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        int32_t run = x - local;
+        for (int32_t i = beg; i < end; ++i) {
+            prefix[i] = run;
+            run += tiles_of(i, false);
+        }
+        if (lane == 31) prefix[B] = x;
+    }
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) pa::mbar_init(&bar[b], 1);
+        pa::mbar_init(&bar[kPFull], 4);
+        pa::mbar_init(&bar[kPFull + 1], 4);
+        pa::mbar_init(&bar[kOFree], 4);
+        pa::mbar_init(&bar[kWs1], 4);
+        pa::fence_barrier_init();
+        *dead = 0;
+    }
+    __syncthreads();
+    const int64_t F = prefix[B];
+    int64_t C = F / kMinTilesPerCta;
+    if (C > (int64_t)gridDim.x) C = gridDim.x;
+    if (C < 1) C = 1;
+    if ((int64_t)blockIdx.x >= C || F == 0) return;   // no work: no TMEM taken
+    const int32_t lo = s_begin(blockIdx.x, F, C), hi = s_begin(blockIdx.x + 1, F, C);
+    if (warp == 1) {
+        pa::tmem_alloc(tmem_slot, kTmemCols);
+        pa::tmem_relinquish();
+    }
+    pa::tc_fence_before();
+    __syncthreads();
+    pa::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            pa::prefetch_tensormap(&qmap);
+            pa::prefetch_tensormap(&kmap);
+        }
+        s_produce(p, prefix, lo, hi, &kmap, &qmap, true, smem, kSOffK, &bar[kKFull],
+                  &bar[kKEmpty], kKStages, bar, dead, lane);
+    } else if (warp == 2) {
+        if (lane == 0) pa::prefetch_tensormap(&vmap);
+        s_produce(p, prefix, lo, hi, &vmap, &qmap, false, smem, kSOffV, &bar[kVFull],
+                  &bar[kVEmpty], kVStages, bar, dead, lane);
+    } else if (warp == 1) {
+        // ============================ MMA issuer ============================
+        // Per segment: S_0(0), S_1(1), then PV_w(j), S_w(j + 2) for j = 0, 1,
+        // ... (w = j % 2): S_w(j + 2) overwrites the TMEM columns of P_w(j) and
+        // is issued after PV_w(j).
+        if (lane == 0) {
+            constexpr uint32_t idS = pa::idesc_f16(kBF16, false, kM, kN);
+            constexpr uint32_t idPV = pa::idesc_f16(kBF16, true, kM, kD);
+            const uint32_t sQ = pa::smem_addr(smem + kSOffQ);
+            const uint32_t sK = pa::smem_addr(smem + kSOffK);
+            const uint32_t sV = pa::smem_addr(smem + kSOffV);
+            uint32_t kc = 0, vc = 0;
+            uint32_t pc[kTiles] = {0, 0};
+            bool alive = true;
+            auto s_mma = [&](int w, uint32_t qb) {   // S_w = Q K^T for the next K tile
+                if (!wait_bar(&bar[kKFull + kc % kKStages], (kc / kKStages) & 1, dead)) return false;
+                pa::tc_fence_after();
+                const uint32_t kb = sK + (kc % kKStages) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t a =
+                        pa::smem_desc_sw128(qb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b =
+                        pa::smem_desc_sw128(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
+                    pa::umma_f16(tmem + w * 256, a, b, idS, kk > 0 ? 1u : 0u);
+                }
+                pa::umma_commit(&bar[kSFull + w]);
+                pa::umma_commit(&bar[kKEmpty + kc % kKStages]);
+                ++kc;
+                return true;
+            };
+            auto pv_mma = [&](int w, uint32_t vb, bool accumulate) {
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint64_t b = pa::smem_desc_sw128(vb + kk * 4096, 1024, 2048);
+                    pa::umma_f16_tmem_a(tmem + w * 256 + 128, tmem + w * 256 + kk * 8, b, idPV,
+                                        (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+            int32_t r = 0;
+            for (int32_t pos = lo; pos < hi && alive; ++r) {
+                const SSeg sg = s_segment(p, prefix, pos, hi);
+                pos += sg.len;
+                const bool residual =
+                    kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);   // the first row's keys
+                const int qs = r & 1;
+                const uint32_t qb = sQ + qs * kTileBytes;
+                if (!wait_bar(&bar[qs ? kQFull1 : kQFull], (uint32_t)((r >> 1) & 1), dead)) break;
+                for (int w = 0; w < kTiles && w < sg.len; ++w)
+                    if (!s_mma(w, qb)) {
+                        alive = false;
+                        break;
+                    }
+                for (int32_t j = 0; j < sg.len && alive; ++j) {
+                    const int w = j & 1;
+                    // O tiles of the previous segment read out first
+                    if (j == 0 && r > 0 && !wait_bar(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) {
+                        alive = false;
+                        break;
+                    }
+                    if (!wait_bar(&bar[kPFull + w], pc[w] & 1, dead)) {
+                        alive = false;
+                        break;
+                    }
+                    ++pc[w];
+                    if (!wait_bar(&bar[kVFull + vc % kVStages], (vc / kVStages) & 1, dead)) {
+                        alive = false;
+                        break;
+                    }
+                    pa::tc_fence_after();
+                    const uint32_t vb = sV + (vc % kVStages) * kTileBytes;
+                    pv_mma(w, vb, j >= 2);
+                    if (residual) {
+                        pa::umma_commit(&bar[kPvDone + w]);   // P's high part read
+                        if (!wait_bar(&bar[kPFull + w], pc[w] & 1, dead)) {
+                            alive = false;
+                            break;
+                        }
+                        ++pc[w];
+                        pa::tc_fence_after();
+                        pv_mma(w, vb, true);
+                    }
+                    pa::umma_commit(&bar[kPvDone + w]);
+                    pa::umma_commit(&bar[kVEmpty + vc % kVStages]);
+                    ++vc;
+                    if (j + 2 < sg.len && !s_mma(w, qb)) {
+                        alive = false;
+                        break;
+                    }
+                }
+                if (!alive) break;
+                pa::umma_commit(&bar[qs ? kQEmpty1 : kQEmpty]);
+            }
+            pa::umma_commit(&bar[kDrain]);
+            pa::mbar_wait(&bar[kDrain], 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ============================== softmax ==============================
+        const int wt = (warp - 4) >> 2;   // the key tiles j % 2 == wt of each segment
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t sp_col = lane_base + wt * 256;
+        const uint32_t o_col = sp_col + 128;
+        const float c2 = p.scale_log2;
+        uint32_t sc = 0, pvc = 0;
+        uint32_t vbase = 0;   // key tiles of the share's earlier segments (V ring position)
+        auto wait_pv = [&]() {
+            const bool ok = warp_wait(&bar[kPvDone + wt], pvc & 1, dead);
+            ++pvc;
+            return ok;
+        };
+        int32_t r = 0;
+        for (int32_t pos = lo; pos < hi; ++r) {
+            const SSeg sg = s_segment(p, prefix, pos, hi);
+            pos += sg.len;
+            const uint32_t vb0 = vbase;
+            vbase += (uint32_t)sg.len;
+            const int32_t rows = sg.qlen * p.G;
+            const bool valid = row < rows;
+            const int32_t t_row = row / p.G;
+            const int32_t lim_min = sg.n - sg.qlen;                 // the first row's limit
+            const int32_t lim = valid ? lim_min + t_row : -1;
+            const bool residual = kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            int32_t mine = 0;   // key tiles of this warpgroup in the segment
+            for (int32_t j = wt; j < sg.len; j += 2, ++mine) {
+                if (!warp_wait(&bar[kSFull + wt], sc & 1, dead)) {
+                    ok = false;
+                    break;
+                }
+                ++sc;
+                pa::tc_fence_after();
+                const int32_t key0 = (sg.kt0 + j) * kN;
+                const bool full = key0 + kN - 1 <= lim_min;
+                float mx = -INFINITY;
+                if (full) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; c += 2) {
+                        uint32_t s0[32], s1[32];
+                        pa::tmem_ld32(sp_col + c * 32, s0);
+                        pa::tmem_ld32(sp_col + c * 32 + 32, s1);
+                        pa::tmem_ld_wait();
+                        pa::reg_fence32(s0);
+                        pa::reg_fence32(s1);
+                        float m2[2] = {mx, -INFINITY};
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            m2[0] = fmaxf(m2[0], __uint_as_float(s0[e]));
+                            m2[1] = fmaxf(m2[1], __uint_as_float(s1[e]));
+                        }
+                        mx = fmaxf(m2[0], m2[1]);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t s[32];
+                        pa::tmem_ld32(sp_col + c * 32, s);
+                        pa::tmem_ld_wait();
+                        pa::reg_fence32(s);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (key0 + c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(s[e]));
+                    }
+                }
+                mx *= c2;
+                const bool grow = mx > m_used + kRescaleLog2;
+                const float m_new = grow ? mx : m_used;
+                const float base = m_new == -INFINITY ? 0.f : m_new;
+                float lsum = 0.f;
+                uint32_t rl[64];
+                if (full && !residual) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t s0[32], s1[32];
+                        pa::tmem_ld32(sp_col + hh * 64, s0);
+                        pa::tmem_ld32(sp_col + hh * 64 + 32, s1);
+                        pa::tmem_ld_wait();
+                        pa::reg_fence32(s0);
+                        pa::reg_fence32(s1);
+                        uint32_t pk[32];
+                        float la = 0.f, lb = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
+                            const float p1 =
+                                pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
+                            const float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
+                            const float p3 =
+                                pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
+                            la += p0 + p1;
+                            lb += p2 + p3;
+                            pk[e >> 1] = pa::pack2<kBF16>(p0, p1);
+                            pk[16 + (e >> 1)] = pa::pack2<kBF16>(p2, p3);
+                        }
+                        lsum += la + lb;
+                        pa::tmem_st32(sp_col + hh * 32, pk);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t s0[32], s1[32];
+                        pa::tmem_ld32(sp_col + hh * 64, s0);
+                        pa::tmem_ld32(sp_col + hh * 64 + 32, s1);
+                        pa::tmem_ld_wait();
+                        pa::reg_fence32(s0);
+                        pa::reg_fence32(s1);
+                        uint32_t pk[32];
+                        float la = 0.f, lb = 0.f;
+                        const int32_t kl = lim - key0 - hh * 64;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
+                            float p1 = pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
+                            float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
+                            float p3 = pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
+                            p0 = e <= kl ? p0 : 0.f;
+                            p1 = e + 1 <= kl ? p1 : 0.f;
+                            p2 = e + 32 <= kl ? p2 : 0.f;
+                            p3 = e + 33 <= kl ? p3 : 0.f;
+                            la += p0 + p1;
+                            lb += p2 + p3;
+                            const uint32_t h01 = pa::pack2<kBF16>(p0, p1);
+                            const uint32_t h23 = pa::pack2<kBF16>(p2, p3);
+                            pk[e >> 1] = h01;
+                            pk[16 + (e >> 1)] = h23;
+                            rl[hh * 32 + (e >> 1)] = pa::bf16x2_residual(h01, p0, p1);
+                            rl[hh * 32 + 16 + (e >> 1)] = pa::bf16x2_residual(h23, p2, p3);
+                        }
+                        lsum += la + lb;
+                        pa::tmem_st32(sp_col + hh * 32, pk);
+                    }
+                }
+                // this warpgroup's previous tile's product done before O moves
+                if (mine >= 1) {
+                    if (!wait_pv()) {
+                        ok = false;
+                        break;
+                    }
+                    pa::tc_fence_after();
+                    if (__any_sync(0xffffffffu, grow)) {
+                        const float f = grow ? pa::fast_exp2(m_used - m_new) : 1.f;
+                        l *= f;
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[32];
+                            pa::tmem_ld32(o_col + c * 32, o);
+                            pa::tmem_ld_wait();
+                            pa::reg_fence32(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                            pa::tmem_st32(o_col + c * 32, o);
+                        }
+                    }
+                }
+                pa::tmem_st_wait();
+                m_used = m_new;
+                l += lsum;
+                if (key0 + kN > sg.n) {
+                    // rows past the context: zero them in V (both halves) once the
+                    // tile has landed; only this warpgroup reads this tile
+                    const uint32_t vt = vb0 + (uint32_t)j;
+                    const uint32_t vs = vt % kVStages;
+                    if (!warp_wait(&bar[kVFull + vs], (vt / kVStages) & 1, dead)) {
+                        ok = false;
+                        break;
+                    }
+                    if (key0 + row >= sg.n) {
+                        unsigned char* vrow = smem + kSOffV + vs * kTileBytes +
+                                              (uint32_t)(row >> 3) * 2048 + (uint32_t)(row & 7) * 128;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                            for (int c16 = 0; c16 < 8; ++c16)
+                                *reinterpret_cast<uint4*>(vrow + hf * 1024 + c16 * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                    pa::fence_proxy_async_smem();
+                }
+                pa::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) pa::mbar_arrive(&bar[kPFull + wt]);
+                if (residual) {
+                    if (!wait_pv()) {
+                        ok = false;
+                        break;
+                    }
+                    pa::tc_fence_after();
+                    uint32_t a[32], b[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        a[e] = rl[e];
+                        b[e] = rl[32 + e];
+                    }
+                    pa::tmem_st32(sp_col, a);
+                    pa::tmem_st32(sp_col + 32, b);
+                    pa::tmem_st_wait();
+                    pa::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) pa::mbar_arrive(&bar[kPFull + wt]);
+                }
+            }
+            if (!ok) break;
+            // ---- this warpgroup's last product, then the merge of the two
+            if (mine > 0) {
+                if (!wait_pv()) break;
+                pa::tc_fence_after();
+            }
+            if (wt == 1) {
+                // warpgroup 0 has read the previous segment's values
+                if (r > 0 && !warp_wait(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) break;
+                row_m1[row] = mine > 0 ? m_used : -INFINITY;
+                row_l1[row] = mine > 0 ? l : 0.f;
+                pa::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) pa::mbar_arrive(&bar[kWs1]);
+                continue;
+            }
+            if (!warp_wait(&bar[kWs1], (uint32_t)(r & 1), dead)) break;
+            pa::tc_fence_after();
+            const float m1 = row_m1[row], l1 = row_l1[row];
+            const float M = fmaxf(m_used, m1);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            const float f0 = pa::fast_exp2(m_used - Ms), f1 = pa::fast_exp2(m1 - Ms);
+            const float L = f0 * l + f1 * l1;
+            const bool two = sg.len > 1;   // warpgroup 1 had a tile
+            const bool whole = sg.kt0 == 0 && sg.len == sg.nkt;
+            const int32_t hq = sg.g * p.G + (row - t_row * p.G);
+            uint16_t* orow = p.out + ((int64_t)(sg.q0 + t_row) * p.H + hq) * kD;
+            float* ps = nullptr;
+            if (!whole) {
+                const int64_t c = blockIdx.x;
+                const int64_t slot = s_begin(c, F, C) >= sg.a ? 2 * c : 2 * c + 1;
+                ps = p.partials + slot * kSlotFloats;
+            }
+            const float inv = whole && L > 0.f ? 1.f / L : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o0[32], o1[32];
+                pa::tmem_ld32(lane_base + 128 + c * 32, o0);
+                if (two) pa::tmem_ld32(lane_base + 256 + 128 + c * 32, o1);
+                pa::tmem_ld_wait();
+                pa::reg_fence32(o0);
+                pa::reg_fence32(o1);
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    v[e] = (f0 * __uint_as_float(o0[e]) + (two ? f1 * __uint_as_float(o1[e]) : 0.f)) * inv;
+                if (!valid) continue;
+                if (whole) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 x;
+                        x.x = pa::pack2<kBF16>(v[e], v[e + 1]);
+                        x.y = pa::pack2<kBF16>(v[e + 2], v[e + 3]);
+                        x.z = pa::pack2<kBF16>(v[e + 4], v[e + 5]);
+                        x.w = pa::pack2<kBF16>(v[e + 6], v[e + 7]);
+                        reinterpret_cast<uint4*>(orow)[(c * 32 + e) >> 3] = x;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(ps + (size_t)row * kD + c * 32 + e) =
+                            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+            }
+            if (!whole && valid) {
+                ps[(size_t)kM * kD + row] = M;
+                ps[(size_t)kM * kD + kM + row] = L;
+            }
+            pa::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kOFree]);
+            if (whole) continue;
+            // Publish: the warpgroup barrier orders every thread's partial
+            // stores before thread 0's release; the ticket names the pair's last
+            // CTA and, for it, acquires every other CTA's partial.
+            pa::named_barrier_sync(1, 128);
+            const int64_t c_first = ((int64_t)(sg.a + 1) * C - 1) / F;
+            const int64_t c_last = ((int64_t)(sg.a + sg.nkt) * C - 1) / F;
+            if (row == 0) {
+                int32_t* ctr = p.counters + (int64_t)sg.i * p.Hkv + sg.g;
+                const int prev = pa::atomic_add_acq_rel_gpu(ctr, 1);
+                const int last = prev == (int)(c_last - c_first);
+                if (last) atomicExch(ctr, 0);
+                *last_flag = last;
+            }
+            pa::named_barrier_sync(1, 128);
+            if (!*last_flag || !valid) continue;
+            // The pair's last CTA: fold every covering CTA's rows.
+            const int ncov = (int)(c_last - c_first + 1);
+            const int64_t slot0 = 2 * c_first + (s_begin(c_first, F, C) == sg.a ? 0 : 1);
+            float Mx = -INFINITY;
+            for (int c = 0; c < ncov; ++c) {
+                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+                Mx = fmaxf(Mx, __ldcg(q + (size_t)kM * kD + row));
+            }
+            const float Mxs = Mx == -INFINITY ? 0.f : Mx;
+            float Ls = 0.f;
+            for (int c = 0; c < ncov; ++c) {
+                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+                Ls += pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs) *
+                      __ldcg(q + (size_t)kM * kD + kM + row);
+            }
+            const float finv = Ls > 0.f ? 1.f / Ls : 0.f;
+            for (int d8 = 0; d8 < kD; d8 += 8) {
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int c = 0; c < ncov; ++c) {
+                    const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+                    const float f = pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs);
+                    const float4 a = __ldcg(reinterpret_cast<const float4*>(q + (size_t)row * kD + d8));
+                    const float4 b =
+                        __ldcg(reinterpret_cast<const float4*>(q + (size_t)row * kD + d8 + 4));
+                    acc[0] += f * a.x;
+                    acc[1] += f * a.y;
+                    acc[2] += f * a.z;
+                    acc[3] += f * a.w;
+                    acc[4] += f * b.x;
+                    acc[5] += f * b.y;
+                    acc[6] += f * b.z;
+                    acc[7] += f * b.w;
+                }
+                uint4 x;
+                x.x = pa::pack2<kBF16>(acc[0] * finv, acc[1] * finv);
+                x.y = pa::pack2<kBF16>(acc[2] * finv, acc[3] * finv);
+                x.z = pa::pack2<kBF16>(acc[4] * finv, acc[5] * finv);
+                x.w = pa::pack2<kBF16>(acc[6] * finv, acc[7] * finv);
+                reinterpret_cast<uint4*>(orow)[d8 >> 3] = x;
+            }
+        }
+        if (*dead && row == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+    }
+    pa::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        pa::tc_fence_after();
+        pa::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // ---- host side -----------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -797,31 +1477,63 @@ pa_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap
     return pa::cuda_status(cudaGetLastError());
 }
 
+size_t split_counters_bytes(int32_t B, int32_t Hkv) {
+    return (((size_t)B * Hkv * sizeof(int32_t)) + 255) & ~size_t(255);
+}
+
+template <bool kBF16>
+pa_status launch_split(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                       const SParams& prm, size_t smem, int grid, cudaStream_t stream) {
+    auto kern = multi_query_tc_split_kernel<kBF16>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)split_smem_total(kMaxBatch));
+    });
+    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(qm, km, vm, prm);
+    return pa::cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 
 extern "C" {
 
+PA_API size_t pa_multi_query_tc_workspace_size(int32_t B, int32_t H, int32_t Hkv, int32_t d) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || d != kD) return 0;
+    const int sms = pa::device_sm_count();
+    if (sms <= 0) return 0;
+    return split_counters_bytes(B, Hkv) + 2 * (size_t)sms * kSlotFloats * sizeof(float);
+}
+
 PA_API pa_status pa_multi_query_tc(const void* q, const int32_t* q_start, int32_t q_rows,
                                    const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int32_t max_blocks,
-                                   const int32_t* context_lens, int32_t B, int32_t H,
-                                   int32_t Hkv, int32_t d, int32_t block_size, int32_t num_blocks,
-                                   float scale, pa_dtype dtype, void* out, void* stream) {
+                                   const int32_t* context_lens, int32_t max_q_len, int32_t B,
+                                   int32_t H, int32_t Hkv, int32_t d, int32_t block_size,
+                                   int32_t num_blocks, float scale, pa_dtype dtype, void* out,
+                                   void* workspace, size_t ws_bytes, void* stream) {
     if (B < 0 || H <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || q_rows < 0 ||
-        !std::isfinite(scale))
+        max_q_len < 0 || !std::isfinite(scale))
         return PA_ERR_INVALID;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (H % Hkv != 0 || d != kD) return PA_ERR_UNSUPPORTED;
     const int G = H / Hkv;
-    if (G > kM || (G & (G - 1)) != 0) return PA_ERR_UNSUPPORTED;   // G | 128
+    if (G > kM) return PA_ERR_UNSUPPORTED;
+    // Every sequence's rows in one query tile: the split mode, any grouping.
+    // Otherwise pairs of query tiles, G a power of two (128 / G tokens a tile).
+    const bool split = (int64_t)max_q_len * G <= kM;
+    if (!split && (G & (G - 1)) != 0) return PA_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
     if (B > kMaxBatch) return PA_ERR_UNSUPPORTED;
     if ((int64_t)num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
-    // item indices are int32: every sequence's 128-row tiles times Hkv
-    if ((int64_t)B * Hkv * (((int64_t)max_blocks * block_size * G + kM - 1) / kM) >=
+    // flattened indices are int32: every sequence's 128-row tiles (or 128-key
+    // tiles) times Hkv
+    if ((int64_t)B * Hkv * (((int64_t)max_blocks * block_size * (split ? 1 : G) + kM - 1) / kM) >=
         ((int64_t)1 << 30))
         return PA_ERR_UNSUPPORTED;
-    if (B == 0 || q_rows == 0) return PA_OK;
+    if (B == 0 || q_rows == 0 || max_q_len == 0) return PA_OK;
     if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return PA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
@@ -830,6 +1542,10 @@ PA_API pa_status pa_multi_query_tc(const void* q, const int32_t* q_start, int32_
     unsigned int* err = pa::device_error_word();
     const int sms = pa::device_sm_count();
     if (!err || !sms) return PA_ERR_CUDA;
+    if (split) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID;
+        if (ws_bytes < pa_multi_query_tc_workspace_size(B, H, Hkv, d)) return PA_ERR_INVALID;
+    }
 
     CUtensorMap qm, km, vm;
     const int32_t rows = num_blocks * block_size;
@@ -837,6 +1553,31 @@ PA_API pa_status pa_multi_query_tc(const void* q, const int32_t* q_start, int32_
         !encode_kv_map(&km, k_cache, rows, Hkv, dtype) ||
         !encode_kv_map(&vm, v_cache, rows, Hkv, dtype))
         return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (split) {
+        SParams sp;
+        sp.q_start = q_start;
+        sp.out = static_cast<uint16_t*>(out);
+        sp.block_tables = block_tables;
+        sp.context_lens = context_lens;
+        sp.counters = static_cast<int32_t*>(workspace);
+        sp.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                               split_counters_bytes(B, Hkv));
+        sp.err = err;
+        sp.max_blocks = max_blocks;
+        sp.B = B;
+        sp.H = H;
+        sp.Hkv = Hkv;
+        sp.G = G;
+        sp.tm = kM / G;
+        sp.bs = block_size;
+        sp.num_blocks = num_blocks;
+        sp.max_q_len = max_q_len;
+        sp.scale_log2 = scale * kLog2e;
+        const size_t smem = split_smem_total(B);
+        return dtype == PA_BF16 ? launch_split<true>(qm, km, vm, sp, smem, sms, st)
+                                : launch_split<false>(qm, km, vm, sp, smem, sms, st);
+    }
     Params prm;
     prm.q_start = q_start;
     prm.out = static_cast<uint16_t*>(out);
@@ -853,7 +1594,6 @@ PA_API pa_status pa_multi_query_tc(const void* q, const int32_t* q_start, int32_
     prm.num_blocks = num_blocks;
     prm.scale_log2 = scale * kLog2e;
     const size_t smem = smem_total(B);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dtype == PA_BF16 ? launch<true>(qm, km, vm, prm, smem, sms, st)
                             : launch<false>(qm, km, vm, prm, smem, sms, st);
 }

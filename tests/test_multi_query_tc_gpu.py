@@ -1,6 +1,9 @@
 """GPU parity of pa_multi_query_tc (several causal query tokens per sequence
-over the paged cache on the tcgen05 tensor cores: the chunked-prefill shape)
-against the fp64 oracle, |gpu - ref| <= 2e-3 + 1e-2 |ref| per element.
+over the paged cache on the tcgen05 tensor cores) against the fp64 oracle,
+|gpu - ref| <= 2e-3 + 1e-2 |ref| per element, in both of its modes: pairs of
+128-row query tiles sharing each key tile (prefill chunks) and one query tile
+per (sequence, KV head) with the key tiles split evenly over the CTAs
+(max_q_len * G <= 128: speculative verification, decode-like batches).
 Unused slots of every last block hold NaN, so keys past a context must
 contribute nothing.  The first case is the smallest one the kernel runs: one
 128-row tile over one key tile."""
@@ -42,11 +45,21 @@ def _setup(lens, qlens, H, Hkv, d, bs, dtype, seed):
     return kc, vc, tbl, ln, q_start, q
 
 
-def _gpu(kc, vc, tbl, ln, q_start, q, scale):
+def _workspace(B, H, Hkv):
+    ws = torch.empty(binding.pa_multi_query_tc_workspace_size(B, H, Hkv, 128), dtype=torch.uint8,
+                     device="cuda")
+    binding.pa_decode_workspace_init(ws)
+    return ws
+
+
+def _gpu(kc, vc, tbl, ln, q_start, q, scale, ws=None, max_q_len=None):
     out = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    mq = int(max_q_len if max_q_len is not None else np.diff(q_start).max(initial=0))
+    if ws is None:
+        ws = _workspace(len(ln), q.shape[1], kc.shape[2])
     binding.pa_multi_query_tc(q.cuda(), torch.from_numpy(q_start).cuda(), kc.cuda(), vc.cuda(),
-                              torch.from_numpy(tbl).cuda(), torch.from_numpy(ln).cuda(), scale,
-                              out)
+                              torch.from_numpy(tbl).cuda(), torch.from_numpy(ln).cuda(), mq, scale,
+                              out, ws)
     return out
 
 
@@ -172,10 +185,95 @@ def test_bad_inputs_are_flagged_and_skipped():
     assert binding.pa_check_device_errors() & binding.DEVERR["BLOCK_ID"]
 
 
-@pytest.mark.parametrize("H,Hkv,d", [(28, 4, 128), (8, 2, 64)])
-def test_unsupported_shapes_are_refused(H, Hkv, d):
-    kc, vc, tbl, ln, qs, q = _setup([40], [8], H, Hkv, d, 16, torch.float16, 27)
+@pytest.mark.parametrize("H,Hkv,d,qlen", [(28, 4, 128, 40), (8, 2, 64, 8)])
+def test_unsupported_shapes_are_refused(H, Hkv, d, qlen):
+    """Head dim 64; a grouping that is not a power of two with more rows per
+    sequence than one tile holds (40 tokens x 7 heads)."""
+    kc, vc, tbl, ln, qs, q = _setup([60], [qlen], H, Hkv, d, 16, torch.float16, 27)
     with pytest.raises(binding.PaError) as e:
         _gpu(kc, vc, tbl, ln, qs, q, 0.1)
     assert binding.STATUS_NAMES[e.value.status] == "PA_ERR_UNSUPPORTED"
     assert binding.pa_check_device_errors() == 0
+
+
+# ---- the split mode: one query tile per (sequence, KV head) ---------------------
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_speculative_verification_full_size(dtype):
+    """128 sequences of the Qwen long-tail shape (28 / 4 heads: G = 7, 42 rows
+    a tile) verifying 6 tokens each; the long contexts are split over CTAs."""
+    w = wl.qwen_longtail(16)
+    lens = np.asarray(w.context_lens, np.int64) + 6
+    kc, vc, tbl, ln, qs, q = _setup(lens, [6] * w.B, w.H, w.Hkv, w.d, 16, dtype, 21)
+    out = _gpu(kc, vc, tbl, ln, qs, q, w.scale)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, w.scale), "speculative 128 x 6")
+
+
+@pytest.mark.parametrize("H,Hkv", [(28, 4), (12, 4), (4, 4), (40, 8), (96, 1), (8, 1)])
+@pytest.mark.parametrize("bs,dtype", [(16, torch.bfloat16), (8, torch.float16),
+                                      (32, torch.bfloat16)])
+def test_split_mode_mixed(H, Hkv, bs, dtype):
+    """Groupings 1 .. 96 (powers of two and not), every block size: decode rows,
+    a few draft tokens, one-token contexts, empty query lists, long contexts
+    split between CTAs."""
+    G = H // Hkv
+    mq = max(1, min(6, 128 // G))
+    lens = [1, 37, 6000, 300, 64, 71, 5, 1000, 17000]
+    qlens = [1, min(mq, 6), mq, 1, 0, mq, min(5, mq), mq, 2 if mq >= 2 else 1]
+    kc, vc, tbl, ln, qs, q = _setup(lens, qlens, H, Hkv, 128, bs, dtype, H + bs + 7)
+    scale = 1 / math.sqrt(128)
+    out = _gpu(kc, vc, tbl, ln, qs, q, scale)
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, scale), "split G=%d bs=%d" % (G, bs))
+
+
+def test_split_mode_one_tile_rows():
+    """Rows filling a whole tile in the split mode: 32 tokens x 4 heads over
+    long contexts, two sequences (both split over many CTAs)."""
+    kc, vc, tbl, ln, qs, q = _setup([30000, 9000], [32, 32], 16, 4, 128, 16, torch.bfloat16, 61)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(out.cpu(), _ref(kc, vc, tbl, ln, qs, q, 1 / math.sqrt(128)), "32 x 4 rows")
+
+
+def test_split_mode_reuses_its_workspace():
+    """Few sequences over long contexts (every pair split between CTAs): a
+    reused workspace must come back with every ticket at zero, and repeats are
+    bit-identical."""
+    kc, vc, tbl, ln, qs, q = _setup([20000, 333, 9000], [6, 1, 6], 28, 4, 128, 16,
+                                    torch.bfloat16, 25)
+    ws = _workspace(3, 28, 4)
+    a = _gpu(kc, vc, tbl, ln, qs, q, 0.09, ws=ws)
+    for _ in range(3):
+        assert torch.equal(a, _gpu(kc, vc, tbl, ln, qs, q, 0.09, ws=ws))
+    assert binding.pa_check_device_errors() == 0
+    assert_close(a.cpu(), _ref(kc, vc, tbl, ln, qs, q, 0.09), "split pairs")
+
+
+def test_split_mode_matches_the_decode():
+    """One query token per sequence is the decode: the split mode equals the
+    oracle's decode of the same batch."""
+    lens = [300, 1, 1000, 64, 5000]
+    kc, vc, tbl, ln, qs, q = _setup(lens, [1] * 5, 8, 2, 128, 16, torch.float16, 24)
+    out = _gpu(kc, vc, tbl, ln, qs, q, 0.1)
+    assert binding.pa_check_device_errors() == 0
+    ref = oracle.decode(wl.bits(q), wl.bits(kc), wl.bits(vc), tbl, ln, 0.1, oracle.DTYPE_F16,
+                        num_threads=THREADS)
+    assert_close(out.cpu(), ref, "decode rows")
+
+
+def test_split_mode_flags_bad_inputs():
+    """More queries than max_q_len promised, or than cached tokens: skipped
+    and flagged; the other sequences are right."""
+    kc, vc, tbl, ln, qs, q = _setup([10, 200, 50], [3, 6, 4], 28, 4, 128, 16, torch.float16, 28)
+    ln_bad = ln.copy()
+    ln_bad[0] = 2
+    out = _gpu(kc, vc, tbl, ln_bad, qs, q, 0.125, max_q_len=6)
+    assert binding.pa_check_device_errors() & binding.DEVERR["CONTEXT"]
+    assert torch.isnan(out[:3].float()).all()
+    assert_close(out[3:].cpu(), _ref(kc, vc, tbl, ln, qs, q, 0.125)[3:], "the valid sequences")
+    out = _gpu(kc, vc, tbl, ln, qs, q, 0.125, max_q_len=5)   # sequence 1 has 6
+    assert binding.pa_check_device_errors() & binding.DEVERR["CONTEXT"]
+    assert torch.isnan(out[3:9].float()).all()
