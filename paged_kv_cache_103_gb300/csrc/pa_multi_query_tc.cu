@@ -87,8 +87,9 @@ __host__ __device__ constexpr uint32_t smem_total(int B) {
 // mbarrier slots; the per-tile ones come in pairs (tile w at + w)
 enum : int {
     kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
-    kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18, kWs1 = 19,
-    kQFull1 = 20, kQEmpty1 = 21   // the split mode's second Q stage
+    kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18,
+    kQFull1 = 20, kQEmpty1 = 21,   // the split mode's second Q stage
+    kWgSync = 22                   // the split mode's per-warpgroup barriers (+ wt)
 };
 
 struct Params {
@@ -742,13 +743,20 @@ multi_query_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 // finish the pair -- an acquire-release ticket, never a wait -- folds them.
 
 constexpr int kMinTilesPerCta = 2;
+// Work units a (sequence, KV head) pair costs beyond its key tiles: its
+// segment's end (the merge of the two warpgroups' states and the output or
+// partial store) takes about two key tiles' time, so a share of many short
+// pairs gets fewer tiles.  The units sit before the pair's first tile on the
+// flattened line the CTAs split evenly.
+constexpr int kPairUnits = 2;
+constexpr int kFoldRows = 4;   // rows a warp folds at once
 constexpr uint32_t kSOffQ = 0;                                   // two Q stages
 constexpr uint32_t kSOffK = kSOffQ + 2 * kTileBytes;
 constexpr uint32_t kSOffV = kSOffK + kKStages * kTileBytes;
-constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // warpgroup 1's m, l [2][128]
-constexpr uint32_t kSOffBar = kSOffRow + 2 * kM * 4;
-constexpr uint32_t kSOffMisc = kSOffBar + kNumBars * 8;           // TMEM base, dead flag, last flag
-constexpr uint32_t kSOffPrefix = kSOffMisc + 16;
+constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // merge and fold row values
+constexpr uint32_t kSOffBar = kSOffRow + 12 * kM * 4;
+constexpr uint32_t kSOffMisc = kSOffBar + kNumBars * 8;   // TMEM base, dead flag, flags per warpgroup
+constexpr uint32_t kSOffPrefix = kSOffMisc + 32;
 constexpr size_t kSlotFloats = (size_t)kM * (kD + 2);            // O rows, then M, then L
 
 __host__ __device__ constexpr uint32_t split_smem_total(int B) {
@@ -768,7 +776,9 @@ struct SParams {
 };
 
 struct SSeg {
-    int32_t i, g, kt0, len, nkt, a;   // a: flattened index of the pair's first key tile
+    int32_t i, g, kt0, len, nkt;
+    int32_t a;      // the pair's first unit on the flattened line (its tile 0 at a + kPairUnits)
+    int32_t next;   // the line position after the segment
     int32_t n, qlen, q0;
 };
 
@@ -776,6 +786,8 @@ __device__ __forceinline__ int32_t s_begin(int64_t c, int64_t F, int64_t C) {
     return (int32_t)(c * F / C);
 }
 
+// The segment of the share [pos, hi) that begins at the first key tile at or
+// after pos (len = 0: no tile left in the share).
 __device__ __forceinline__ SSeg s_segment(const SParams& p, const int32_t* prefix, int32_t pos,
                                           int32_t hi) {
     int32_t lo = 0, hb = p.B;   // largest i with prefix[i] <= pos
@@ -785,12 +797,15 @@ __device__ __forceinline__ SSeg s_segment(const SParams& p, const int32_t* prefi
     }
     SSeg s;
     s.i = lo;
-    s.nkt = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+    const int32_t units = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+    s.nkt = units - kPairUnits;
     const int32_t local = pos - prefix[lo];
-    s.g = local / s.nkt;
-    s.kt0 = local - s.g * s.nkt;
-    s.a = prefix[lo] + s.g * s.nkt;
-    s.len = min(hi - pos, s.nkt - s.kt0);
+    s.g = local / units;
+    s.a = prefix[lo] + s.g * units;
+    const int32_t start = max(pos, s.a + kPairUnits);
+    s.kt0 = start - s.a - kPairUnits;
+    s.len = max(0, min(hi - start, s.nkt - s.kt0));
+    s.next = start + s.len;
     s.n = clamp_len(__ldg(p.context_lens + lo), p.max_blocks * p.bs);
     s.q0 = __ldg(p.q_start + lo);
     s.qlen = __ldg(p.q_start + lo + 1) - s.q0;
@@ -814,7 +829,8 @@ __device__ __forceinline__ void s_produce(const SParams& p, const int32_t* prefi
     int32_t r = 0, q_issued = 0;
     for (int32_t pos = lo; pos < hi; ++r) {
         const SSeg sg = s_segment(p, prefix, pos, hi);
-        pos += sg.len;
+        if (sg.len == 0) break;
+        pos = sg.next;
         if (with_q) {
             // Q stage r % 2: the next segment's Q travels while this one computes
             const int qs = r & 1;
@@ -891,16 +907,19 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSOffMisc);
     volatile int* dead = reinterpret_cast<volatile int*>(smem + kSOffMisc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);
-    float* row_m1 = reinterpret_cast<float*>(smem + kSOffRow);
-    float* row_l1 = row_m1 + kM;
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);    // [2]
+    volatile int* seg_role = reinterpret_cast<volatile int*>(smem + kSOffMisc + 16);    // [2]
+    int* seg_arrive = reinterpret_cast<int*>(smem + kSOffMisc + 24);                    // [2]
+    float* row_ml = reinterpret_cast<float*>(smem + kSOffRow);   // [2 parities][2 wgs][m, l][128]
+    float* fold_ml = row_ml + 8 * kM;                            // [2 wgs][max, 1 / sum][128]
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSOffPrefix);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = p.B;
     const int32_t max_len = p.max_blocks * p.bs;
 
-    // ---- prefix of key tiles: prefix[i] = Hkv * sum_{i' < i} ceil(n_i' / 128),
-    // by warp 0 (lane l sums a contiguous slice of the sequences, then a scan)
+    // ---- prefix of work units: prefix[i] = Hkv * sum_{i' < i} u_i', with
+    // u = ceil(n / 128) + kPairUnits for a sequence with query rows and keys,
+    // else 0; by warp 0 (lane l sums a contiguous slice, then a scan)
     if (warp == 0) {
         const int32_t per = (B + 31) / 32;
         const int32_t beg = min(lane * per, B), end = min(beg + per, B);
@@ -913,7 +932,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 if (raw > max_len) pa::raise_error(p.err, PA_DEVERR_TABLE_WIDTH);
                 if (bad) pa::raise_error(p.err, PA_DEVERR_CONTEXT);
             }
-            return (ql > 0 && !bad) ? p.Hkv * ((n + kN - 1) / kN) : 0;
+            return (ql > 0 && !bad) ? p.Hkv * ((n + kN - 1) / kN + kPairUnits) : 0;
         };
         int32_t local = 0;
         for (int32_t i = beg; i < end; ++i) local += tiles_of(i, true);
@@ -935,9 +954,12 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
         pa::mbar_init(&bar[kPFull], 4);
         pa::mbar_init(&bar[kPFull + 1], 4);
         pa::mbar_init(&bar[kOFree], 4);
-        pa::mbar_init(&bar[kWs1], 4);
+        pa::mbar_init(&bar[kWgSync], 4);
+        pa::mbar_init(&bar[kWgSync + 1], 4);
         pa::fence_barrier_init();
         *dead = 0;
+        seg_arrive[0] = 0;
+        seg_arrive[1] = 0;
     }
     __syncthreads();
     const int64_t F = prefix[B];
@@ -1008,7 +1030,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             int32_t r = 0;
             for (int32_t pos = lo; pos < hi && alive; ++r) {
                 const SSeg sg = s_segment(p, prefix, pos, hi);
-                pos += sg.len;
+                if (sg.len == 0) break;
+                pos = sg.next;
                 const bool residual =
                     kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);   // the first row's keys
                 const int qs = r & 1;
@@ -1072,8 +1095,15 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
         const uint32_t sp_col = lane_base + wt * 256;
         const uint32_t o_col = sp_col + 128;
         const float c2 = p.scale_log2;
-        uint32_t sc = 0, pvc = 0;
+        uint32_t sc = 0, pvc = 0, wsc = 0;
         uint32_t vbase = 0;   // key tiles of the share's earlier segments (V ring position)
+        // the warpgroup's four warps meet (a bounded wait; release and
+        // acquire order their shared and global stores for one another)
+        auto wg_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kWgSync + wt]);
+            return warp_wait(&bar[kWgSync + wt], (wsc++) & 1, dead);
+        };
         auto wait_pv = [&]() {
             const bool ok = warp_wait(&bar[kPvDone + wt], pvc & 1, dead);
             ++pvc;
@@ -1082,7 +1112,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
         int32_t r = 0;
         for (int32_t pos = lo; pos < hi; ++r) {
             const SSeg sg = s_segment(p, prefix, pos, hi);
-            pos += sg.len;
+            if (sg.len == 0) break;
+            pos = sg.next;
             const uint32_t vb0 = vbase;
             vbase += (uint32_t)sg.len;
             const int32_t rows = sg.qlen * p.G;
@@ -1272,28 +1303,41 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
             }
             if (!ok) break;
-            // ---- this warpgroup's last product, then the merge of the two
+            // ---- this warpgroup's last product; the warpgroup that finishes the
+            // segment second merges the two states, the first moves on to its
+            // next segment (whose products wait for O to be read out)
             if (mine > 0) {
                 if (!wait_pv()) break;
                 pa::tc_fence_after();
             }
-            if (wt == 1) {
-                // warpgroup 0 has read the previous segment's values
-                if (r > 0 && !warp_wait(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) break;
-                row_m1[row] = mine > 0 ? m_used : -INFINITY;
-                row_l1[row] = mine > 0 ? l : 0.f;
-                pa::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) pa::mbar_arrive(&bar[kWs1]);
-                continue;
+            // the previous segment's merge has read its row values (a warpgroup
+            // without a tile here could otherwise run two segments ahead and
+            // overwrite the values of this parity)
+            if (r > 0 && !warp_wait(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) break;
+            float* my_ml = row_ml + ((r & 1) * 2 + wt) * 2 * kM;
+            my_ml[row] = mine > 0 ? m_used : -INFINITY;
+            my_ml[kM + row] = mine > 0 ? l : 0.f;
+            pa::tc_fence_before();
+            if (!wg_sync()) break;
+            if (row == 0) {
+                // arrivals at parity r & 1 count up by two per use: an odd count
+                // before this one means the other warpgroup is done
+                __threadfence_block();
+                seg_role[wt] = atomicAdd(&seg_arrive[r & 1], 1) & 1;
+                __threadfence_block();
             }
-            if (!warp_wait(&bar[kWs1], (uint32_t)(r & 1), dead)) break;
+            if (!wg_sync()) break;
+            if (seg_role[wt] == 0) continue;
             pa::tc_fence_after();
-            const float m1 = row_m1[row], l1 = row_l1[row];
-            const float M = fmaxf(m_used, m1);
+            const float* oth = row_ml + ((r & 1) * 2 + (wt ^ 1)) * 2 * kM;
+            const float mo = oth[row], lo_ = oth[kM + row];
+            const float mm = mine > 0 ? m_used : -INFINITY, lm = mine > 0 ? l : 0.f;
+            const float m0 = wt == 0 ? mm : mo, l0 = wt == 0 ? lm : lo_;
+            const float m1 = wt == 0 ? mo : mm, l1 = wt == 0 ? lo_ : lm;
+            const float M = fmaxf(m0, m1);
             const float Ms = M == -INFINITY ? 0.f : M;
-            const float f0 = pa::fast_exp2(m_used - Ms), f1 = pa::fast_exp2(m1 - Ms);
-            const float L = f0 * l + f1 * l1;
+            const float f0 = pa::fast_exp2(m0 - Ms), f1 = pa::fast_exp2(m1 - Ms);
+            const float L = f0 * l0 + f1 * l1;
             const bool two = sg.len > 1;   // warpgroup 1 had a tile
             const bool whole = sg.kt0 == 0 && sg.len == sg.nkt;
             const int32_t hq = sg.g * p.G + (row - t_row * p.G);
@@ -1346,57 +1390,83 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             // Publish: the warpgroup barrier orders every thread's partial
             // stores before thread 0's release; the ticket names the pair's last
             // CTA and, for it, acquires every other CTA's partial.
-            pa::named_barrier_sync(1, 128);
-            const int64_t c_first = ((int64_t)(sg.a + 1) * C - 1) / F;
-            const int64_t c_last = ((int64_t)(sg.a + sg.nkt) * C - 1) / F;
+            if (!wg_sync()) break;
+            // the CTAs holding the pair's first and last key tiles
+            const int64_t t0 = (int64_t)sg.a + kPairUnits;
+            const int64_t c_first = ((t0 + 1) * C - 1) / F;
+            const int64_t c_last = ((t0 + sg.nkt) * C - 1) / F;
             if (row == 0) {
                 int32_t* ctr = p.counters + (int64_t)sg.i * p.Hkv + sg.g;
                 const int prev = pa::atomic_add_acq_rel_gpu(ctr, 1);
                 const int last = prev == (int)(c_last - c_first);
                 if (last) atomicExch(ctr, 0);
-                *last_flag = last;
+                last_flag[wt] = last;
             }
-            pa::named_barrier_sync(1, 128);
-            if (!*last_flag || !valid) continue;
-            // The pair's last CTA: fold every covering CTA's rows.
+            if (!wg_sync()) break;
+            if (!last_flag[wt]) continue;
+            // The pair's last CTA folds every covering CTA's rows.  The first
+            // covering CTA holds the pair in its first slot when the pair is its
+            // first segment; every later one holds it in its first slot.
             const int ncov = (int)(c_last - c_first + 1);
-            const int64_t slot0 = 2 * c_first + (s_begin(c_first, F, C) == sg.a ? 0 : 1);
-            float Mx = -INFINITY;
-            for (int c = 0; c < ncov; ++c) {
-                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-                Mx = fmaxf(Mx, __ldcg(q + (size_t)kM * kD + row));
-            }
-            const float Mxs = Mx == -INFINITY ? 0.f : Mx;
-            float Ls = 0.f;
-            for (int c = 0; c < ncov; ++c) {
-                const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-                Ls += pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs) *
-                      __ldcg(q + (size_t)kM * kD + kM + row);
-            }
-            const float finv = Ls > 0.f ? 1.f / Ls : 0.f;
-            for (int d8 = 0; d8 < kD; d8 += 8) {
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const int64_t slot0 = 2 * c_first + (s_begin(c_first, F, C) >= sg.a ? 0 : 1);
+            auto slot_ptr = [&](int c) {
+                return p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
+            };
+            // per row (thread = row): the common maximum and 1 / sum
+            float* fold = fold_ml + wt * 2 * kM;
+            {
+                float Mx = -INFINITY;
+                for (int c = 0; c < ncov; ++c)
+                    Mx = fmaxf(Mx, __ldcg(slot_ptr(c) + (size_t)kM * kD + row));
+                const float Mxs = Mx == -INFINITY ? 0.f : Mx;
+                float Ls = 0.f;
                 for (int c = 0; c < ncov; ++c) {
-                    const float* q = p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
-                    const float f = pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs);
-                    const float4 a = __ldcg(reinterpret_cast<const float4*>(q + (size_t)row * kD + d8));
-                    const float4 b =
-                        __ldcg(reinterpret_cast<const float4*>(q + (size_t)row * kD + d8 + 4));
-                    acc[0] += f * a.x;
-                    acc[1] += f * a.y;
-                    acc[2] += f * a.z;
-                    acc[3] += f * a.w;
-                    acc[4] += f * b.x;
-                    acc[5] += f * b.y;
-                    acc[6] += f * b.z;
-                    acc[7] += f * b.w;
+                    const float* q = slot_ptr(c);
+                    Ls += pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs) *
+                          __ldcg(q + (size_t)kM * kD + kM + row);
                 }
-                uint4 x;
-                x.x = pa::pack2<kBF16>(acc[0] * finv, acc[1] * finv);
-                x.y = pa::pack2<kBF16>(acc[2] * finv, acc[3] * finv);
-                x.z = pa::pack2<kBF16>(acc[4] * finv, acc[5] * finv);
-                x.w = pa::pack2<kBF16>(acc[6] * finv, acc[7] * finv);
-                reinterpret_cast<uint4*>(orow)[d8 >> 3] = x;
+                fold[row] = Mxs;
+                fold[kM + row] = Ls > 0.f ? 1.f / Ls : 0.f;
+            }
+            if (!wg_sync()) break;
+            // per row (warp = 32 rows, lane = 4 of its 128 values): coalesced
+            // 512-byte reads, kFoldRows rows in flight per covering CTA
+            const int rows_valid = sg.qlen * p.G;
+#pragma unroll 1
+            for (int r0 = wq * 32; r0 < wq * 32 + 32 && r0 < rows_valid; r0 += kFoldRows) {
+                float4 acc[kFoldRows];
+#pragma unroll
+                for (int k = 0; k < kFoldRows; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                for (int c = 0; c < ncov; ++c) {
+                    const float* q = slot_ptr(c);
+                    float4 v[kFoldRows];
+                    float mc[kFoldRows];
+#pragma unroll
+                    for (int k = 0; k < kFoldRows; ++k) {
+                        v[k] = __ldcg(reinterpret_cast<const float4*>(q + (size_t)(r0 + k) * kD) + lane);
+                        mc[k] = __ldcg(q + (size_t)kM * kD + r0 + k);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kFoldRows; ++k) {
+                        const float f = pa::fast_exp2(mc[k] - fold[r0 + k]) * fold[kM + r0 + k];
+                        acc[k].x += f * v[k].x;
+                        acc[k].y += f * v[k].y;
+                        acc[k].z += f * v[k].z;
+                        acc[k].w += f * v[k].w;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kFoldRows; ++k) {
+                    const int rr = r0 + k;
+                    if (rr >= rows_valid) break;
+                    const int32_t tr = rr / p.G;
+                    uint16_t* o = p.out + ((int64_t)(sg.q0 + tr) * p.H + sg.g * p.G + (rr - tr * p.G)) * kD;
+                    uint2 x;
+                    x.x = pa::pack2<kBF16>(acc[k].x, acc[k].y);
+                    x.y = pa::pack2<kBF16>(acc[k].z, acc[k].w);
+                    reinterpret_cast<uint2*>(o)[lane] = x;
+                }
             }
         }
         if (*dead && row == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
