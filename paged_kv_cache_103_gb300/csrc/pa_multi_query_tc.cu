@@ -749,7 +749,7 @@ constexpr int kMinTilesPerCta = 2;
 // pairs gets fewer tiles.  The units sit before the pair's first tile on the
 // flattened line the CTAs split evenly.
 constexpr int kPairUnits = 2;
-constexpr int kFoldRows = 4;   // rows a warp folds at once
+constexpr int kFoldRows = 8;   // rows a warp folds at once
 constexpr uint32_t kSOffQ = 0;                                   // two Q stages
 constexpr uint32_t kSOffK = kSOffQ + 2 * kTileBytes;
 constexpr uint32_t kSOffV = kSOffK + kKStages * kTileBytes;
@@ -1429,11 +1429,12 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 fold[kM + row] = Ls > 0.f ? 1.f / Ls : 0.f;
             }
             if (!wg_sync()) break;
-            // per row (warp = 32 rows, lane = 4 of its 128 values): coalesced
-            // 512-byte reads, kFoldRows rows in flight per covering CTA
+            // per row (warp wq: rows wq, wq + 4, ...; lane = 4 of the row's 128
+            // values): coalesced 512-byte reads, kFoldRows rows in flight per
+            // covering CTA
             const int rows_valid = sg.qlen * p.G;
 #pragma unroll 1
-            for (int r0 = wq * 32; r0 < wq * 32 + 32 && r0 < rows_valid; r0 += kFoldRows) {
+            for (int r0 = 0; r0 + wq < rows_valid; r0 += 4 * kFoldRows) {
                 float4 acc[kFoldRows];
 #pragma unroll
                 for (int k = 0; k < kFoldRows; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1444,12 +1445,14 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     float mc[kFoldRows];
 #pragma unroll
                     for (int k = 0; k < kFoldRows; ++k) {
-                        v[k] = __ldcg(reinterpret_cast<const float4*>(q + (size_t)(r0 + k) * kD) + lane);
-                        mc[k] = __ldcg(q + (size_t)kM * kD + r0 + k);
+                        const int rr = min(r0 + 4 * k + wq, kM - 1);
+                        v[k] = __ldcg(reinterpret_cast<const float4*>(q + (size_t)rr * kD) + lane);
+                        mc[k] = __ldcg(q + (size_t)kM * kD + rr);
                     }
 #pragma unroll
                     for (int k = 0; k < kFoldRows; ++k) {
-                        const float f = pa::fast_exp2(mc[k] - fold[r0 + k]) * fold[kM + r0 + k];
+                        const int rr = min(r0 + 4 * k + wq, kM - 1);
+                        const float f = pa::fast_exp2(mc[k] - fold[rr]) * fold[kM + rr];
                         acc[k].x += f * v[k].x;
                         acc[k].y += f * v[k].y;
                         acc[k].z += f * v[k].z;
@@ -1458,7 +1461,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
 #pragma unroll
                 for (int k = 0; k < kFoldRows; ++k) {
-                    const int rr = r0 + k;
+                    const int rr = r0 + 4 * k + wq;
                     if (rr >= rows_valid) break;
                     const int32_t tr = rr / p.G;
                     uint16_t* o = p.out + ((int64_t)(sg.q0 + tr) * p.H + sg.g * p.G + (rr - tr * p.G)) * kD;
