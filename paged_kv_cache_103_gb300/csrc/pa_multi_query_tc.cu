@@ -89,7 +89,8 @@ enum : int {
     kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
     kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18,
     kQFull1 = 20, kQEmpty1 = 21,   // the split mode's second Q stage
-    kWgSync = 22                   // the split mode's per-warpgroup barriers (+ wt)
+    kEpiSync = 19,                 // the split mode's epilogue warps meet
+    kSegDone = 22                  // the split mode: a segment's state handed over (+ O buffer)
 };
 
 struct Params {
@@ -735,26 +736,30 @@ multi_query_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 // Launches in which every sequence's rows fit one 128-row tile (max_q_len * G
 // <= 128: speculative verification, decode-like batches; any G up to 128)
 // split the work like the decode: the flattened list of (sequence i, KV head g,
-// 128-key tile) is cut into equal contiguous shares over the CTAs.  Inside a
-// share the two softmax warpgroups take alternate key tiles of the same query
-// tile (warpgroup w the tiles j with j % 2 == w) and warpgroup 0 merges the
-// two states from TMEM at the pair's end.  A pair split between CTAs leaves
+// 128-key tile) is cut into equal contiguous shares over the CTAs.  One
+// softmax warpgroup takes every key tile of the share, with two S buffers in
+// TMEM so that the next tile's scores are computed while it works; a second
+// warpgroup reads each segment's O out of one of two O buffers while the
+// next segment accumulates in the other.  A pair split between CTAs leaves
 // its (M, L, O) rows in one of the CTA's two workspace slots; the last CTA to
 // finish the pair -- an acquire-release ticket, never a wait -- folds them.
 
 constexpr int kMinTilesPerCta = 2;
-// Work units a (sequence, KV head) pair costs beyond its key tiles: its
-// segment's end (the merge of the two warpgroups' states and the output or
-// partial store) takes about two key tiles' time, so a share of many short
-// pairs gets fewer tiles.  The units sit before the pair's first tile on the
-// flattened line the CTAs split evenly.
-constexpr int kPairUnits = 2;
+// Work units a (sequence, KV head) pair costs beyond its key tiles (the
+// segment's start and end: pipeline refill, the last product's latency), so
+// a share of many short pairs gets fewer tiles.  The units sit before the
+// pair's first tile on the flattened line the CTAs split evenly.
+constexpr int kPairUnits = 4;
 constexpr int kFoldRows = 8;   // rows a warp folds at once
+// TMEM: two S / P buffers of 128 key columns, then two O buffers of d columns
+// (segment r accumulates in O buffer r % 2, read out while r + 1 runs)
+constexpr uint32_t kSBufCols = kN;
+constexpr uint32_t kOCol = 2 * kSBufCols;
 constexpr uint32_t kSOffQ = 0;                                   // two Q stages
 constexpr uint32_t kSOffK = kSOffQ + 2 * kTileBytes;
 constexpr uint32_t kSOffV = kSOffK + kKStages * kTileBytes;
-constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // merge and fold row values
-constexpr uint32_t kSOffBar = kSOffRow + 12 * kM * 4;
+constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // (m, l) and fold row values
+constexpr uint32_t kSOffBar = kSOffRow + 6 * kM * 4;
 constexpr uint32_t kSOffMisc = kSOffBar + kNumBars * 8;   // TMEM base, dead flag, flags per warpgroup
 constexpr uint32_t kSOffPrefix = kSOffMisc + 32;
 constexpr size_t kSlotFloats = (size_t)kM * (kD + 2);            // O rows, then M, then L
@@ -907,11 +912,9 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSOffMisc);
     volatile int* dead = reinterpret_cast<volatile int*>(smem + kSOffMisc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);    // [2]
-    volatile int* seg_role = reinterpret_cast<volatile int*>(smem + kSOffMisc + 16);    // [2]
-    int* seg_arrive = reinterpret_cast<int*>(smem + kSOffMisc + 24);                    // [2]
-    float* row_ml = reinterpret_cast<float*>(smem + kSOffRow);   // [2 parities][2 wgs][m, l][128]
-    float* fold_ml = row_ml + 8 * kM;                            // [2 wgs][max, 1 / sum][128]
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);
+    float* row_ml = reinterpret_cast<float*>(smem + kSOffRow);   // [O buffer][m, l][128]
+    float* fold_ml = row_ml + 4 * kM;                            // [max, 1 / sum][128]
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSOffPrefix);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = p.B;
@@ -953,13 +956,13 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int b = 0; b < kNumBars; ++b) pa::mbar_init(&bar[b], 1);
         pa::mbar_init(&bar[kPFull], 4);
         pa::mbar_init(&bar[kPFull + 1], 4);
-        pa::mbar_init(&bar[kOFree], 4);
-        pa::mbar_init(&bar[kWgSync], 4);
-        pa::mbar_init(&bar[kWgSync + 1], 4);
+        for (int b = 0; b < 2; ++b) {
+            pa::mbar_init(&bar[kOFree + b], 4);
+            pa::mbar_init(&bar[kSegDone + b], 4);
+        }
+        pa::mbar_init(&bar[kEpiSync], 4);
         pa::fence_barrier_init();
         *dead = 0;
-        seg_arrive[0] = 0;
-        seg_arrive[1] = 0;
     }
     __syncthreads();
     const int64_t F = prefix[B];
@@ -990,9 +993,9 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                   &bar[kVEmpty], kVStages, bar, dead, lane);
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
-        // Per segment: S_0(0), S_1(1), then PV_w(j), S_w(j + 2) for j = 0, 1,
-        // ... (w = j % 2): S_w(j + 2) overwrites the TMEM columns of P_w(j) and
-        // is issued after PV_w(j).
+        // Per segment: S(0) -> buffer 0, S(1) -> buffer 1, then for each key
+        // tile j: PV(j) into the segment's O buffer (r % 2), and S(j + 2) into
+        // buffer j % 2 -- after PV(j), which reads P(j) from those columns.
         if (lane == 0) {
             constexpr uint32_t idS = pa::idesc_f16(kBF16, false, kM, kN);
             constexpr uint32_t idPV = pa::idesc_f16(kBF16, true, kM, kD);
@@ -1000,9 +1003,9 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             const uint32_t sK = pa::smem_addr(smem + kSOffK);
             const uint32_t sV = pa::smem_addr(smem + kSOffV);
             uint32_t kc = 0, vc = 0;
-            uint32_t pc[kTiles] = {0, 0};
+            uint32_t pc[2] = {0, 0};
             bool alive = true;
-            auto s_mma = [&](int w, uint32_t qb) {   // S_w = Q K^T for the next K tile
+            auto s_mma = [&](int b, uint32_t qb) {   // S into buffer b for the next K tile
                 if (!wait_bar(&bar[kKFull + kc % kKStages], (kc / kKStages) & 1, dead)) return false;
                 pa::tc_fence_after();
                 const uint32_t kb = sK + (kc % kKStages) * kTileBytes;
@@ -1010,20 +1013,20 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint64_t a =
                         pa::smem_desc_sw128(qb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b =
+                    const uint64_t bd =
                         pa::smem_desc_sw128(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
-                    pa::umma_f16(tmem + w * 256, a, b, idS, kk > 0 ? 1u : 0u);
+                    pa::umma_f16(tmem + b * kSBufCols, a, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                pa::umma_commit(&bar[kSFull + w]);
+                pa::umma_commit(&bar[kSFull + b]);
                 pa::umma_commit(&bar[kKEmpty + kc % kKStages]);
                 ++kc;
                 return true;
             };
-            auto pv_mma = [&](int w, uint32_t vb, bool accumulate) {
+            auto pv_mma = [&](uint32_t o_tmem, int b, uint32_t vb, bool accumulate) {
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk) {
-                    const uint64_t b = pa::smem_desc_sw128(vb + kk * 4096, 1024, 2048);
-                    pa::umma_f16_tmem_a(tmem + w * 256 + 128, tmem + w * 256 + kk * 8, b, idPV,
+                    const uint64_t bd = pa::smem_desc_sw128(vb + kk * 4096, 1024, 2048);
+                    pa::umma_f16_tmem_a(o_tmem, tmem + b * kSBufCols + kk * 8, bd, idPV,
                                         (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
@@ -1036,45 +1039,47 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);   // the first row's keys
                 const int qs = r & 1;
                 const uint32_t qb = sQ + qs * kTileBytes;
+                const uint32_t o_tmem = tmem + kOCol + (uint32_t)(r & 1) * kD;
                 if (!wait_bar(&bar[qs ? kQFull1 : kQFull], (uint32_t)((r >> 1) & 1), dead)) break;
-                for (int w = 0; w < kTiles && w < sg.len; ++w)
-                    if (!s_mma(w, qb)) {
+                for (int b = 0; b < 2 && b < sg.len; ++b)
+                    if (!s_mma(b, qb)) {
                         alive = false;
                         break;
                     }
                 for (int32_t j = 0; j < sg.len && alive; ++j) {
-                    const int w = j & 1;
-                    // O tiles of the previous segment read out first
-                    if (j == 0 && r > 0 && !wait_bar(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) {
+                    const int b = j & 1;
+                    // this O buffer's previous segment (r - 2) read out first
+                    if (j == 0 && r >= 2 &&
+                        !wait_bar(&bar[kOFree + (r & 1)], (uint32_t)(((r >> 1) - 1) & 1), dead)) {
                         alive = false;
                         break;
                     }
-                    if (!wait_bar(&bar[kPFull + w], pc[w] & 1, dead)) {
+                    if (!wait_bar(&bar[kPFull + b], pc[b] & 1, dead)) {
                         alive = false;
                         break;
                     }
-                    ++pc[w];
+                    ++pc[b];
                     if (!wait_bar(&bar[kVFull + vc % kVStages], (vc / kVStages) & 1, dead)) {
                         alive = false;
                         break;
                     }
                     pa::tc_fence_after();
                     const uint32_t vb = sV + (vc % kVStages) * kTileBytes;
-                    pv_mma(w, vb, j >= 2);
+                    pv_mma(o_tmem, b, vb, j > 0);
                     if (residual) {
-                        pa::umma_commit(&bar[kPvDone + w]);   // P's high part read
-                        if (!wait_bar(&bar[kPFull + w], pc[w] & 1, dead)) {
+                        pa::umma_commit(&bar[kPvDone]);   // P's high part read
+                        if (!wait_bar(&bar[kPFull + b], pc[b] & 1, dead)) {
                             alive = false;
                             break;
                         }
-                        ++pc[w];
+                        ++pc[b];
                         pa::tc_fence_after();
-                        pv_mma(w, vb, true);
+                        pv_mma(o_tmem, b, vb, true);
                     }
-                    pa::umma_commit(&bar[kPvDone + w]);
+                    pa::umma_commit(&bar[kPvDone]);
                     pa::umma_commit(&bar[kVEmpty + vc % kVStages]);
                     ++vc;
-                    if (j + 2 < sg.len && !s_mma(w, qb)) {
+                    if (j + 2 < sg.len && !s_mma(b, qb)) {
                         alive = false;
                         break;
                     }
@@ -1086,26 +1091,18 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             pa::mbar_wait(&bar[kDrain], 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ============================== softmax ==============================
-        const int wt = (warp - 4) >> 2;   // the key tiles j % 2 == wt of each segment
+        // Every key tile of the share; S(j + 1) is computed in the other
+        // buffer while this one is worked on.
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t sp_col = lane_base + wt * 256;
-        const uint32_t o_col = sp_col + 128;
         const float c2 = p.scale_log2;
-        uint32_t sc = 0, pvc = 0, wsc = 0;
+        uint32_t sc[2] = {0, 0}, pvc = 0;
         uint32_t vbase = 0;   // key tiles of the share's earlier segments (V ring position)
-        // the warpgroup's four warps meet (a bounded wait; release and
-        // acquire order their shared and global stores for one another)
-        auto wg_sync = [&]() {
-            __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&bar[kWgSync + wt]);
-            return warp_wait(&bar[kWgSync + wt], (wsc++) & 1, dead);
-        };
         auto wait_pv = [&]() {
-            const bool ok = warp_wait(&bar[kPvDone + wt], pvc & 1, dead);
+            const bool ok = warp_wait(&bar[kPvDone], pvc & 1, dead);
             ++pvc;
             return ok;
         };
@@ -1122,15 +1119,17 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             const int32_t lim_min = sg.n - sg.qlen;                 // the first row's limit
             const int32_t lim = valid ? lim_min + t_row : -1;
             const bool residual = kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);
+            const uint32_t o_col = lane_base + kOCol + (uint32_t)(r & 1) * kD;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
-            int32_t mine = 0;   // key tiles of this warpgroup in the segment
-            for (int32_t j = wt; j < sg.len; j += 2, ++mine) {
-                if (!warp_wait(&bar[kSFull + wt], sc & 1, dead)) {
+            for (int32_t j = 0; j < sg.len; ++j) {
+                const int b = j & 1;
+                const uint32_t sp_col = lane_base + b * kSBufCols;
+                if (!warp_wait(&bar[kSFull + b], sc[b] & 1, dead)) {
                     ok = false;
                     break;
                 }
-                ++sc;
+                ++sc[b];
                 pa::tc_fence_after();
                 const int32_t key0 = (sg.kt0 + j) * kN;
                 const bool full = key0 + kN - 1 <= lim_min;
@@ -1233,7 +1232,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     }
                 }
                 // this warpgroup's previous tile's product done before O moves
-                if (mine >= 1) {
+                if (j >= 1) {
                     if (!wait_pv()) {
                         ok = false;
                         break;
@@ -1281,64 +1280,64 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
                 pa::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) pa::mbar_arrive(&bar[kPFull + wt]);
+                if (lane == 0) pa::mbar_arrive(&bar[kPFull + b]);
                 if (residual) {
                     if (!wait_pv()) {
                         ok = false;
                         break;
                     }
                     pa::tc_fence_after();
-                    uint32_t a[32], b[32];
+                    uint32_t ra[32], rb[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        a[e] = rl[e];
-                        b[e] = rl[32 + e];
+                        ra[e] = rl[e];
+                        rb[e] = rl[32 + e];
                     }
-                    pa::tmem_st32(sp_col, a);
-                    pa::tmem_st32(sp_col + 32, b);
+                    pa::tmem_st32(sp_col, ra);
+                    pa::tmem_st32(sp_col + 32, rb);
                     pa::tmem_st_wait();
                     pa::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) pa::mbar_arrive(&bar[kPFull + wt]);
+                    if (lane == 0) pa::mbar_arrive(&bar[kPFull + b]);
                 }
             }
             if (!ok) break;
-            // ---- this warpgroup's last product; the warpgroup that finishes the
-            // segment second merges the two states, the first moves on to its
-            // next segment (whose products wait for O to be read out)
-            if (mine > 0) {
-                if (!wait_pv()) break;
-                pa::tc_fence_after();
-            }
-            // the previous segment's merge has read its row values (a warpgroup
-            // without a tile here could otherwise run two segments ahead and
-            // overwrite the values of this parity)
-            if (r > 0 && !warp_wait(&bar[kOFree], (uint32_t)((r - 1) & 1), dead)) break;
-            float* my_ml = row_ml + ((r & 1) * 2 + wt) * 2 * kM;
-            my_ml[row] = mine > 0 ? m_used : -INFINITY;
-            my_ml[kM + row] = mine > 0 ? l : 0.f;
+            // the segment's last product, then its state to the epilogue warpgroup
+            if (!wait_pv()) break;
+            float* ml = row_ml + (r & 1) * 2 * kM;
+            ml[row] = m_used;
+            ml[kM + row] = l;
             pa::tc_fence_before();
-            if (!wg_sync()) break;
-            if (row == 0) {
-                // arrivals at parity r & 1 count up by two per use: an odd count
-                // before this one means the other warpgroup is done
-                __threadfence_block();
-                seg_role[wt] = atomicAdd(&seg_arrive[r & 1], 1) & 1;
-                __threadfence_block();
-            }
-            if (!wg_sync()) break;
-            if (seg_role[wt] == 0) continue;
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kSegDone + (r & 1)]);
+        }
+        if (*dead && row == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+    } else if (warp >= 8) {
+        // ============================== epilogue ==============================
+        // Per segment, once the softmax has handed over its (m, l) and O is
+        // final: O / l to the output (a whole pair) or (O, M, L) to this CTA's
+        // workspace slot; then, for a split pair, the ticket and the fold.
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        uint32_t esc = 0;
+        auto wg_sync = [&]() {   // the four epilogue warps meet (bounded)
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kEpiSync]);
+            return warp_wait(&bar[kEpiSync], (esc++) & 1, dead);
+        };
+        int32_t r = 0;
+        for (int32_t pos = lo; pos < hi; ++r) {
+            const SSeg sg = s_segment(p, prefix, pos, hi);
+            if (sg.len == 0) break;
+            pos = sg.next;
+            if (!warp_wait(&bar[kSegDone + (r & 1)], (uint32_t)((r >> 1) & 1), dead)) break;
             pa::tc_fence_after();
-            const float* oth = row_ml + ((r & 1) * 2 + (wt ^ 1)) * 2 * kM;
-            const float mo = oth[row], lo_ = oth[kM + row];
-            const float mm = mine > 0 ? m_used : -INFINITY, lm = mine > 0 ? l : 0.f;
-            const float m0 = wt == 0 ? mm : mo, l0 = wt == 0 ? lm : lo_;
-            const float m1 = wt == 0 ? mo : mm, l1 = wt == 0 ? lo_ : lm;
-            const float M = fmaxf(m0, m1);
-            const float Ms = M == -INFINITY ? 0.f : M;
-            const float f0 = pa::fast_exp2(m0 - Ms), f1 = pa::fast_exp2(m1 - Ms);
-            const float L = f0 * l0 + f1 * l1;
-            const bool two = sg.len > 1;   // warpgroup 1 had a tile
+            const int32_t rows = sg.qlen * p.G;
+            const bool valid = row < rows;
+            const int32_t t_row = row / p.G;
+            const float* ml = row_ml + (r & 1) * 2 * kM;
+            const float M = ml[row], L = ml[kM + row];
             const bool whole = sg.kt0 == 0 && sg.len == sg.nkt;
             const int32_t hq = sg.g * p.G + (row - t_row * p.G);
             uint16_t* orow = p.out + ((int64_t)(sg.q0 + t_row) * p.H + hq) * kD;
@@ -1349,34 +1348,30 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 ps = p.partials + slot * kSlotFloats;
             }
             const float inv = whole && L > 0.f ? 1.f / L : 1.f;
+            const uint32_t o_col = lane_base + kOCol + (uint32_t)(r & 1) * kD;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                uint32_t o0[32], o1[32];
-                pa::tmem_ld32(lane_base + 128 + c * 32, o0);
-                if (two) pa::tmem_ld32(lane_base + 256 + 128 + c * 32, o1);
+                uint32_t o[32];
+                pa::tmem_ld32(o_col + c * 32, o);
                 pa::tmem_ld_wait();
-                pa::reg_fence32(o0);
-                pa::reg_fence32(o1);
-                float v[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    v[e] = (f0 * __uint_as_float(o0[e]) + (two ? f1 * __uint_as_float(o1[e]) : 0.f)) * inv;
+                pa::reg_fence32(o);
                 if (!valid) continue;
                 if (whole) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 x;
-                        x.x = pa::pack2<kBF16>(v[e], v[e + 1]);
-                        x.y = pa::pack2<kBF16>(v[e + 2], v[e + 3]);
-                        x.z = pa::pack2<kBF16>(v[e + 4], v[e + 5]);
-                        x.w = pa::pack2<kBF16>(v[e + 6], v[e + 7]);
+                        x.x = pa::pack2<kBF16>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        x.y = pa::pack2<kBF16>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        x.z = pa::pack2<kBF16>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        x.w = pa::pack2<kBF16>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
                         reinterpret_cast<uint4*>(orow)[(c * 32 + e) >> 3] = x;
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4*>(ps + (size_t)row * kD + c * 32 + e) =
-                            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                        __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
                 }
             }
             if (!whole && valid) {
@@ -1385,7 +1380,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             pa::tc_fence_before();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&bar[kOFree]);
+            if (lane == 0) pa::mbar_arrive(&bar[kOFree + (r & 1)]);
             if (whole) continue;
             // Publish: the warpgroup barrier orders every thread's partial
             // stores before thread 0's release; the ticket names the pair's last
@@ -1400,10 +1395,10 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 const int prev = pa::atomic_add_acq_rel_gpu(ctr, 1);
                 const int last = prev == (int)(c_last - c_first);
                 if (last) atomicExch(ctr, 0);
-                last_flag[wt] = last;
+                *last_flag = last;
             }
             if (!wg_sync()) break;
-            if (!last_flag[wt]) continue;
+            if (!*last_flag) continue;
             // The pair's last CTA folds every covering CTA's rows.  The first
             // covering CTA holds the pair in its first slot when the pair is its
             // first segment; every later one holds it in its first slot.
@@ -1413,7 +1408,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 return p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
             };
             // per row (thread = row): the common maximum and 1 / sum
-            float* fold = fold_ml + wt * 2 * kM;
+            float* fold = fold_ml;
             {
                 float Mx = -INFINITY;
                 for (int c = 0; c < ncov; ++c)
