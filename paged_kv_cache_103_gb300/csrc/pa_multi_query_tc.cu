@@ -76,7 +76,7 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTiles * kTileBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 26;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;      // TMEM base, dead flag
 constexpr uint32_t kOffPrefix = kOffMisc + 16;             // [B + 1] int32 items
 
@@ -89,8 +89,8 @@ enum : int {
     kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
     kSFull = 10, kPFull = 12, kPvDone = 14, kOFree = 16, kDrain = 18,
     kQFull1 = 20, kQEmpty1 = 21,   // the split mode's second Q stage
-    kEpiSync = 19,                 // the split mode's epilogue warps meet
-    kSegDone = 22                  // the split mode: a segment's state handed over (+ O buffer)
+    kAll8 = 19,                    // the split mode's eight softmax warps meet
+    kXch = 22                      // the split mode's row-quarter pair exchanges (+ quarter)
 };
 
 struct Params {
@@ -736,13 +736,15 @@ multi_query_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 // Launches in which every sequence's rows fit one 128-row tile (max_q_len * G
 // <= 128: speculative verification, decode-like batches; any G up to 128)
 // split the work like the decode: the flattened list of (sequence i, KV head g,
-// 128-key tile) is cut into equal contiguous shares over the CTAs.  One
-// softmax warpgroup takes every key tile of the share, with two S buffers in
-// TMEM so that the next tile's scores are computed while it works; a second
-// warpgroup reads each segment's O out of one of two O buffers while the
-// next segment accumulates in the other.  A pair split between CTAs leaves
-// its (M, L, O) rows in one of the CTA's two workspace slots; the last CTA to
-// finish the pair -- an acquire-release ticket, never a wait -- folds them.
+// 128-key tile) is cut into equal contiguous shares over the CTAs.  Every key
+// tile's scores land in one of two S buffers in TMEM, so the next tile's are
+// computed while this one is worked on; the two softmax warpgroups take one
+// half of the tile's keys each (trading row maxima through shared memory)
+// and, at a segment's end, one half of O, which alternates between two TMEM
+// buffers so that the next segment's products need not wait for the store.
+// A pair split between CTAs leaves its (M, L, O) rows in one of the CTA's two
+// workspace slots; the last CTA to finish the pair -- an acquire-release
+// ticket, never a wait -- folds them.
 
 constexpr int kMinTilesPerCta = 2;
 // Work units a (sequence, KV head) pair costs beyond its key tiles (the
@@ -752,7 +754,8 @@ constexpr int kMinTilesPerCta = 2;
 constexpr int kPairUnits = 4;
 constexpr int kFoldRows = 8;   // rows a warp folds at once
 // TMEM: two S / P buffers of 128 key columns, then two O buffers of d columns
-// (segment r accumulates in O buffer r % 2, read out while r + 1 runs)
+// (segment r accumulates in O buffer r % 2: the next segment's first
+// products need not wait for this one's read-out)
 constexpr uint32_t kSBufCols = kN;
 constexpr uint32_t kOCol = 2 * kSBufCols;
 constexpr uint32_t kSOffQ = 0;                                   // two Q stages
@@ -913,8 +916,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSOffMisc);
     volatile int* dead = reinterpret_cast<volatile int*>(smem + kSOffMisc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kSOffMisc + 8);
-    float* row_ml = reinterpret_cast<float*>(smem + kSOffRow);   // [O buffer][m, l][128]
-    float* fold_ml = row_ml + 4 * kM;                            // [max, 1 / sum][128]
+    float* xch = reinterpret_cast<float*>(smem + kSOffRow);   // [parity][warpgroup][128]
+    float* fold_ml = xch + 4 * kM;                            // [max, 1 / sum][128]
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSOffPrefix);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = p.B;
@@ -954,13 +957,12 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) pa::mbar_init(&bar[b], 1);
-        pa::mbar_init(&bar[kPFull], 4);
-        pa::mbar_init(&bar[kPFull + 1], 4);
         for (int b = 0; b < 2; ++b) {
-            pa::mbar_init(&bar[kOFree + b], 4);
-            pa::mbar_init(&bar[kSegDone + b], 4);
+            pa::mbar_init(&bar[kPFull + b], 8);
+            pa::mbar_init(&bar[kOFree + b], 8);
         }
-        pa::mbar_init(&bar[kEpiSync], 4);
+        for (int q = 0; q < 4; ++q) pa::mbar_init(&bar[kXch + q], 2);
+        pa::mbar_init(&bar[kAll8], 8);
         pa::fence_barrier_init();
         *dead = 0;
     }
@@ -1091,20 +1093,42 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             pa::mbar_wait(&bar[kDrain], 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4) {
         // ============================== softmax ==============================
-        // Every key tile of the share; S(j + 1) is computed in the other
-        // buffer while this one is worked on.
+        // Warpgroup h takes keys [64 h, 64 h + 64) of every tile (P columns
+        // [32 h, 32 h + 32), O columns [64 h, 64 h + 64)); the two warps that
+        // share a row quarter trade their row maxima once per tile and their
+        // row sums once per segment.  At a segment's end both read their half
+        // of O out and store it; for a split pair, the ticket and the fold.
+        const int h = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const float c2 = p.scale_log2;
-        uint32_t sc[2] = {0, 0}, pvc = 0;
+        uint32_t sc[2] = {0, 0}, pvc = 0, xc = 0, ac = 0;
         uint32_t vbase = 0;   // key tiles of the share's earlier segments (V ring position)
         auto wait_pv = [&]() {
             const bool ok = warp_wait(&bar[kPvDone], pvc & 1, dead);
             ++pvc;
             return ok;
+        };
+        // this row's value from the other warpgroup (bounded pair barrier;
+        // the slot's parity alternates, so a slot is rewritten only after the
+        // partner has passed the next exchange, i.e. read this one)
+        auto exchange = [&](float v, float& other) {
+            float* slot = xch + (xc & 1) * 2 * kM;
+            slot[h * kM + row] = v;
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kXch + wq]);
+            const bool ok = warp_wait(&bar[kXch + wq], xc & 1, dead);
+            ++xc;
+            other = slot[(h ^ 1) * kM + row];
+            return ok;
+        };
+        auto all8 = [&]() {   // the eight softmax warps meet (bounded)
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bar[kAll8]);
+            return warp_wait(&bar[kAll8], (ac++) & 1, dead);
         };
         int32_t r = 0;
         for (int32_t pos = lo; pos < hi; ++r) {
@@ -1119,119 +1143,94 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             const int32_t lim_min = sg.n - sg.qlen;                 // the first row's limit
             const int32_t lim = valid ? lim_min + t_row : -1;
             const bool residual = kBF16 && (sg.n - sg.qlen + 1 < kResidualKeys);
-            const uint32_t o_col = lane_base + kOCol + (uint32_t)(r & 1) * kD;
+            const uint32_t o_col = lane_base + kOCol + (uint32_t)(r & 1) * kD + h * 64;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int32_t j = 0; j < sg.len; ++j) {
                 const int b = j & 1;
-                const uint32_t sp_col = lane_base + b * kSBufCols;
+                const uint32_t s_col = lane_base + b * kSBufCols + h * 64;   // this half's scores
+                const uint32_t p_col = lane_base + b * kSBufCols + h * 32;   // this half's P pairs
                 if (!warp_wait(&bar[kSFull + b], sc[b] & 1, dead)) {
                     ok = false;
                     break;
                 }
                 ++sc[b];
                 pa::tc_fence_after();
-                const int32_t key0 = (sg.kt0 + j) * kN;
-                const bool full = key0 + kN - 1 <= lim_min;
+                const int32_t key0 = (sg.kt0 + j) * kN + h * 64;   // this half's first key
+                const bool full = key0 + 63 <= lim_min;
+                uint32_t s0[32], s1[32];
+                pa::tmem_ld32(s_col, s0);
+                pa::tmem_ld32(s_col + 32, s1);
+                pa::tmem_ld_wait();
+                pa::reg_fence32(s0);
+                pa::reg_fence32(s1);
                 float mx = -INFINITY;
                 if (full) {
-#pragma unroll 1
-                    for (int c = 0; c < 4; c += 2) {
-                        uint32_t s0[32], s1[32];
-                        pa::tmem_ld32(sp_col + c * 32, s0);
-                        pa::tmem_ld32(sp_col + c * 32 + 32, s1);
-                        pa::tmem_ld_wait();
-                        pa::reg_fence32(s0);
-                        pa::reg_fence32(s1);
-                        float m2[2] = {mx, -INFINITY};
+                    float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            m2[0] = fmaxf(m2[0], __uint_as_float(s0[e]));
-                            m2[1] = fmaxf(m2[1], __uint_as_float(s1[e]));
-                        }
-                        mx = fmaxf(m2[0], m2[1]);
+                    for (int e = 0; e < 32; ++e) {
+                        m2[0] = fmaxf(m2[0], __uint_as_float(s0[e]));
+                        m2[1] = fmaxf(m2[1], __uint_as_float(s1[e]));
                     }
+                    mx = fmaxf(m2[0], m2[1]);
                 } else {
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t s[32];
-                        pa::tmem_ld32(sp_col + c * 32, s);
-                        pa::tmem_ld_wait();
-                        pa::reg_fence32(s);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (key0 + c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(s[e]));
+                    for (int e = 0; e < 32; ++e) {
+                        if (key0 + e <= lim) mx = fmaxf(mx, __uint_as_float(s0[e]));
+                        if (key0 + 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(s1[e]));
                     }
                 }
-                mx *= c2;
+                float mx_o;
+                if (!exchange(mx, mx_o)) {
+                    ok = false;
+                    break;
+                }
+                mx = fmaxf(mx, mx_o) * c2;   // the same value in both warpgroups
                 const bool grow = mx > m_used + kRescaleLog2;
                 const float m_new = grow ? mx : m_used;
                 const float base = m_new == -INFINITY ? 0.f : m_new;
-                float lsum = 0.f;
-                uint32_t rl[64];
+                float lsum;
+                uint32_t pk[32], rl[32];
                 if (full && !residual) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t s0[32], s1[32];
-                        pa::tmem_ld32(sp_col + hh * 64, s0);
-                        pa::tmem_ld32(sp_col + hh * 64 + 32, s1);
-                        pa::tmem_ld_wait();
-                        pa::reg_fence32(s0);
-                        pa::reg_fence32(s1);
-                        uint32_t pk[32];
-                        float la = 0.f, lb = 0.f;
+                    float la = 0.f, lb = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
-                            const float p1 =
-                                pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
-                            const float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
-                            const float p3 =
-                                pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
-                            la += p0 + p1;
-                            lb += p2 + p3;
-                            pk[e >> 1] = pa::pack2<kBF16>(p0, p1);
-                            pk[16 + (e >> 1)] = pa::pack2<kBF16>(p2, p3);
-                        }
-                        lsum += la + lb;
-                        pa::tmem_st32(sp_col + hh * 32, pk);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
+                        const float p1 = pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
+                        const float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
+                        const float p3 = pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
+                        la += p0 + p1;
+                        lb += p2 + p3;
+                        pk[e >> 1] = pa::pack2<kBF16>(p0, p1);
+                        pk[16 + (e >> 1)] = pa::pack2<kBF16>(p2, p3);
                     }
+                    lsum = la + lb;
                 } else {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t s0[32], s1[32];
-                        pa::tmem_ld32(sp_col + hh * 64, s0);
-                        pa::tmem_ld32(sp_col + hh * 64 + 32, s1);
-                        pa::tmem_ld_wait();
-                        pa::reg_fence32(s0);
-                        pa::reg_fence32(s1);
-                        uint32_t pk[32];
-                        float la = 0.f, lb = 0.f;
-                        const int32_t kl = lim - key0 - hh * 64;
+                    float la = 0.f, lb = 0.f;
+                    const int32_t kl = lim - key0;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
-                            float p1 = pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
-                            float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
-                            float p3 = pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
-                            p0 = e <= kl ? p0 : 0.f;
-                            p1 = e + 1 <= kl ? p1 : 0.f;
-                            p2 = e + 32 <= kl ? p2 : 0.f;
-                            p3 = e + 33 <= kl ? p3 : 0.f;
-                            la += p0 + p1;
-                            lb += p2 + p3;
-                            const uint32_t h01 = pa::pack2<kBF16>(p0, p1);
-                            const uint32_t h23 = pa::pack2<kBF16>(p2, p3);
-                            pk[e >> 1] = h01;
-                            pk[16 + (e >> 1)] = h23;
-                            rl[hh * 32 + (e >> 1)] = pa::bf16x2_residual(h01, p0, p1);
-                            rl[hh * 32 + 16 + (e >> 1)] = pa::bf16x2_residual(h23, p2, p3);
-                        }
-                        lsum += la + lb;
-                        pa::tmem_st32(sp_col + hh * 32, pk);
+                    for (int e = 0; e < 32; e += 2) {
+                        float p0 = pa::fast_exp2(fmaf(__uint_as_float(s0[e]), c2, -base));
+                        float p1 = pa::fast_exp2(fmaf(__uint_as_float(s0[e + 1]), c2, -base));
+                        float p2 = pa::fast_exp2(fmaf(__uint_as_float(s1[e]), c2, -base));
+                        float p3 = pa::fast_exp2(fmaf(__uint_as_float(s1[e + 1]), c2, -base));
+                        p0 = e <= kl ? p0 : 0.f;
+                        p1 = e + 1 <= kl ? p1 : 0.f;
+                        p2 = e + 32 <= kl ? p2 : 0.f;
+                        p3 = e + 33 <= kl ? p3 : 0.f;
+                        la += p0 + p1;
+                        lb += p2 + p3;
+                        const uint32_t h01 = pa::pack2<kBF16>(p0, p1);
+                        const uint32_t h23 = pa::pack2<kBF16>(p2, p3);
+                        pk[e >> 1] = h01;
+                        pk[16 + (e >> 1)] = h23;
+                        rl[e >> 1] = pa::bf16x2_residual(h01, p0, p1);
+                        rl[16 + (e >> 1)] = pa::bf16x2_residual(h23, p2, p3);
                     }
+                    lsum = la + lb;
                 }
-                // this warpgroup's previous tile's product done before O moves
+                pa::tmem_st32(p_col, pk);
+                // the previous tile's product done before O moves
                 if (j >= 1) {
                     if (!wait_pv()) {
                         ok = false;
@@ -1242,7 +1241,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                         const float f = grow ? pa::fast_exp2(m_used - m_new) : 1.f;
                         l *= f;
 #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < 2; ++c) {
                             uint32_t o[32];
                             pa::tmem_ld32(o_col + c * 32, o);
                             pa::tmem_ld_wait();
@@ -1257,24 +1256,22 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 pa::tmem_st_wait();
                 m_used = m_new;
                 l += lsum;
-                if (key0 + kN > sg.n) {
-                    // rows past the context: zero them in V (both halves) once the
-                    // tile has landed; only this warpgroup reads this tile
+                if ((sg.kt0 + j) * kN + kN > sg.n) {
+                    // keys past the context: their V rows zeroed (this warpgroup
+                    // the 128-byte half h of each row) once the tile has landed
                     const uint32_t vt = vb0 + (uint32_t)j;
                     const uint32_t vs = vt % kVStages;
                     if (!warp_wait(&bar[kVFull + vs], (vt / kVStages) & 1, dead)) {
                         ok = false;
                         break;
                     }
-                    if (key0 + row >= sg.n) {
+                    if ((sg.kt0 + j) * kN + row >= sg.n) {
                         unsigned char* vrow = smem + kSOffV + vs * kTileBytes +
-                                              (uint32_t)(row >> 3) * 2048 + (uint32_t)(row & 7) * 128;
+                                              (uint32_t)(row >> 3) * 2048 + (uint32_t)(row & 7) * 128 +
+                                              (uint32_t)h * 1024;
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                            for (int c16 = 0; c16 < 8; ++c16)
-                                *reinterpret_cast<uint4*>(vrow + hf * 1024 + c16 * 16) =
-                                    make_uint4(0, 0, 0, 0);
+                        for (int c16 = 0; c16 < 8; ++c16)
+                            *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
                     }
                     pa::fence_proxy_async_smem();
                 }
@@ -1282,19 +1279,13 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
                 if (lane == 0) pa::mbar_arrive(&bar[kPFull + b]);
                 if (residual) {
+                    // the bf16 rounding residual of P, a second product over V
                     if (!wait_pv()) {
                         ok = false;
                         break;
                     }
                     pa::tc_fence_after();
-                    uint32_t ra[32], rb[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        ra[e] = rl[e];
-                        rb[e] = rl[32 + e];
-                    }
-                    pa::tmem_st32(sp_col, ra);
-                    pa::tmem_st32(sp_col + 32, rb);
+                    pa::tmem_st32(p_col, rl);
                     pa::tmem_st_wait();
                     pa::tc_fence_before();
                     __syncwarp();
@@ -1302,45 +1293,16 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
             }
             if (!ok) break;
-            // the segment's last product, then its state to the epilogue warpgroup
+            // ---- the segment's end: the last product, the row sums, then O
             if (!wait_pv()) break;
-            float* ml = row_ml + (r & 1) * 2 * kM;
-            ml[row] = m_used;
-            ml[kM + row] = l;
-            pa::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&bar[kSegDone + (r & 1)]);
-        }
-        if (*dead && row == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
-    } else if (warp >= 8) {
-        // ============================== epilogue ==============================
-        // Per segment, once the softmax has handed over its (m, l) and O is
-        // final: O / l to the output (a whole pair) or (O, M, L) to this CTA's
-        // workspace slot; then, for a split pair, the ticket and the fold.
-        const int wq = warp & 3;
-        const int row = wq * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        uint32_t esc = 0;
-        auto wg_sync = [&]() {   // the four epilogue warps meet (bounded)
-            __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&bar[kEpiSync]);
-            return warp_wait(&bar[kEpiSync], (esc++) & 1, dead);
-        };
-        int32_t r = 0;
-        for (int32_t pos = lo; pos < hi; ++r) {
-            const SSeg sg = s_segment(p, prefix, pos, hi);
-            if (sg.len == 0) break;
-            pos = sg.next;
-            if (!warp_wait(&bar[kSegDone + (r & 1)], (uint32_t)((r >> 1) & 1), dead)) break;
             pa::tc_fence_after();
-            const int32_t rows = sg.qlen * p.G;
-            const bool valid = row < rows;
-            const int32_t t_row = row / p.G;
-            const float* ml = row_ml + (r & 1) * 2 * kM;
-            const float M = ml[row], L = ml[kM + row];
+            float l_o;
+            if (!exchange(l, l_o)) break;
+            const float L = h == 0 ? l + l_o : l_o + l;   // the same sum in both warpgroups
+            const float M = m_used;
             const bool whole = sg.kt0 == 0 && sg.len == sg.nkt;
             const int32_t hq = sg.g * p.G + (row - t_row * p.G);
-            uint16_t* orow = p.out + ((int64_t)(sg.q0 + t_row) * p.H + hq) * kD;
+            uint16_t* orow = p.out + ((int64_t)(sg.q0 + t_row) * p.H + hq) * kD + h * 64;
             float* ps = nullptr;
             if (!whole) {
                 const int64_t c = blockIdx.x;
@@ -1348,9 +1310,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 ps = p.partials + slot * kSlotFloats;
             }
             const float inv = whole && L > 0.f ? 1.f / L : 1.f;
-            const uint32_t o_col = lane_base + kOCol + (uint32_t)(r & 1) * kD;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t o[32];
                 pa::tmem_ld32(o_col + c * 32, o);
                 pa::tmem_ld_wait();
@@ -1369,12 +1330,12 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(ps + (size_t)row * kD + c * 32 + e) =
+                        *reinterpret_cast<float4*>(ps + (size_t)row * kD + h * 64 + c * 32 + e) =
                             make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
                                         __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
                 }
             }
-            if (!whole && valid) {
+            if (!whole && valid && h == 0) {
                 ps[(size_t)kM * kD + row] = M;
                 ps[(size_t)kM * kD + kM + row] = L;
             }
@@ -1382,22 +1343,22 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             __syncwarp();
             if (lane == 0) pa::mbar_arrive(&bar[kOFree + (r & 1)]);
             if (whole) continue;
-            // Publish: the warpgroup barrier orders every thread's partial
-            // stores before thread 0's release; the ticket names the pair's last
-            // CTA and, for it, acquires every other CTA's partial.
-            if (!wg_sync()) break;
+            // Publish: the meeting orders every thread's partial stores before
+            // thread 0's release; the ticket names the pair's last CTA and, for
+            // it, acquires every other CTA's partial.
+            if (!all8()) break;
             // the CTAs holding the pair's first and last key tiles
             const int64_t t0 = (int64_t)sg.a + kPairUnits;
             const int64_t c_first = ((t0 + 1) * C - 1) / F;
             const int64_t c_last = ((t0 + sg.nkt) * C - 1) / F;
-            if (row == 0) {
+            if (row == 0 && h == 0) {
                 int32_t* ctr = p.counters + (int64_t)sg.i * p.Hkv + sg.g;
                 const int prev = pa::atomic_add_acq_rel_gpu(ctr, 1);
                 const int last = prev == (int)(c_last - c_first);
                 if (last) atomicExch(ctr, 0);
                 *last_flag = last;
             }
-            if (!wg_sync()) break;
+            if (!all8()) break;
             if (!*last_flag) continue;
             // The pair's last CTA folds every covering CTA's rows.  The first
             // covering CTA holds the pair in its first slot when the pair is its
@@ -1407,9 +1368,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
             auto slot_ptr = [&](int c) {
                 return p.partials + (c ? 2 * (c_first + c) : slot0) * kSlotFloats;
             };
-            // per row (thread = row): the common maximum and 1 / sum
-            float* fold = fold_ml;
-            {
+            // per row (warpgroup 0, thread = row): the common maximum and 1 / sum
+            if (h == 0) {
                 float Mx = -INFINITY;
                 for (int c = 0; c < ncov; ++c)
                     Mx = fmaxf(Mx, __ldcg(slot_ptr(c) + (size_t)kM * kD + row));
@@ -1420,16 +1380,16 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     Ls += pa::fast_exp2(__ldcg(q + (size_t)kM * kD + row) - Mxs) *
                           __ldcg(q + (size_t)kM * kD + kM + row);
                 }
-                fold[row] = Mxs;
-                fold[kM + row] = Ls > 0.f ? 1.f / Ls : 0.f;
+                fold_ml[row] = Mxs;
+                fold_ml[kM + row] = Ls > 0.f ? 1.f / Ls : 0.f;
             }
-            if (!wg_sync()) break;
-            // per row (warp wq: rows wq, wq + 4, ...; lane = 4 of the row's 128
-            // values): coalesced 512-byte reads, kFoldRows rows in flight per
-            // covering CTA
-            const int rows_valid = sg.qlen * p.G;
+            if (!all8()) break;
+            // per row (warp w8 of the eight: rows w8, w8 + 8, ...; lane = 4 of
+            // the row's 128 values): coalesced 512-byte reads, kFoldRows rows in
+            // flight per covering CTA
+            const int w8 = h * 4 + wq;
 #pragma unroll 1
-            for (int r0 = 0; r0 + wq < rows_valid; r0 += 4 * kFoldRows) {
+            for (int r0 = 0; r0 + w8 < rows; r0 += 8 * kFoldRows) {
                 float4 acc[kFoldRows];
 #pragma unroll
                 for (int k = 0; k < kFoldRows; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1440,14 +1400,14 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     float mc[kFoldRows];
 #pragma unroll
                     for (int k = 0; k < kFoldRows; ++k) {
-                        const int rr = min(r0 + 4 * k + wq, kM - 1);
+                        const int rr = min(r0 + 8 * k + w8, kM - 1);
                         v[k] = __ldcg(reinterpret_cast<const float4*>(q + (size_t)rr * kD) + lane);
                         mc[k] = __ldcg(q + (size_t)kM * kD + rr);
                     }
 #pragma unroll
                     for (int k = 0; k < kFoldRows; ++k) {
-                        const int rr = min(r0 + 4 * k + wq, kM - 1);
-                        const float f = pa::fast_exp2(mc[k] - fold[rr]) * fold[kM + rr];
+                        const int rr = min(r0 + 8 * k + w8, kM - 1);
+                        const float f = pa::fast_exp2(mc[k] - fold_ml[rr]) * fold_ml[kM + rr];
                         acc[k].x += f * v[k].x;
                         acc[k].y += f * v[k].y;
                         acc[k].z += f * v[k].z;
@@ -1456,8 +1416,8 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
 #pragma unroll
                 for (int k = 0; k < kFoldRows; ++k) {
-                    const int rr = r0 + 4 * k + wq;
-                    if (rr >= rows_valid) break;
+                    const int rr = r0 + 8 * k + w8;
+                    if (rr >= rows) break;
                     const int32_t tr = rr / p.G;
                     uint16_t* o = p.out + ((int64_t)(sg.q0 + tr) * p.H + sg.g * p.G + (rr - tr * p.G)) * kD;
                     uint2 x;
@@ -1466,8 +1426,10 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                     reinterpret_cast<uint2*>(o)[lane] = x;
                 }
             }
+            // the fold's reads of fold_ml done before a later fold rewrites it
+            if (!all8()) break;
         }
-        if (*dead && row == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
+        if (*dead && row == 0 && h == 0) pa::raise_error(p.err, PA_DEVERR_TIMEOUT);
     }
     pa::tc_fence_before();
     __syncthreads();
