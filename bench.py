@@ -569,6 +569,9 @@ def run_gpu(args):
     if args.sweep != "none" and not fp8 and args.workload == "llama13b":
         result["sweep"], result["launch_floor"] = run_sweep(args, dev, stream, sampler, peak,
                                                              peak_kind, local)
+    if args.multi_query == "on" and rank == 0 and not fp8 and args.workload == "llama13b":
+        torch.cuda.synchronize()
+        result["multi_query"] = multi_query_summary(measure_multi_query(args, with_cpu=False))
     if sampler:
         sampler.stop()
     if rank == 0:
@@ -1038,6 +1041,32 @@ def load_tensor_peak():
 
 
 def run_multi_query(args):
+    print(json.dumps(measure_multi_query(args, with_cpu=not args.no_cpu_baseline)))
+
+
+def multi_query_summary(mq):
+    """The figures of a measure_multi_query result that the decode line
+    carries: each kernel's rate, roofline fraction and time per launch."""
+    sv = mq["speculative_verification"]
+    return {
+        "chunked_prefill": {
+            "kernel": mq["roofline"]["kernel"], "value": mq["value"], "unit": mq["unit"],
+            "frac": mq["roofline"]["frac"], "peak": mq["roofline"]["peak"],
+            "us_per_launch": mq["roofline"]["avg_launch_us"],
+            "mma_sync_kernel": {k: mq["roofline"]["mma_sync_kernel"][k]
+                                for k in ("kernel", "value", "unit", "us_per_launch")},
+            "workload": mq["config"]["workload"]},
+        "speculative_verification": {
+            "kernel": "pa_multi_query_tc", "value": sv["value"], "unit": sv["unit"],
+            "frac": round(sv["pct_of_hbm_peak"] / 100.0, 4), "us_per_launch": sv["us_per_launch"],
+            "mma_sync_kernel": {k: sv["mma_sync_kernel"][k]
+                                for k in ("kernel", "value", "us_per_launch")},
+            "workload": sv["config"]},
+        "how": "bench.py --measure multi_query, run after the decode sweep in the same process",
+    }
+
+
+def measure_multi_query(args, with_cpu=True):
     """pa_multi_query on two shapes: a chunked prefill (4 sequences, a
     2048-token chunk each on top of 6144 cached tokens, 7B GQA 32 / 8 heads,
     bf16) timed against the tensor roofline, and speculative verification (the
@@ -1144,7 +1173,7 @@ def run_multi_query(args):
     # the oracle on the host cores: 256 query rows of the first prefill sequence (each over its
     # full causal context), same tables and cache contents
     cpu = None
-    if not args.no_cpu_baseline:
+    if with_cpu:
         import oracle
         oracle.build()
         threads = os.cpu_count() or 1
@@ -1165,7 +1194,7 @@ def run_multi_query(args):
                "kind": "oracle", "seconds": round(dt, 2),
                "sample": "%d query rows of one 2048-token prefill chunk (each over its %d+ "
                          "causal keys), fp64 C oracle" % (rows, q_off + 1)}
-    print(json.dumps({
+    return ({
         "metric": "multi-query paged attention: TFLOP/s (chunked prefill), KV GB/s "
                   "(speculative verification)",
         "cpu_baseline": cpu,
@@ -1205,7 +1234,7 @@ def run_multi_query(args):
         "gpu_launches": 4 * (reps + 3) + 8,
         "config": {"workload": "chunked prefill: 4 sequences x 2048-token chunk on 6144 cached "
                                "tokens, 32 / 8 heads of 128, bf16, block 16",
-                   "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}}))
+                   "causal_keys": int(keys), "us_per_launch": round(t_pf * 1e3, 2)}})
 
 
 def main():
@@ -1230,6 +1259,9 @@ def main():
                     help="seconds of untimed replays before each sweep entry's timed replays")
     ap.add_argument("--kv-format", choices=["native", "fp8", "int8"], default="native",
                     help="cache in the workload's 16-bit dtype, or E4M3 / INT8 codes + fp32 scales")
+    ap.add_argument("--multi-query", choices=["on", "off"], default="on",
+                    help="after the sweep, time the chunked prefill and speculative verification "
+                         "kernels too and add their figures to the line (llama13b runs only)")
     ap.add_argument("--measure", choices=["decode", "swap", "multi_query"], default="decode",
                     help="swap: device<->host block swap bandwidth; multi_query: chunked prefill "
                          "and speculative verification, instead of the decode step")
