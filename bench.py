@@ -572,6 +572,10 @@ def run_gpu(args):
     if args.multi_query == "on" and rank == 0 and not fp8 and args.workload == "llama13b":
         torch.cuda.synchronize()
         result["multi_query"] = multi_query_summary(measure_multi_query(args, with_cpu=False))
+    if args.kv8 == "on" and rank == 0 and world == 1 and not fp8 and args.workload == "llama13b":
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        result["kv8"] = {f: kv8_summary(f, args) for f in ("fp8", "int8")}
     if sampler:
         sampler.stop()
     if rank == 0:
@@ -1044,6 +1048,30 @@ def run_multi_query(args):
     print(json.dumps(measure_multi_query(args, with_cpu=not args.no_cpu_baseline)))
 
 
+def kv8_summary(fmt, args):
+    """The same llama13b decode step over an 8-bit cache (E4M3 or INT8 codes
+    and fp32 scales), timed by a child run of this bench (its own pre-roll,
+    clock record and traffic figure); the figures the decode line carries."""
+    steps = max(20, min(args.steps, 500))
+    cmd = [sys.executable, os.path.abspath(__file__), "--kv-format", fmt, "--sweep", "none",
+           "--multi-query", "off", "--kv8", "off", "--no-cpu-baseline",
+           "--steps", str(steps), "--warmup", str(max(3, args.warmup))]
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=900)
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    if r.returncode != 0 or not lines:
+        raise RuntimeError("the %s decode run failed:\n%s" % (fmt, r.stderr[-2000:]))
+    d = json.loads(lines[-1])
+    rf = d["roofline"]
+    return {"kernel": rf["kernel"], "value": d["value"], "unit": d["unit"],
+            "pct_of_hbm_peak": d["pct_of_hbm_peak"], "ms_per_step": d["ms_per_step"],
+            "steps": d["steps"],
+            "roofline": {k: rf.get(k) for k in ("achieved", "peak", "frac", "traffic",
+                                                "algorithmic_bytes_per_launch", "avg_launch_us")},
+            "e2e": {"value": d["e2e"]["value"], "unit": d["e2e"]["unit"]},
+            "clocks": d.get("clocks"), "config": d["config"],
+            "how": "bench.py --kv-format %s --sweep none --steps %d, a child process" % (fmt, steps)}
+
+
 def multi_query_summary(mq):
     """The figures of a measure_multi_query result that the decode line
     carries: each kernel's rate, roofline fraction and time per launch."""
@@ -1259,6 +1287,9 @@ def main():
                     help="seconds of untimed replays before each sweep entry's timed replays")
     ap.add_argument("--kv-format", choices=["native", "fp8", "int8"], default="native",
                     help="cache in the workload's 16-bit dtype, or E4M3 / INT8 codes + fp32 scales")
+    ap.add_argument("--kv8", choices=["on", "off"], default="on",
+                    help="after the 16-bit line, time the same decode step over FP8 and INT8 "
+                         "caches in child runs and add their figures (llama13b, one GPU)")
     ap.add_argument("--multi-query", choices=["on", "off"], default="on",
                     help="after the sweep, time the chunked prefill and speculative verification "
                          "kernels too and add their figures to the line (llama13b runs only)")
