@@ -94,3 +94,32 @@ def test_e2e_appends_fit_the_grown_pool():
         assert np.array_equal(plain.export(seqs, width)[0], alloc.export(seqs, width)[0]), name
         for _ in range(2 * extra + 1):
             alloc.append_batch(seqs)
+
+
+def test_multi_query_summary_keeps_each_kernels_figures():
+    """The decode line's multi-query object carries, for each shape, the
+    tcgen05 kernel's rate, fraction and time and the mma.sync kernel's beside
+    it, taken unchanged from the multi-query measurement."""
+    sys.path.insert(0, ROOT)
+    import bench
+    mq = {"value": 940.0, "unit": "TFLOP/s",
+          "roofline": {"kernel": "pa_multi_query_tc", "frac": 0.5, "peak": 1880.0,
+                       "avg_launch_us": 1020.0,
+                       "mma_sync_kernel": {"kernel": "pa_multi_query", "value": 220.0,
+                                           "unit": "TFLOP/s", "us_per_launch": 4300.0,
+                                           "note": "dropped"}},
+          "config": {"workload": "prefill shape"},
+          "speculative_verification": {"value": 4600.0, "unit": "GB/s", "pct_of_hbm_peak": 68.1,
+                                       "us_per_launch": 170.0, "config": "verify shape",
+                                       "mma_sync_kernel": {"kernel": "pa_multi_query",
+                                                           "value": 3400.0, "us_per_launch": 230.0,
+                                                           "pct_of_hbm_peak": 50.0}}}
+    s = bench.multi_query_summary(mq)
+    pf, sv = s["chunked_prefill"], s["speculative_verification"]
+    assert (pf["value"], pf["frac"], pf["us_per_launch"], pf["workload"]) == \
+        (940.0, 0.5, 1020.0, "prefill shape")
+    assert pf["mma_sync_kernel"] == {"kernel": "pa_multi_query", "value": 220.0,
+                                     "unit": "TFLOP/s", "us_per_launch": 4300.0}
+    assert (sv["value"], sv["frac"], sv["us_per_launch"], sv["workload"]) == \
+        (4600.0, 0.681, 170.0, "verify shape")
+    assert sv["mma_sync_kernel"]["us_per_launch"] == 230.0
