@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 3-D TMA tile prefetch global -> L2 (no shared memory written, nothing to
+// await; coordinates are bounds-checked like a load's).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Transposes an 8x8 matrix of 16-bit values held across the warp in the
 // ldmatrix fragment layout (lane l: row l/4, columns 2(l%4), 2(l%4)+1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {

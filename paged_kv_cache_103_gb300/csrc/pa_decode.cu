@@ -273,6 +273,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             const int32_t j = g_wbase + lane;
             g_went = j < p.max_blocks ? __ldg(trow + j) : -1;
             g_wnext = j + 32 < p.max_blocks ? __ldg(trow + j + 32) : -1;
+            // ... and the K / V blocks of this producer's first chunk (chunk
+            // c0 + prod of the guessed pair) are prefetched into L2, so that
+            // the real loads after the scan find them there; a wrong guess only
+            // costs the prefetch.  Block ids are checked as for a load.
+            // Only when CTAs average four chunks or more: with a chunk or two
+            // each, the real load follows the prefetch at once (measured slower).
+            const int32_t prod = warp - kConsumerWarps;
+            const int32_t cg = c0 + prod;
+            if (cg < nc && Wg >= 4 * Cg) {
+                const int bpc_g = kChunk >> rows_shift;
+                const int32_t j0 = (cg * kChunk) >> (31 - __clz(bs));
+                const int32_t kvh_g = ((lo_g - g_i * Hkv * nc) / nc) / p.subs;
+                for (int b = 0; b < bpc_g; ++b) {
+                    const int32_t e = __shfl_sync(0xffffffffu, g_went, (j0 - g_wbase + b) & 31);
+                    if (lane == 0 && e >= 0 && e < p.num_blocks) {
+                        pa::tma_prefetch_3d(&kmap, 0, e * bs, kvh_g * (int32_t)kHalves);
+                        pa::tma_prefetch_3d(&vmap, 0, e * bs, kvh_g * (int32_t)kHalves);
+                    }
+                }
+            }
         }
     }
 
