@@ -42,6 +42,11 @@
 //  * V rows past a context are zeroed in shared memory before use (unwritten
 //    slots may hold NaN); blocks past the table's used entries and out-of-pool
 //    ids load as zeros from outside the tensor map.  Every wait is bounded.
+//  * Launches in which every sequence's rows fit one tile (speculative
+//    verification: a few draft tokens times the group) run the split mode
+//    further down instead: one query tile per (sequence, KV head), the key
+//    tiles of all of them cut into equal shares over the CTAs, double-buffered
+//    S, both softmax warpgroups on every tile, partials folded across CTAs.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
