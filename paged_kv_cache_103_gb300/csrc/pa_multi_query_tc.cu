@@ -766,7 +766,7 @@ constexpr uint32_t kOCol = 2 * kSBufCols;
 constexpr uint32_t kSOffQ = 0;                                   // two Q stages
 constexpr uint32_t kSOffK = kSOffQ + 2 * kTileBytes;
 constexpr uint32_t kSOffV = kSOffK + kKStages * kTileBytes;
-constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // (m, l) and fold row values
+constexpr uint32_t kSOffRow = kSOffV + kVStages * kTileBytes;   // warpgroup exchanges, fold values
 constexpr uint32_t kSOffBar = kSOffRow + 6 * kM * 4;
 constexpr uint32_t kSOffMisc = kSOffBar + kNumBars * 8;   // TMEM base, dead flag, flags per warpgroup
 constexpr uint32_t kSOffPrefix = kSOffMisc + 32;
