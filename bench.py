@@ -569,13 +569,23 @@ def run_gpu(args):
     if args.sweep != "none" and not fp8 and args.workload == "llama13b":
         result["sweep"], result["launch_floor"] = run_sweep(args, dev, stream, sampler, peak,
                                                              peak_kind, local)
+    # The extras below add figures to the line; a failure in one is recorded in
+    # its own object and never costs the headline.
     if args.multi_query == "on" and rank == 0 and not fp8 and args.workload == "llama13b":
         torch.cuda.synchronize()
-        result["multi_query"] = multi_query_summary(measure_multi_query(args, with_cpu=False))
+        try:
+            result["multi_query"] = multi_query_summary(measure_multi_query(args, with_cpu=False))
+        except Exception as e:   # noqa: BLE001 -- reported, not hidden
+            result["multi_query"] = {"error": "%s: %s" % (type(e).__name__, str(e)[:500])}
     if args.kv8 == "on" and rank == 0 and world == 1 and not fp8 and args.workload == "llama13b":
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        result["kv8"] = {f: kv8_summary(f, args) for f in ("fp8", "int8")}
+        result["kv8"] = {}
+        for f in ("fp8", "int8"):
+            try:
+                result["kv8"][f] = kv8_summary(f, args)
+            except Exception as e:   # noqa: BLE001 -- reported, not hidden
+                result["kv8"][f] = {"error": "%s: %s" % (type(e).__name__, str(e)[:500])}
     if sampler:
         sampler.stop()
     if rank == 0:
