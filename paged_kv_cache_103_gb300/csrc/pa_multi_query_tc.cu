@@ -1038,8 +1038,11 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
             };
             int32_t r = 0;
-            for (int32_t pos = lo; pos < hi && alive; ++r) {
-                const SSeg sg = s_segment(p, prefix, pos, hi);
+            // the CTA's shares, grid-stride (C <= gridDim.x: one share)
+            for (int32_t c = blockIdx.x; c < C && alive; c += gridDim.x) {
+                const int32_t hi_c = s_begin(c + 1, F, C);
+                for (int32_t pos = s_begin(c, F, C); pos < hi_c && alive; ++r) {
+                const SSeg sg = s_segment(p, prefix, pos, hi_c);
                 if (sg.len == 0) break;
                 pos = sg.next;
                 const bool residual =
@@ -1093,6 +1096,7 @@ multi_query_tc_split_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
                 if (!alive) break;
                 pa::umma_commit(&bar[qs ? kQEmpty1 : kQEmpty]);
+                }
             }
             pa::umma_commit(&bar[kDrain]);
             pa::mbar_wait(&bar[kDrain], 0, kWaitLimitNs);
